@@ -1,0 +1,231 @@
+"""The CSA2 hot path, step by step, as plain numpy (oracle side).
+
+Pages followed (titles and sections):
+
+[KN]  "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression"
+      (knowledge note): "CSA2: share cache, refresh selection only when
+      needed" (mode table), "Hierarchical Sparse Indexer: make later searches
+      bounded", "FP4 main KV: trade precision for bytes, not for a new GEMM",
+      "Putting It Together" (steps 5-8 of the request trace).
+[ID]  "Inside DeepSeek V4.1 Flash: CED, CSA2 and the 890-Byte KV Cache":
+      "CSA2: reuse memory and reuse selection independently", "Hierarchical
+      indexing bounds later searches, not every search", "Reconstructing the
+      890-byte cache budget".
+[MT]  "DeepSeek-V4.1-Flash：把 KV 缓存压缩从“算法点”推进为“部署系统”":
+      section "3. FP4 主 KV" (quantised after RoPE, dequantised before
+      attention, SWA kept in FP8).
+[EB]  "The 890-Byte Token - DeepSeek-V4.1 Flash's Elegant KV Cache
+      Optimizations": "FP4 main KV cache" (range after normalisation),
+      "Hierarchical Sparse Indexer".
+
+Readings of points the pages leave open (each is also listed in the design doc):
+
+* RoPE rotates the last ``rope_dim`` channels in interleaved pairs
+  (2i, 2i+1) with angle p * theta**(-2i/rope_dim); the cos/sin table is an
+  fp32 input; each output takes two fp32 products and one fp32 add/sub, each
+  rounded once (no fused multiply-add).
+* FP4 scale = E4M3(RNE(amax / 6)) with a correctly rounded fp32 division; a
+  zero scale gives all-zero codes; codes = E2M1(RNE(y / scale)); element 2j
+  in the low nibble of byte j.
+* Indexer score s_t = sum_h w_h * max(0, q_h . k_t) over E4M3 operands, no
+  extra constant factor.
+* Ranking order for top-k and for the pool: larger score first, lower index
+  on equal scores.  The pool keeps min(2048, ceil(N/8)) blocks of 8
+  positions ranked by block maximum.  Outputs are sorted ascending.
+* Attention: one softmax over the selected global rows followed by the SWA
+  rows (no de-duplication), K = V = the dequantised row, logit scale
+  1/sqrt(D) unless given.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from .formats import (e2m1_decode, e2m1_encode, e4m3_decode, e4m3_encode)
+
+GROUP = 16          # channels per E4M3 scale of the main-KV format
+BLOCK = 8           # positions per pool block
+POOL_BLOCKS = 2048  # pool capacity in blocks
+
+
+# ---------------------------------------------------------------- step 1: RoPE
+def rope_rotate(x, pos, cos_tab, sin_tab, rope_dim):
+    """Rotate the last ``rope_dim`` channels of fp32 rows ``x`` [n, D] at positions ``pos``.
+
+    [KN] "FP4 main KV": the cache is quantised after RoPE; [MT] "3. FP4 主 KV".
+    Pair i is (D-R+2i, D-R+2i+1); with (c, s) = table[pos, i]:
+    y0 = x0*c - x1*s,  y1 = x0*s + x1*c  (fp32, one rounding per operation).
+    Pinned: identity at position 0, exact rotation of unit vectors, norm kept
+    within fp32 rounding, agreement with complex multiplication in fp64.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    y = x.copy()
+    if rope_dim == 0:
+        return y
+    d = x.shape[-1]
+    pos = np.asarray(pos, dtype=np.int64)
+    c = np.asarray(cos_tab, dtype=np.float32)[pos]
+    s = np.asarray(sin_tab, dtype=np.float32)[pos]
+    x0 = x[:, d - rope_dim::2]
+    x1 = x[:, d - rope_dim + 1::2]
+    y[:, d - rope_dim::2] = (x0 * c) - (x1 * s)
+    y[:, d - rope_dim + 1::2] = (x0 * s) + (x1 * c)
+    return y
+
+
+# ------------------------------------------------------- step 1: FP4 quantise
+def quantize_fp4(y):
+    """Post-RoPE fp32 rows [n, D] -> (codes uint8 [n, D/2], scales uint8 [n, D/16]).
+
+    [KN] "FP4 main KV": E2M1 values, one E4M3 scale per 16 channels, no second
+    global scale; [ID] "Reconstructing the 890-byte cache budget": 512 x 4/8 +
+    512/16 bytes per entry.
+    For each group of 16 channels: amax = max|y|; scale code = E4M3(amax/6);
+    s = value of that code; codes = E2M1(y/s), or all zero when s == 0.
+    Pinned: zero groups, exact power-of-two groups, saturation, the per-element
+    error bound of the E2M1 grid, byte counts of the pages.
+    """
+    y = np.asarray(y, dtype=np.float32)
+    n, d = y.shape
+    g = y.reshape(n, d // GROUP, GROUP)
+    amax = np.max(np.abs(g), axis=-1)
+    scale_code = e4m3_encode(amax / np.float32(6.0))
+    s = e4m3_decode(scale_code).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = g / s[..., None]
+    codes = e2m1_encode(np.where(s[..., None] == 0, np.float32(0.0), q))
+    codes = np.where(s[..., None] == 0, np.uint8(0), codes).reshape(n, d)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, scale_code.astype(np.uint8)
+
+
+def dequantize_fp4(codes, scales, dim):
+    """(codes [n, D/2], scales [n, >= D/16]) -> float64 rows [n, D].
+
+    [KN] "Putting It Together", step 8: FP4 blocks are dequantised when
+    attention needs them.  x = E2M1(code) * E4M3(scale of the channel's group).
+    """
+    codes = np.asarray(codes, dtype=np.uint8)[:, : dim // 2]
+    lo = e2m1_decode(codes & 0xF)
+    hi = e2m1_decode(codes >> 4)
+    v = np.empty((codes.shape[0], dim), dtype=np.float64)
+    v[:, 0::2] = lo
+    v[:, 1::2] = hi
+    s = e4m3_decode(np.asarray(scales, dtype=np.uint8)[:, : dim // GROUP])
+    return v * np.repeat(s, GROUP, axis=1)
+
+
+def quant_append_rows(kv, pos, cos_tab, sin_tab, rope_dim):
+    """Pre-RoPE fp32 rows and their positions -> the bytes appended to the cache."""
+    return quantize_fp4(rope_rotate(kv, pos, cos_tab, sin_tab, rope_dim))
+
+
+def fp8_cast(x):
+    """fp32 -> E4M3 codes (SWA rows, indexer keys and queries)."""
+    return e4m3_encode(x)
+
+
+# -------------------------------------------------------- step 2: indexer score
+def indexer_scores(q_codes, w, k_codes):
+    """Lightning-indexer scores of one query against key rows (fp64).
+
+    [KN] "Hierarchical Sparse Indexer"; [ID] "Hierarchical indexing bounds
+    later searches".  s_t = sum_h w_h * max(0, sum_d q[h,d] k[t,d]) with
+    q, k decoded from E4M3.  The inner products are exact in fp64 (products
+    of two E4M3 values have at most 8 significant bits and 128 of them sum
+    well inside 53 bits).
+    Pinned: with one head and w = 1 it equals ReLU(q.k) computed in exact
+    rational arithmetic.
+    """
+    q = e4m3_decode(q_codes).reshape(len(w), -1)
+    k = e4m3_decode(k_codes).reshape(-1, q.shape[1])
+    dots = k @ q.T
+    return np.maximum(dots, 0.0) @ np.asarray(w, dtype=np.float64)
+
+
+def block_maxima(scores):
+    """Per 8-position block: max score over the positions that exist."""
+    scores = np.asarray(scores, dtype=np.float64)
+    n = len(scores)
+    nb = -(-n // BLOCK)
+    pad = np.full(nb * BLOCK, -np.inf)
+    pad[:n] = scores
+    return pad.reshape(nb, BLOCK).max(axis=1)
+
+
+# ------------------------------------------------------------ step 3: selection
+def topk(scores, k, ids=None):
+    """The k best ids by (score descending, id ascending), returned ascending."""
+    scores = np.asarray(scores, dtype=np.float64)
+    ids = np.arange(len(scores)) if ids is None else np.asarray(ids)
+    k = min(k, len(scores))
+    if k <= 0:
+        return np.zeros(0, dtype=np.int64)
+    order = np.lexsort((ids, -scores))
+    return np.sort(ids[order[:k]]).astype(np.int64)
+
+
+def full_select(scores, k, pool_blocks=POOL_BLOCKS):
+    """Full layer: top-k positions and the block pool.
+
+    [KN] "Hierarchical Sparse Indexer": the first Full indexer scores all
+    positions and block maxima select a shared pool; [ID] "Hierarchical
+    indexing": up to 2,048 blocks of eight positions, at most 16,384
+    candidates.  Returns (idx ascending, pool block ids ascending).
+    """
+    n = len(scores)
+    idx = topk(scores, k)
+    bm = block_maxima(scores)
+    pool = topk(bm, min(pool_blocks, len(bm)))
+    return idx, pool
+
+
+def pool_positions(pool, n):
+    """Positions covered by the pool blocks that are < n, ascending."""
+    pool = np.asarray(pool, dtype=np.int64)
+    pos = (pool[:, None] * BLOCK + np.arange(BLOCK)[None, :]).reshape(-1)
+    return pos[pos < n]
+
+
+def reindex_select(q_codes, w, k_codes_of, pool, n, k):
+    """Reindex layer: own indexer query over the pool's positions only.
+
+    [KN] "CSA2" mode table (Reindex reuses main KV and indexer K, computes a
+    new indexer Q and a fresh top-k) and "Hierarchical Sparse Indexer" (later
+    Reindex layers score only the pool).  ``k_codes_of(positions)`` returns
+    the E4M3 indexer-key rows of those positions.
+    """
+    pos = pool_positions(pool, n)
+    s = indexer_scores(q_codes, w, k_codes_of(pos))
+    return topk(s, k, ids=pos)
+
+
+# --------------------------------------------------- steps 4-5: attention
+def sparse_attention(q, rows, scale=None):
+    """One softmax over ``rows`` (selected global rows then SWA rows), K = V = rows.
+
+    [KN] "CSA2" (every mode computes its own Q and SWA path) and "Putting It
+    Together" step 7 (sparse attention with local SWA); [ID] "CSA2: reuse
+    memory and reuse selection independently" (the query attends to the
+    selected entries together with the local window).
+    q: float64 [H, D]; rows: float64 [n, D].  Output float64 [H, D]; n == 0
+    gives zeros.  Pinned: equals dense attention when every row is selected;
+    one row gives that row; equal logits give the mean; invariant to adding a
+    constant to every logit.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    rows = np.asarray(rows, dtype=np.float64)
+    if scale is None or scale <= 0:
+        scale = 1.0 / math.sqrt(q.shape[1])
+    if rows.shape[0] == 0:
+        return np.zeros_like(q)
+    logits = scale * (q @ rows.T)
+    m = logits.max(axis=1, keepdims=True)
+    p = np.exp(logits - m)
+    return (p @ rows) / p.sum(axis=1, keepdims=True)
+
+
+def swa_rows_decode(swa_codes):
+    """FP8 SWA rows -> float64 (plain per-element E4M3, no scale)."""
+    return e4m3_decode(swa_codes)
