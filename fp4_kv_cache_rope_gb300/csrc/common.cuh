@@ -1,0 +1,257 @@
+// Shared device-side building blocks of the CSA2 kernels (sm_103a):
+// PTX wrappers for mbarriers, TMA / bulk copies, tcgen05 MMA and tensor
+// memory, bounded waits, and the workspace layout shared by the launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/csa2.h"
+
+namespace csa2 {
+
+constexpr int kGroup = 16;                  // channels per E4M3 scale
+constexpr int kBlock = CSA2_BLOCK;          // positions per pool block
+constexpr int kPoolBlocks = CSA2_POOL_BLOCKS;
+constexpr int kMaxTopk = CSA2_MAX_TOPK;
+constexpr int kPoolPositions = kPoolBlocks * kBlock;   // 16,384 candidates
+constexpr int kMaxSplits = 16;              // attention split-K limit
+constexpr int kSplitSlots = 160;            // CTA budget used to size split-K partials
+constexpr uint64_t kWaitNs = 2000000000ull; // bounded on-chip waits give up after ~2 s
+
+// ------------------------------------------------------------------ workspace
+// The workspace is carved into 256-byte aligned regions in this order.
+struct WsLayout {
+  size_t status;       // uint32 status word
+  size_t row_len;      // int32 [max_rows]  visible length per query row
+  size_t tile_prefix;  // int32 [max_rows+1] prefix sum of 128-position tiles
+  size_t scores;       // fp32 [max_rows, score_stride]
+  size_t blockmax;     // fp32 [max_rows, bm_stride]
+  size_t cand;         // fp32 [max_rows, kPoolPositions] Reindex candidate scores
+  size_t part_o;       // fp32 [kslots, heads_pad, D] split-K partial outputs
+  size_t part_ml;      // fp32 [kslots, heads_pad, 2] split-K (max, sum)
+  size_t total;
+  int64_t score_stride, bm_stride;
+  int64_t slots;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(int64_t max_len, int64_t max_rows, int64_t heads, int64_t dim) {
+  WsLayout L{};
+  L.score_stride = (max_len + 127) / 128 * 128;
+  L.bm_stride = (L.score_stride / kBlock + 31) / 32 * 32;
+  L.slots = max_rows > kSplitSlots ? max_rows : kSplitSlots;
+  const int64_t hp = 64;
+  (void)heads;
+  size_t off = 0;
+  L.status = off; off = align256(off + 256);
+  L.row_len = off; off = align256(off + 4 * max_rows);
+  L.tile_prefix = off; off = align256(off + 4 * (max_rows + 1));
+  L.scores = off; off = align256(off + 4 * (size_t)max_rows * L.score_stride);
+  L.blockmax = off; off = align256(off + 4 * (size_t)max_rows * L.bm_stride);
+  L.cand = off; off = align256(off + 4 * (size_t)max_rows * kPoolPositions);
+  L.part_o = off; off = align256(off + 4 * (size_t)L.slots * hp * dim);
+  L.part_ml = off; off = align256(off + 4 * (size_t)L.slots * hp * 2);
+  L.total = off;
+  return L;
+}
+
+// ------------------------------------------------------------ device helpers
+__device__ __forceinline__ void set_status(uint32_t* st, uint32_t bits) {
+  if (st) atomicOr(st, bits);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Physical cache row of (sequence b, position t); -1 when the page id is bad.
+struct RowMap {
+  const int32_t* page_table;
+  int32_t page_size, max_pages_per_seq, max_len, num_pages;
+  __device__ __forceinline__ int64_t row(int b, int64_t t) const {
+    if (page_size == 0) return (int64_t)b * max_len + t;
+    int64_t pg = t / page_size;
+    int32_t phys = page_table[(int64_t)b * max_pages_per_seq + pg];
+    if (phys < 0 || phys >= num_pages) return -1;
+    return (int64_t)phys * page_size + (t - pg * page_size);
+  }
+};
+
+// ------------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase with the given parity to complete.  Gives up after
+// kWaitNs or when *abort is set by another thread; returns false then and the
+// caller records CSA2_DEV_TIMEOUT and winds down.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kWaitNs) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ async copies
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, FP8 E4M3 operands, fp32 accumulate.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, f16 operands, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+// Arrives on `bar` once all previously issued MMAs of this thread completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns; lane i of the warp reads TMEM lane
+// (base lane + i).  Values are valid only after tmem_ld_wait().
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// Keeps the compiler from moving uses of r above the preceding wait.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// Shared-memory matrix descriptor of tcgen05 (K-major or MN-major canonical
+// layouts).  swizzle: 0 none, 2 = 128 B, 4 = 64 B, 6 = 32 B.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t swizzle) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version of sm_100-class MMAs
+  d |= (uint64_t)(swizzle & 7) << 61;
+  return d;
+}
+
+// Instruction descriptor: fp32 accumulator, operand formats a/b, majorness,
+// M and N.  kind::f16: 0 = f16, 1 = bf16.  kind::f8f6f4: 0 = E4M3.
+__host__ __device__ constexpr uint32_t instr_desc(uint32_t afmt, uint32_t bfmt, bool a_mn,
+                                                  bool b_mn, int m, int n) {
+  return (1u << 4) | (afmt << 7) | (bfmt << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// Order-preserving map of fp32 onto uint32 (larger float -> larger key);
+// -0.0 is mapped like +0.0.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ------------------------------------------------------------ launchers
+struct IndexLaunch;  // defined in indexer.cu
+}  // namespace csa2

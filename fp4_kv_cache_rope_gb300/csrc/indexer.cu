@@ -1,0 +1,484 @@
+// Step 2 of the path: lightning-indexer scores on the 5th-generation tensor
+// cores.
+//
+//   s_t = sum_h w_h * max(0, q_h . k_t)
+//
+// over E4M3 indexer keys k_t (di channels) and E4M3 queries q_h.  A Full layer
+// scores every visible position and also emits per-8-position block maxima;
+// a Reindex layer scores only the positions of the pool's blocks.  Pages:
+// "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression" knowledge
+// note, section "Hierarchical Sparse Indexer: make later searches bounded"
+// (the first Full indexer scans all positions; block maxima select a pool of
+// at most 2,048 blocks of 8 positions; later Reindex layers score only the
+// pool); "Inside DeepSeek V4.1 Flash: CED, CSA2 and the 890-Byte KV Cache",
+// section "Hierarchical indexing bounds later searches, not every search".
+//
+// Kernel shape (one persistent CTA per SM, 6 warps):
+//   warp 0   TMA producer: 128 key rows per stage (one 128-row box, or one box
+//            per page, or one 8-row box per pool block) into an 8-deep ring,
+//            plus the row's query block [Hi x di] into a double buffer;
+//   warp 1   MMA issuer: D[128 positions x Hp heads] = K_tile x Q^T with
+//            tcgen05.mma kind::f8f6f4 (M = 128, N = Hp, K = 32 per
+//            instruction), accumulators double-buffered in tensor memory;
+//   warps 2-5  epilogue: one thread per position reads its Hp accumulators
+//            (tcgen05.ld 32x32b), applies ReLU and the head weights, writes
+//            the fp32 score and, for Full layers, the block maximum.
+// The decode indexer reads 128 bytes of key per position and does 2*Hp*di
+// flops on them (128 flop/byte at Hp = 64): it is HBM bound on GB300.
+#include "launch.h"
+
+namespace csa2 {
+
+struct IndexerParams {
+  int32_t mode;  // 0 = Full, 1 = pool positions
+  int32_t n_rows, tq, hi, batch;
+  const int32_t* batch_ids;
+  const int32_t* q_pos;
+  const int32_t* seq_len;
+  const int32_t* pool_blocks;
+  const int32_t* pool_cnt;
+  const float* w;
+  RowMap map;
+  int32_t rows_per_load;  // Full mode box height (128 or the page size)
+  int32_t* row_len;
+  int32_t* tile_prefix;
+  float* scores;
+  int64_t score_stride;
+  float* blockmax;
+  int64_t bm_stride;
+  float* cand;
+  uint32_t* status;
+};
+
+__device__ __forceinline__ int row_seq(const IndexerParams& p, int row) {
+  const int bi = row / p.tq;
+  return p.batch_ids ? p.batch_ids[bi] : bi;
+}
+
+// Visible length and 128-wide tile count of every query row, then the prefix
+// sum of tile counts (one block of 1024 threads).
+__global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerParams p) {
+  __shared__ int warp_tot[32];
+  __shared__ int carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int base = 0; base < p.n_rows; base += 1024) {
+    const int row = base + threadIdx.x;
+    int tiles = 0;
+    if (row < p.n_rows) {
+      const int b = row_seq(p, row);
+      const int tq = row % p.tq;
+      int len = 0;
+      if (b >= 0 && b < p.batch) {
+        len = p.seq_len[b];
+        if (p.q_pos) {
+          const int lim = p.q_pos[(int64_t)b * p.tq + tq] + 1;
+          len = lim < len ? lim : len;
+        }
+        len = len < 0 ? 0 : (len > p.map.max_len ? p.map.max_len : len);
+      }
+      p.row_len[row] = len;
+      if (p.mode == 0) {
+        tiles = (len + 127) / 128;
+      } else {
+        int pc = (b >= 0 && b < p.batch) ? p.pool_cnt[(int64_t)b * p.tq + tq] : 0;
+        pc = pc < 0 ? 0 : (pc > kPoolBlocks ? kPoolBlocks : pc);
+        tiles = (pc + 15) / 16;
+      }
+    }
+    // block-wide inclusive scan of tiles
+    int v = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int t = warp_tot[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += u;
+      }
+      warp_tot[lane] = t;
+    }
+    __syncthreads();
+    const int incl = v + (warp > 0 ? warp_tot[warp - 1] : 0) + carry;
+    if (row < p.n_rows) p.tile_prefix[row + 1] = incl;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.tile_prefix[0] = 0;
+}
+
+template <int HP, int DI>
+struct IdxCfg {
+  static constexpr int kTile = 128;
+  static constexpr int kStageBytes = kTile * DI;
+  static constexpr int kStages = 8;
+  static constexpr int kQBytes = HP * DI;
+  static constexpr int kSwizzle = DI == 128 ? 2 : (DI == 64 ? 4 : 6);
+  static constexpr uint32_t kSbo = 8 * DI;
+  static constexpr int kKSteps = DI / 32;
+  static constexpr int kAccCols = 2 * HP < 32 ? 32 : 2 * HP;
+  static constexpr int kTmemCols = kAccCols <= 32 ? 32 : (kAccCols <= 64 ? 64 : (kAccCols <= 128 ? 128 : 256));
+  static constexpr int kBarOff = kStages * kStageBytes + 2 * kQBytes;
+  static constexpr int kSmem = kBarOff + 256;
+};
+
+// First row whose tile range contains tile t (tile_prefix is non-decreasing).
+__device__ __forceinline__ int find_row(const int32_t* prefix, int n_rows, int t) {
+  int lo = 0, hi = n_rows - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int HP, int DI>
+__global__ void __launch_bounds__(192, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                   IndexerParams p) {
+  using C = IdxCfg<HP, DI>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* stages = smem;
+  uint8_t* qbuf = smem + C::kStages * C::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* full = bars;                       // [kStages]
+  uint64_t* empty = bars + C::kStages;         // [kStages]
+  uint64_t* qfull = bars + 2 * C::kStages;     // [2]
+  uint64_t* qempty = qfull + 2;                // [2]
+  uint64_t* tfull = qempty + 2;                // [2]
+  uint64_t* tempty = tfull + 2;                // [2]
+  uint64_t* drain = tempty + 2;                // [1]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(drain + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1) + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled layouts need 1 KB alignment
+    if (threadIdx.x == 0) set_status(p.status, CSA2_DEV_BAD_ALIGN);
+    return;
+  }
+  const int total = p.tile_prefix[p.n_rows];
+  const int t_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
+  const int t_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(qfull + s, 1);
+      mbar_init(qempty + s, 1);
+      mbar_init(tfull + s, 1);
+      mbar_init(tempty + s, 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  // Zero both query buffers: rows hi..HP-1 stay zero (padded heads).
+  for (int i = threadIdx.x; i < 2 * C::kQBytes / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
+  fence_async_smem();
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool issued_mma = false;
+
+  if (t_begin < t_end) {
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      int row = find_row(p.tile_prefix, p.n_rows, t_begin);
+      int cur = -1, qn = 0, stage = 0;
+      uint32_t phase = 0;
+      for (int t = t_begin; t < t_end; ++t) {
+        while (t >= p.tile_prefix[row + 1]) ++row;
+        const int b = row_seq(p, row);
+        const int tq = row % p.tq;
+        if (row != cur) {
+          const int qs = qn & 1;
+          if (!mbar_wait(qempty + qs, ((qn >> 1) & 1) ^ 1, abort_flag)) break;
+          mbar_arrive_expect_tx(qfull + qs, (uint32_t)(p.hi * DI));
+          tma_load_2d(qbuf + qs * C::kQBytes, &tm_q, 0, (int)(((int64_t)b * p.tq + tq) * p.hi),
+                      qfull + qs);
+          cur = row;
+          ++qn;
+        }
+        if (!mbar_wait(empty + stage, phase ^ 1, abort_flag)) break;
+        const int j = t - p.tile_prefix[row];
+        const int len = p.row_len[row];
+        uint8_t* dst = stages + stage * C::kStageBytes;
+        uint32_t bytes = 0;
+        if (p.mode == 0) {
+          const int64_t t0 = (int64_t)j * 128;
+          if (p.map.page_size == 0) {
+            bytes = 128 * DI;
+            mbar_arrive_expect_tx(full + stage, bytes);
+            tma_load_2d(dst, &tm_k, 0, (int)((int64_t)b * p.map.max_len + t0), full + stage);
+          } else {
+            const int rpl = p.rows_per_load;
+            int nload = 0;
+            int64_t src_rows[16];
+            for (int u = 0; u < 128 / rpl; ++u) {
+              const int64_t pos = t0 + (int64_t)u * rpl;
+              src_rows[u] = -1;
+              if (pos < len) {
+                const int64_t r = p.map.row(b, pos);
+                if (r < 0) set_status(p.status, CSA2_DEV_BAD_PAGE);
+                else { src_rows[u] = r; ++nload; }
+              }
+            }
+            bytes = (uint32_t)(nload * rpl * DI);
+            mbar_arrive_expect_tx(full + stage, bytes);
+            for (int u = 0; u < 128 / rpl; ++u)
+              if (src_rows[u] >= 0)
+                tma_load_2d(dst + u * rpl * DI, &tm_k, 0, (int)src_rows[u], full + stage);
+          }
+        } else {
+          int pc = p.pool_cnt[(int64_t)b * p.tq + tq];
+          pc = pc < 0 ? 0 : (pc > kPoolBlocks ? kPoolBlocks : pc);
+          const int32_t* pool = p.pool_blocks + ((int64_t)b * p.tq + tq) * kPoolBlocks;
+          int64_t src_rows[16];
+          int nload = 0;
+          for (int e = 0; e < 16; ++e) {
+            const int pi = j * 16 + e;
+            src_rows[e] = -1;
+            if (pi < pc) {
+              const int blk = pool[pi];
+              if (blk < 0 || (int64_t)blk * kBlock >= len) {
+                set_status(p.status, CSA2_DEV_BAD_POOL);
+              } else {
+                const int64_t r = p.map.row(b, (int64_t)blk * kBlock);
+                if (r < 0) set_status(p.status, CSA2_DEV_BAD_PAGE);
+                else { src_rows[e] = r; ++nload; }
+              }
+            }
+          }
+          bytes = (uint32_t)(nload * kBlock * DI);
+          mbar_arrive_expect_tx(full + stage, bytes);
+          for (int e = 0; e < 16; ++e)
+            if (src_rows[e] >= 0)
+              tma_load_2d(dst + e * kBlock * DI, &tm_k, 0, (int)src_rows[e], full + stage);
+        }
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // --------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = instr_desc(0, 0, false, false, 128, HP);
+      int row = find_row(p.tile_prefix, p.n_rows, t_begin);
+      int cur = -1, qn = 0, stage = 0, acc = 0;
+      uint32_t phase = 0, aphase = 0;
+      const uint32_t st_base = smem_u32(stages), q_base = smem_u32(qbuf);
+      for (int t = t_begin; t < t_end; ++t) {
+        while (t >= p.tile_prefix[row + 1]) ++row;
+        if (row != cur) {
+          if (cur >= 0) mma_commit(qempty + ((qn - 1) & 1));
+          if (!mbar_wait(qfull + (qn & 1), (qn >> 1) & 1, abort_flag)) break;
+          cur = row;
+          ++qn;
+        }
+        const int qs = (qn - 1) & 1;
+        if (!mbar_wait(full + stage, phase, abort_flag)) break;
+        if (!mbar_wait(tempty + acc, aphase ^ 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t a0 = st_base + stage * C::kStageBytes;
+        const uint32_t b0 = q_base + qs * C::kQBytes;
+#pragma unroll
+        for (int kk = 0; kk < C::kKSteps; ++kk) {
+          mma_f8(tmem + acc * HP, smem_desc(a0 + kk * 32, 16, C::kSbo, C::kSwizzle),
+                 smem_desc(b0 + kk * 32, 16, C::kSbo, C::kSwizzle), idesc, kk > 0 ? 1u : 0u);
+        }
+        issued_mma = true;
+        mma_commit(empty + stage);
+        mma_commit(tfull + acc);
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        if (++acc == 2) { acc = 0; aphase ^= 1; }
+      }
+    } else if (warp >= 2) {
+      // ----------------------------------------------------------- epilogue
+      const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+      int row = find_row(p.tile_prefix, p.n_rows, t_begin);
+      int cur = -1, acc = 0;
+      uint32_t aphase = 0;
+      float wv[HP];
+      for (int t = t_begin; t < t_end; ++t) {
+        while (t >= p.tile_prefix[row + 1]) ++row;
+        const int b = row_seq(p, row);
+        const int tq = row % p.tq;
+        if (row != cur) {
+          const float* wr = p.w + ((int64_t)b * p.tq + tq) * p.hi;
+#pragma unroll
+          for (int h = 0; h < HP; ++h) wv[h] = h < p.hi ? __ldg(wr + h) : 0.0f;
+          cur = row;
+        }
+        if (!mbar_wait(tfull + acc, aphase, abort_flag)) break;
+        tc_fence_after();
+        uint32_t r[HP];
+#pragma unroll
+        for (int c = 0; c < HP; c += 16) {
+          uint32_t (&rr)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[c]);
+          tmem_ld16(tmem + acc * HP + c + ((uint32_t)(32 * quad) << 16), rr);
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < HP; c += 16) reg_fence(*reinterpret_cast<uint32_t(*)[16]>(&r[c]));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty + acc);
+        float s = 0.0f;
+#pragma unroll
+        for (int h = 0; h < HP; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(r[h]), 0.0f), s);
+        const int j = t - p.tile_prefix[row];
+        const int len = p.row_len[row];
+        const int local = 32 * quad + lane;
+        if (p.mode == 0) {
+          const int64_t pos = (int64_t)j * 128 + local;
+          const bool valid = pos < len;
+          if (valid) p.scores[(int64_t)row * p.score_stride + pos] = s;
+          float m = valid ? s : -INFINITY;
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          if ((lane & 7) == 0 && valid) p.blockmax[(int64_t)row * p.bm_stride + pos / kBlock] = m;
+        } else {
+          const int c = j * 128 + local;
+          p.cand[(int64_t)row * kPoolPositions + c] = s;
+        }
+        if (++acc == 2) { acc = 0; aphase ^= 1; }
+      }
+    }
+  }
+  __syncwarp();
+  if (warp == 1) {
+    if (lane == 0 && issued_mma) {  // let every issued MMA land before freeing TMEM
+      mma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never);
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+  if (threadIdx.x == 0 && *abort_flag) set_status(p.status, CSA2_DEV_TIMEOUT);
+}
+
+// Host side ---------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D byte tensor [rows, width] with a row stride, box [box_rows, width].
+static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int width, int64_t stride,
+                     int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)stride};
+  cuuint32_t box[2] = {(cuuint32_t)width, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUtensorMapSwizzle sw = width == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : width == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                        : CU_TENSOR_MAP_SWIZZLE_32B;
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int HP, int DI>
+static cudaError_t run_indexer(const CUtensorMap& tk, const CUtensorMap& tq, const IndexerParams& p,
+                               int num_sms, cudaStream_t s) {
+  using C = IdxCfg<HP, DI>;
+  auto kern = indexer_kernel<HP, DI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  record_launch_begin(CSA2_KERNEL_INDEXER, s);
+  kern<<<num_sms, 192, C::kSmem, s>>>(tk, tq, p);
+  record_launch_end(CSA2_KERNEL_INDEXER, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_indexer(const csa2_cache& c, const RowSet& rows, int mode, const uint8_t* q_idx,
+                           const float* w, int32_t hi, const int32_t* pool_blocks,
+                           const int32_t* pool_cnt, const WsLayout& L, uint8_t* ws, int num_sms,
+                           cudaStream_t s) {
+  IndexerParams p;
+  p.mode = mode;
+  p.n_rows = rows.n_rows;
+  p.tq = rows.tq;
+  p.hi = hi;
+  p.batch = c.batch;
+  p.batch_ids = rows.batch_ids;
+  p.q_pos = rows.q_pos;
+  p.seq_len = c.seq_len;
+  p.pool_blocks = pool_blocks;
+  p.pool_cnt = pool_cnt;
+  p.w = w;
+  p.map = RowMap{c.page_table, c.page_size, c.max_pages_per_seq, c.max_len, c.num_pages};
+  p.row_len = reinterpret_cast<int32_t*>(ws + L.row_len);
+  p.tile_prefix = reinterpret_cast<int32_t*>(ws + L.tile_prefix);
+  p.scores = reinterpret_cast<float*>(ws + L.scores);
+  p.score_stride = L.score_stride;
+  p.blockmax = reinterpret_cast<float*>(ws + L.blockmax);
+  p.bm_stride = L.bm_stride;
+  p.cand = reinterpret_cast<float*>(ws + L.cand);
+  p.status = reinterpret_cast<uint32_t*>(ws + L.status);
+  if (rows.n_rows <= 0) return cudaSuccess;
+
+  const int di = c.idx_dim;
+  int64_t phys_rows;
+  int box_rows;
+  if (mode == 1) {
+    box_rows = kBlock;
+  } else if (c.page_size == 0) {
+    box_rows = 128;
+  } else {
+    box_rows = c.page_size < 128 ? c.page_size : 128;
+  }
+  p.rows_per_load = box_rows;
+  phys_rows = c.page_size == 0 ? (int64_t)c.batch * c.max_len : (int64_t)c.num_pages * c.page_size;
+  CUtensorMap tk, tq;
+  if (!make_map(&tk, c.idx_k, phys_rows, di, c.idxk_stride, box_rows)) return cudaErrorInvalidValue;
+  const int64_t q_rows = (int64_t)c.batch * rows.tq * hi;
+  if (!make_map(&tq, q_idx, q_rows, di, di, hi)) return cudaErrorInvalidValue;
+
+  indexer_plan_kernel<<<1, 1024, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  const int hp = hi <= 16 ? 16 : (hi <= 32 ? 32 : 64);
+#define CSA2_IDX_CASE(HPV, DIV) \
+  if (hp == HPV && di == DIV) return run_indexer<HPV, DIV>(tk, tq, p, num_sms, s);
+  CSA2_IDX_CASE(16, 32) CSA2_IDX_CASE(16, 64) CSA2_IDX_CASE(16, 128)
+  CSA2_IDX_CASE(32, 32) CSA2_IDX_CASE(32, 64) CSA2_IDX_CASE(32, 128)
+  CSA2_IDX_CASE(64, 32) CSA2_IDX_CASE(64, 64) CSA2_IDX_CASE(64, 128)
+#undef CSA2_IDX_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace csa2

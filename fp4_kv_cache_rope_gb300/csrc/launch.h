@@ -1,0 +1,63 @@
+// Host-side launch functions shared between the C-ABI layer (api.cu) and the
+// kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/csa2.h"
+#include "common.cuh"
+
+namespace csa2 {
+
+// Benchmark instrumentation (api.cu): records the family's begin/end events
+// on stream s when they are set.
+void record_launch_begin(int family, cudaStream_t s);
+void record_launch_end(int family, cudaStream_t s);
+
+// quant.cu
+cudaError_t launch_fp8_quant(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
+cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const float* idx_in,
+                                int32_t T, uint32_t* status, cudaStream_t s);
+
+// Description of the query rows of one indexer call.
+struct RowSet {
+  int32_t n_rows;           // n_batch * Tq
+  int32_t tq;               // queries per sequence
+  const int32_t* batch_ids; // [n_batch] or null (identity)
+  const int32_t* q_pos;     // [B, Tq] or null (decode)
+};
+
+// indexer.cu: mode 0 = Full (all visible positions), 1 = pool positions.
+cudaError_t launch_indexer(const csa2_cache& c, const RowSet& rows, int mode,
+                           const uint8_t* q_idx, const float* w, int32_t hi,
+                           const int32_t* pool_blocks, const int32_t* pool_cnt,
+                           const WsLayout& L, uint8_t* ws, int num_sms, cudaStream_t s);
+
+// select.cu
+cudaError_t launch_select(const csa2_cache& c, const RowSet& rows, int mode, int32_t k,
+                          const int32_t* pool_in, const int32_t* pool_cnt_in, int32_t* out_idx,
+                          int32_t* out_cnt, int32_t* pool_out, int32_t* pool_cnt_out,
+                          const WsLayout& L, uint8_t* ws, cudaStream_t s);
+
+// attention.cu
+struct AttnArgs {
+  const uint16_t* q;        // bf16 [rows, H, D]
+  int32_t heads;
+  int32_t n_rows;           // B * Tq
+  int32_t tq;               // 1 for decode
+  const int32_t* q_pos;     // prefill positions [B, Tq] or null
+  const int32_t* idx;       // [rows, kcap]
+  const int32_t* cnt;       // [rows]
+  int32_t kcap;
+  const uint8_t* swa;       // decode [B, W, D]; prefill band [B, Tq+W-1, D]
+  const int32_t* swa_cnt;   // decode only, or null
+  int32_t window;
+  float scale;
+  float* out;               // [rows, H, D]
+};
+cudaError_t launch_attention(const csa2_cache& c, const AttnArgs& a, const WsLayout& L,
+                             uint8_t* ws, int num_sms, cudaStream_t s);
+
+}  // namespace csa2

@@ -1,0 +1,184 @@
+// Step 1 of the path: RoPE + FP4 (E2M1 x E4M3-per-16) quantisation + append,
+// and the plain FP8 (E4M3) cast used for the SWA window and indexer operands.
+//
+// "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression" knowledge
+// note, section "FP4 main KV: trade precision for bytes, not for a new GEMM":
+// the main cache is quantised after RoPE to E2M1 values with one E4M3 scale
+// per 16 channels and no second global scale; the SWA cache stays FP8.
+// "Inside DeepSeek V4.1 Flash: CED, CSA2 and the 890-Byte KV Cache", section
+// "Reconstructing the 890-byte cache budget": D/2 code bytes + D/16 scale
+// bytes per entry.
+//
+// One thread owns one group of 16 channels of one row: it loads 64 bytes of
+// fp32, rotates the pairs that fall in the RoPE slice, takes the group
+// maximum, encodes the scale and the 16 codes, and stores 8 code bytes and
+// one scale byte.  Consecutive threads own consecutive groups, so loads and
+// stores are coalesced.  The kernel is HBM bound (2.3 KB read, 324 B written
+// per D = 576 row).
+#include "codec.cuh"
+#include "launch.h"
+
+namespace csa2 {
+
+struct QuantParams {
+  const float* kv;
+  const float* idx_in;
+  uint8_t* codes;
+  uint8_t* scales;
+  uint8_t* idx_k;
+  int64_t code_stride, scale_stride, idxk_stride;
+  const int32_t* seq_len;
+  const float* rope_cos;
+  const float* rope_sin;
+  RowMap map;
+  int32_t B, T, D, R, di;
+  int32_t groups_main, groups_total;  // per row
+  uint32_t* status;
+};
+
+__global__ void __launch_bounds__(256) quant_append_kernel(QuantParams p) {
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t rows = (int64_t)p.B * p.T;
+  if (gid >= rows * p.groups_total) return;
+  const int64_t row = gid / p.groups_total;
+  const int g = (int)(gid - row * p.groups_total);
+  const int b = (int)(row / p.T);
+  const int i = (int)(row - (int64_t)b * p.T);
+  const int64_t pos = (int64_t)p.seq_len[b] + i;
+  if (pos >= p.map.max_len || pos < 0) {
+    set_status(p.status, CSA2_DEV_OVERFLOW);
+    return;
+  }
+  const int64_t r = p.map.row(b, pos);
+  if (r < 0) {
+    set_status(p.status, CSA2_DEV_BAD_PAGE);
+    return;
+  }
+
+  if (g >= p.groups_main) {  // indexer key: plain E4M3 per element
+    const int gi = g - p.groups_main;
+    const float4* src = reinterpret_cast<const float4*>(p.idx_in + row * p.di + 16 * gi);
+    uint32_t w[4];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const float4 f = __ldg(src + v);
+      w[v] = e4m3_encode(f.x) | (e4m3_encode(f.y) << 8) | (e4m3_encode(f.z) << 16) |
+             (e4m3_encode(f.w) << 24);
+    }
+    *reinterpret_cast<uint4*>(p.idx_k + r * p.idxk_stride + 16 * gi) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+    return;
+  }
+
+  float y[16];
+  const float4* src = reinterpret_cast<const float4*>(p.kv + row * p.D + 16 * g);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const float4 f = __ldg(src + v);
+    y[4 * v + 0] = f.x;
+    y[4 * v + 1] = f.y;
+    y[4 * v + 2] = f.z;
+    y[4 * v + 3] = f.w;
+  }
+  // RoPE on interleaved pairs of the last R channels: two fp32 products and one
+  // add/sub per output, each rounded once (no contraction into an FMA).
+  const int c0 = 16 * g;
+  const int rope0 = p.D - p.R;
+  if (c0 + 16 > rope0) {
+    const int half = p.R >> 1;
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      const int c = c0 + e;
+      if (c >= rope0) {
+        const int j = (c - rope0) >> 1;
+        const float cs = __ldg(p.rope_cos + pos * half + j);
+        const float sn = __ldg(p.rope_sin + pos * half + j);
+        const float x0 = y[e], x1 = y[e + 1];
+        y[e] = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
+        y[e + 1] = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, cs));
+      }
+    }
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(y[e]));
+  const uint32_t sc = e4m3_encode_mag(__fdiv_rn(amax, 6.0f));
+  const float s = e4m3_decode(sc);
+  uint32_t lo = 0, hi = 0;
+  if (s != 0.0f) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) lo |= e2m1_encode(__fdiv_rn(y[e], s)) << (4 * e);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) hi |= e2m1_encode(__fdiv_rn(y[8 + e], s)) << (4 * e);
+  }
+  *reinterpret_cast<uint2*>(p.codes + r * p.code_stride + 8 * g) = make_uint2(lo, hi);
+  p.scales[r * p.scale_stride + g] = (uint8_t)sc;
+}
+
+__global__ void advance_len_kernel(int32_t* seq_len, int32_t B, int32_t T, int32_t max_len) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) {
+    const int64_t n = (int64_t)seq_len[b] + T;
+    seq_len[b] = (int32_t)(n > max_len ? max_len : n);
+  }
+}
+
+__global__ void __launch_bounds__(256) fp8_quant_kernel(const float* __restrict__ x, int64_t n,
+                                                        uint8_t* __restrict__ out) {
+  const int64_t i4 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i4 + 3 < n && ((reinterpret_cast<uintptr_t>(x) & 15) == 0) &&
+      ((reinterpret_cast<uintptr_t>(out) & 3) == 0)) {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(x + i4));
+    *reinterpret_cast<uint32_t*>(out + i4) = e4m3_encode(f.x) | (e4m3_encode(f.y) << 8) |
+                                              (e4m3_encode(f.z) << 16) |
+                                              (e4m3_encode(f.w) << 24);
+  } else {
+    for (int64_t i = i4; i < n && i < i4 + 4; ++i) out[i] = (uint8_t)e4m3_encode(x[i]);
+  }
+}
+
+cudaError_t launch_fp8_quant(const float* x, int64_t n, uint8_t* out, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t threads = (n + 3) / 4;
+  const int64_t blocks = (threads + 255) / 256;
+  fp8_quant_kernel<<<(unsigned)blocks, 256, 0, s>>>(x, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const float* idx_in,
+                                int32_t T, uint32_t* status, cudaStream_t s) {
+  QuantParams p;
+  p.kv = kv;
+  p.idx_in = idx_in;
+  p.codes = c.kv_codes;
+  p.scales = c.kv_scales;
+  p.idx_k = c.idx_k;
+  p.code_stride = c.code_stride;
+  p.scale_stride = c.scale_stride;
+  p.idxk_stride = c.idxk_stride;
+  p.seq_len = c.seq_len;
+  p.rope_cos = c.rope_cos;
+  p.rope_sin = c.rope_sin;
+  p.map = RowMap{c.page_table, c.page_size, c.max_pages_per_seq, c.max_len, c.num_pages};
+  p.B = c.batch;
+  p.T = T;
+  p.D = c.dim;
+  p.R = c.rope_dim;
+  p.di = c.idx_dim;
+  p.groups_main = c.dim / kGroup;
+  p.groups_total = p.groups_main + (idx_in ? c.idx_dim / 16 : 0);
+  p.status = status;
+  const int64_t total = (int64_t)c.batch * T * p.groups_total;
+  if (total > 0) {
+    const int64_t blocks = (total + 255) / 256;
+    record_launch_begin(CSA2_KERNEL_QUANT, s);
+    quant_append_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+    record_launch_end(CSA2_KERNEL_QUANT, s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  advance_len_kernel<<<(c.batch + 127) / 128, 128, 0, s>>>(c.seq_len, c.batch, T, c.max_len);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

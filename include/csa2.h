@@ -1,0 +1,254 @@
+/*
+ * csa2.h -- C ABI of the CSA2 sparse-attention path over an FP4 global KV cache
+ * (GB300 / sm_103a).
+ *
+ * The path, as the pages describe it:
+ *   1. main-KV rows are rotated (RoPE) and then quantised to E2M1 values with
+ *      one E4M3 scale per 16 channels, no second global scale, and appended to
+ *      the cache ("DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache
+ *      Compression" knowledge note, section "FP4 main KV: trade precision for
+ *      bytes, not for a new GEMM"; "Inside DeepSeek V4.1 Flash: CED, CSA2 and
+ *      the 890-Byte KV Cache", section "Reconstructing the 890-byte cache
+ *      budget");
+ *   2. a lightning indexer scores cached positions against FP8 indexer keys;
+ *   3. a top-k is selected per query; a Full layer also keeps a pool of at most
+ *      2,048 blocks of 8 positions ranked by block-maximum score, which Reindex
+ *      layers search; Reuse layers take the previous selection unchanged
+ *      (knowledge note, sections "CSA2: share cache, refresh selection only
+ *      when needed" and "Hierarchical Sparse Indexer: make later searches
+ *      bounded");
+ *   4. the selected FP4 rows are gathered and dequantised;
+ *   5. one softmax runs over those rows together with an FP8 sliding window
+ *      (SWA) of the most recent rows (knowledge note, "Putting It Together",
+ *      steps 5-8).
+ *
+ * Layer modes are chosen by which calls the caller makes: Full =
+ * csa2_index_full then csa2_attn_*; Reindex = csa2_index_reindex with the pool
+ * of the last Full call, then csa2_attn_*; Reuse = csa2_attn_* with the
+ * previous index set.
+ *
+ * Conventions for every call
+ *  - All array arguments are DEVICE pointers to caller-owned memory unless a
+ *    comment says "host".  The library allocates no device memory.
+ *  - `stream` is a cudaStream_t passed as void*.  Calls enqueue kernels on it
+ *    and return without synchronising (except csa2_get_status).
+ *  - `ws` is a caller-owned device workspace of at least csa2_workspace_size()
+ *    bytes, 256-byte aligned.  It holds scratch and a 32-bit device status word.
+ *    Calls that share one workspace must be ordered on one stream.
+ *  - Return value: CSA2_OK, or CSA2_ERR_INVALID for an argument rejected on
+ *    the host (nothing is launched), or CSA2_ERR_CUDA when a launch failed.
+ *  - Faults found on the device (an index past the visible length, a page id
+ *    out of range, an append past max_len, a bounded wait that gave up) are
+ *    never trapped: the kernel skips the offending row or element and ORs a
+ *    CSA2_DEV_* bit into the status word, read with csa2_get_status.
+ *  - No C++ exception crosses this boundary.
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum csa2_status {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID = 1,      /* argument rejected on the host; nothing launched */
+  CSA2_ERR_CUDA = 2,         /* a CUDA runtime or driver call failed */
+  CSA2_ERR_UNSUPPORTED = 3,  /* valid request outside the shapes this build runs */
+  CSA2_ERR_TIMEOUT = 4,      /* reserved for host-side waits */
+  CSA2_ERR_DEVICE = 5        /* csa2_get_status found device status bits set */
+} csa2_status;
+
+/* Bits of the device status word. */
+#define CSA2_DEV_BAD_INDEX 0x1u   /* selected position < 0 or >= visible length */
+#define CSA2_DEV_BAD_PAGE 0x2u    /* page-table entry outside [0, num_pages) */
+#define CSA2_DEV_OVERFLOW 0x4u    /* append past max_len */
+#define CSA2_DEV_TIMEOUT 0x8u     /* a bounded on-chip wait gave up */
+#define CSA2_DEV_BAD_POOL 0x10u   /* pool block id outside the visible blocks */
+#define CSA2_DEV_BAD_ALIGN 0x20u  /* on-chip buffer misaligned (kernel skipped work) */
+
+/* Largest k and the pool capacity (blocks of 8 positions). */
+#define CSA2_MAX_TOPK 2048
+#define CSA2_POOL_BLOCKS 2048
+#define CSA2_BLOCK 8
+/* Longest sequence (positions) the selection kernels accept. */
+#define CSA2_MAX_LEN (1 << 21)
+
+/*
+ * One shared global cache (one CSA2 group).  Row layout of the cache:
+ *   kv_codes  [rows, code_stride]  E2M1 codes, two per byte, channel 2j in the
+ *                                  low nibble of byte j (D/2 bytes used)
+ *   kv_scales [rows, scale_stride] one E4M3 scale byte per 16 channels, in
+ *                                  channel order (D/16 bytes used)
+ *   idx_k     [rows, idxk_stride]  indexer key, one E4M3 byte per channel
+ * The physical row of position t of sequence b is
+ *   page_size == 0 : b * max_len + t
+ *   page_size  > 0 : page_table[b * max_pages_per_seq + t / page_size]
+ *                    * page_size + t % page_size
+ */
+typedef struct csa2_cache {
+  int32_t batch;              /* B sequences */
+  int32_t dim;                /* D channels per main-KV row; multiple of 64, <= 576 */
+  int32_t rope_dim;           /* R: the last R channels are rotated; even, <= D */
+  int32_t idx_dim;            /* di: 32, 64 or 128 */
+  int32_t page_size;          /* 0 = contiguous; else a multiple of 8 that divides 128
+                                 or a multiple of 128 */
+  int32_t max_pages_per_seq;  /* columns of page_table (paged only) */
+  int32_t max_len;            /* capacity in positions per sequence; <= CSA2_MAX_LEN */
+  int32_t num_pages;          /* physical pages (paged), used for bounds checks */
+  uint8_t *kv_codes;
+  int64_t code_stride;        /* bytes per row, >= D/2, multiple of 16 */
+  uint8_t *kv_scales;
+  int64_t scale_stride;       /* bytes per row, >= round_up(D/16, 16), multiple of 16 */
+  uint8_t *idx_k;
+  int64_t idxk_stride;        /* bytes per row, >= di, multiple of 16 */
+  const int32_t *page_table;  /* [B, max_pages_per_seq] or NULL when page_size == 0 */
+  int32_t *seq_len;           /* [B] visible positions; advanced by csa2_quant_append */
+  const float *rope_cos;      /* [max_len, R/2] fp32: cos(p * theta^(-2i/R)) */
+  const float *rope_sin;      /* [max_len, R/2] fp32: sin(p * theta^(-2i/R)) */
+} csa2_cache;
+
+/*
+ * Workspace bytes for calls on `cache` that process at most `max_rows` query
+ * rows (B * Tq of one call) with `heads` attention heads.  Returns 0 when the
+ * cache description is invalid.
+ */
+size_t csa2_workspace_size(const csa2_cache *cache, int32_t max_rows, int32_t heads);
+
+/*
+ * Bytes of one FP4 main-KV entry as stored algorithmically: D/2 code bytes +
+ * D/16 scale bytes (288 for D = 512, 324 for D = 576).
+ */
+int64_t csa2_entry_bytes(int32_t dim);
+
+/*
+ * FP8 cast used for the SWA window rows and the indexer operands: every fp32
+ * x[i] becomes the E4M3 code of the nearest representable value, ties to the
+ * even code, saturating at +-448, sign bit copied from x (so -0.0 -> 0x80).
+ * x: device fp32 [n]; out: device uint8 [n].  Non-finite inputs: unspecified.
+ */
+csa2_status csa2_fp8_quant(const float *x, int64_t n, uint8_t *out, void *stream);
+
+/*
+ * Step 1: RoPE + FP4 quantisation + append.
+ * kv:       device fp32 [B, T, D], rows BEFORE rotation.
+ * idx_k_in: device fp32 [B, T, di] or NULL; when given it is cast to E4M3 as
+ *           csa2_fp8_quant does and written to the same rows' idx_k.
+ * Row i of sequence b lands at position p = seq_len[b] + i: channels D-R+2j
+ * and D-R+2j+1 are rotated by (c, s) = (rope_cos, rope_sin)[p][j] as
+ * y0 = x0*c - x1*s, y1 = x0*s + x1*c in fp32 with one rounding per operation;
+ * per group of 16 channels the scale byte is E4M3(amax/6) (correctly rounded
+ * fp32 division, RNE, saturating) and each code is E2M1(y/scale) (RNE,
+ * saturating, sign copied), all codes 0 when the scale decodes to 0.
+ * Afterwards seq_len[b] += T.  A row with p >= max_len is skipped and sets
+ * CSA2_DEV_OVERFLOW.
+ */
+csa2_status csa2_quant_append(const csa2_cache *cache, const float *kv, const float *idx_k_in,
+                              int32_t T, void *ws, void *stream);
+
+/*
+ * Steps 2-3, Full layer: score every visible position and select.
+ * q_idx:    device E4M3 [B, Tq, Hi, di] indexer queries.
+ * w:        device fp32 [B, Tq, Hi] head weights.
+ * Hi:       indexer heads, 1..128.
+ * q_pos:    device int32 [B, Tq] inclusive causal limit per query, or NULL for
+ *           decode (visible = [0, seq_len[b])).
+ * batch_ids, n_batch: device int32 subset of sequences to process, or NULL
+ *           with n_batch = B.
+ * k:        1..CSA2_MAX_TOPK.
+ * Score of position t: s_t = sum_h w_h * max(0, q_h . k_t) (fp32 accumulate).
+ * Outputs (only rows of the processed sequences are written):
+ *   out_idx     [B, Tq, k]  int32 positions of the top min(k, visible) scores
+ *                           ranked by (score desc, position asc), written in
+ *                           ascending position order; cnt entries used
+ *   out_cnt     [B, Tq]     int32
+ *   pool_blocks [B, Tq, CSA2_POOL_BLOCKS] int32 or NULL: block ids b (positions
+ *                           8b..8b+7) of the min(2048, ceil(visible/8)) blocks
+ *                           with the largest block maximum (ties: lower id),
+ *                           ascending
+ *   pool_cnt    [B, Tq]     int32 or NULL
+ */
+csa2_status csa2_index_full(const csa2_cache *cache, const uint8_t *q_idx, const float *w,
+                            int32_t Hi, int32_t Tq, const int32_t *q_pos,
+                            const int32_t *batch_ids, int32_t n_batch, int32_t k,
+                            int32_t *out_idx, int32_t *out_cnt, int32_t *pool_blocks,
+                            int32_t *pool_cnt, void *ws, void *stream);
+
+/*
+ * Steps 2-3, Reindex layer: score only the pool's visible positions with this
+ * layer's own indexer query and select its top-k (same ranking and output
+ * order as csa2_index_full).  pool_blocks [B, Tq, CSA2_POOL_BLOCKS] must be
+ * ascending block ids (as csa2_index_full writes them); pool_cnt [B, Tq].
+ * A block id past the visible blocks sets CSA2_DEV_BAD_POOL and is skipped.
+ */
+csa2_status csa2_index_reindex(const csa2_cache *cache, const uint8_t *q_idx, const float *w,
+                               int32_t Hi, int32_t Tq, const int32_t *q_pos,
+                               const int32_t *pool_blocks, const int32_t *pool_cnt,
+                               const int32_t *batch_ids, int32_t n_batch, int32_t k,
+                               int32_t *out_idx, int32_t *out_cnt, void *ws, void *stream);
+
+/*
+ * Steps 4-5, decode: for each sequence b and head h,
+ *   o = sum_j softmax_j(scale * q_h . x_j) * x_j
+ * over j = the cnt[b] selected global rows idx[b][0..cnt) (dequantised
+ * E2M1 x E4M3) followed by the swa_cnt[b] window rows swa[b][0..swa_cnt)
+ * (E4M3 per element, no scale).  K = V = the dequantised row (value width D).
+ * q:    device bf16 bits [B, H, D], already rotated; H <= 64.
+ * idx:  device int32 [B, kcap]; cnt: device int32 [B] (clamped to kcap).
+ * swa:  device E4M3 [B, W, D]; swa_cnt: device int32 [B] or NULL (= W).
+ * softmax_scale <= 0 selects 1/sqrt(D).  out: device fp32 [B, H, D].
+ * A row with no keys gives zeros.  An index outside [0, seq_len[b]) sets
+ * CSA2_DEV_BAD_INDEX and is left out of the softmax.
+ */
+csa2_status csa2_attn_decode(const csa2_cache *cache, const uint16_t *q, int32_t H,
+                             const int32_t *idx, const int32_t *cnt, int32_t kcap,
+                             const uint8_t *swa, const int32_t *swa_cnt, int32_t W,
+                             float softmax_scale, float *out, void *ws, void *stream);
+
+/*
+ * Steps 4-5, prefill chunk: as csa2_attn_decode for Tq query rows per
+ * sequence.  q: bf16 [B, Tq, H, D]; q_pos [B, Tq] positions (visible global
+ * positions are <= q_pos); idx [B, Tq, kcap]; cnt [B, Tq].
+ * swa: E4M3 band [B, Tq + W - 1, D]; band row r holds position
+ * q_pos[b][0] - (W - 1) + r, and query tq attends to band rows tq .. tq+W-1
+ * whose positions are >= 0 (the W most recent positions up to itself).
+ * out: fp32 [B, Tq, H, D].
+ */
+csa2_status csa2_attn_prefill(const csa2_cache *cache, const uint16_t *q, int32_t H, int32_t Tq,
+                              const int32_t *q_pos, const int32_t *idx, const int32_t *cnt,
+                              int32_t kcap, const uint8_t *swa, int32_t W, float softmax_scale,
+                              float *out, void *ws, void *stream);
+
+/* Copies the device status word to *host_status after the stream drains.
+ * Returns CSA2_ERR_DEVICE when any bit is set. */
+csa2_status csa2_get_status(void *ws, uint32_t *host_status, void *stream);
+
+/* Clears the device status word (stream ordered). */
+csa2_status csa2_reset_status(void *ws, void *stream);
+
+/*
+ * Optional instrumentation for benchmarks: while set, the main kernel of the
+ * given family is bracketed by cudaEventRecord(begin) / cudaEventRecord(end)
+ * on the stream of the call that launches it.  Families:
+ *   CSA2_KERNEL_QUANT (step 1), CSA2_KERNEL_INDEXER (step 2),
+ *   CSA2_KERNEL_SELECT (step 3), CSA2_KERNEL_ATTENTION (steps 4-5).
+ * begin/end are cudaEvent_t passed as void*; NULL/NULL turns it off.
+ * Process-wide setting, not thread safe; it does not change any result.
+ */
+#define CSA2_KERNEL_QUANT 0
+#define CSA2_KERNEL_INDEXER 1
+#define CSA2_KERNEL_SELECT 2
+#define CSA2_KERNEL_ATTENTION 3
+csa2_status csa2_set_launch_events(int32_t family, void *begin, void *end);
+
+/* Static string for a status code. */
+const char *csa2_status_string(csa2_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA2_H */

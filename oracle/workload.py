@@ -1,0 +1,97 @@
+"""Oracle view of a workload: the reference result of one sequence (or one
+query row) computed from the seeded host inputs of ``synth`` with the oracle's
+own codecs and steps.  Test infrastructure only; imports nothing from the
+CUDA path.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import synth
+from synth.device import host_layer_inputs, host_rows_normal
+from synth.workloads import Workload
+
+from . import csa2 as O
+
+
+class SeqRef:
+    """Reference quantities of sequence ``b`` of workload ``wl``."""
+
+    def __init__(self, wl: Workload, b: int, n: int | None = None, cos=None, sin=None):
+        self.wl, self.b = wl, b
+        self.n = wl.lengths[b] if n is None else n
+        self.mult = (synth.outlier_multipliers(wl.seed, wl.dim, wl.outlier_frac)
+                     if wl.outlier_frac else None)
+        if cos is None:
+            cos, sin = synth.rope_table(wl.max_len, wl.rope_dim, wl.theta)
+        self.cos, self.sin = cos, sin
+        self._idxk = None
+
+    # ---- cache contents ----------------------------------------------------
+    def cache_rows(self, positions):
+        """(codes, scales) the cache must hold at ``positions``."""
+        x = host_rows_normal(self.wl.seed, synth.T_KV, self.b, positions, self.wl.dim, self.mult)
+        return O.quant_append_rows(x, np.asarray(positions), self.cos, self.sin, self.wl.rope_dim)
+
+    def idxk_rows(self, positions):
+        x = host_rows_normal(self.wl.seed, synth.T_IDXK, self.b, positions, self.wl.idx_dim)
+        return O.fp8_cast(x)
+
+    def idxk_all(self, n=None):
+        n = self.n if n is None else n
+        if self._idxk is None or len(self._idxk) < n:
+            self._idxk = self.idxk_rows(np.arange(n))
+        return self._idxk[:n]
+
+    def dequant_rows(self, positions):
+        codes, scales = self.cache_rows(positions)
+        return O.dequantize_fp4(codes, scales, self.wl.dim)
+
+    # ---- one layer ---------------------------------------------------------
+    def inputs(self, layer, tq=1):
+        h = host_layer_inputs(self.wl, layer, self.b, tq)
+        h["q_idx"] = O.fp8_cast(h["q_idx_f32"])
+        h["swa"] = O.fp8_cast(h["swa_f32"])
+        return h
+
+    def scores(self, layer, n=None, tq=0, tq_total=1):
+        inp = self.inputs(layer, tq_total)
+        n = self.n if n is None else n
+        return O.indexer_scores(inp["q_idx"][tq], inp["w"][tq], self.idxk_all(n)[:n])
+
+    def full(self, layer, k, n=None, tq=0, tq_total=1):
+        s = self.scores(layer, n, tq, tq_total)
+        idx, pool = O.full_select(s, k)
+        return s, idx, pool
+
+    def reindex(self, layer, pool, k, n=None):
+        inp = self.inputs(layer)
+        n = self.n if n is None else n
+        ik = self.idxk_all(n)
+        pos = O.pool_positions(pool, n)
+        s = O.indexer_scores(inp["q_idx"][0], inp["w"][0], ik[pos])
+        return s, pos, O.topk(s, k, ids=pos)
+
+    def attention(self, layer, idx, swa_count=None, tq=0, tq_total=1, scale=None):
+        """Decode attention (tq_total == 1) or prefill row tq."""
+        inp = self.inputs(layer, tq_total)
+        wl = self.wl
+        q = synth_bf16_to_f64(inp["q_bf16"][tq])
+        rows = [self.dequant_rows(np.asarray(idx))] if len(idx) else [np.zeros((0, wl.dim))]
+        if tq_total == 1:
+            wc = wl.window if swa_count is None else swa_count
+            rows.append(O.swa_rows_decode(inp["swa"][:wc]))
+        else:
+            p0 = self.n_prior_positions
+            pos_q = p0 + tq
+            lo = max(tq, (wl.window - 1) - p0)
+            rows.append(O.swa_rows_decode(inp["swa"][lo:tq + wl.window]))
+            del pos_q
+        return O.sparse_attention(q, np.concatenate(rows), scale)
+
+    n_prior_positions = 0
+
+
+def synth_bf16_to_f64(bits):
+    from .formats import bf16_bits_to_f64
+    return bf16_bits_to_f64(bits)

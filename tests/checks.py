@@ -1,0 +1,56 @@
+"""Comparison rules between the CUDA path and the oracle.
+
+* Codes, scales, FP8 bytes: bit-exact.
+* Top-k and pool sets: the set is unique except among near-ties, so the GPU
+  set must contain every id whose oracle score is above the oracle's k-th
+  score by more than ``RTOL_TIE`` (relative) and no id below it by more than
+  that; it must have the right size, be ascending and hold valid ids only.
+* Attention rows: max_i |o_i - o*_i| / max(max_i |o*_i|, 1e-6) <= ATOL_ROW.
+  The bar (2e-3) is the one stated for the path; the kernel's own error budget
+  (f16 softmax weights, fp32 accumulation) is about 1e-4.
+"""
+import numpy as np
+
+RTOL_TIE = 1e-5
+ATOL_ROW = 2e-3
+
+
+def check_select(gpu_ids, ref_scores, ref_ids, k, what="topk"):
+    gpu_ids = np.asarray(gpu_ids, dtype=np.int64)
+    ref_scores = np.asarray(ref_scores, dtype=np.float64)
+    ref_ids = np.asarray(ref_ids, dtype=np.int64)
+    kk = min(k, len(ref_ids))
+    assert len(gpu_ids) == kk, f"{what}: count {len(gpu_ids)} != {kk}"
+    if kk == 0:
+        return 0
+    assert np.all(np.diff(gpu_ids) > 0), f"{what}: not strictly ascending"
+    pos = {int(t): i for i, t in enumerate(ref_ids)}
+    assert all(int(t) in pos for t in gpu_ids), f"{what}: id outside the candidates"
+    order = np.lexsort((ref_ids, -ref_scores))
+    sigma = ref_scores[order[kk - 1]]
+    scale = max(abs(sigma), float(np.mean(np.abs(ref_scores))) * 1e-3, 1e-30)
+    tol = RTOL_TIE * scale
+    must = set(ref_ids[ref_scores > sigma + tol].tolist())
+    never = set(ref_ids[ref_scores < sigma - tol].tolist())
+    got = set(gpu_ids.tolist())
+    missing = must - got
+    extra = got & never
+    assert not missing, f"{what}: {len(missing)} required ids missing, e.g. {sorted(missing)[:5]}"
+    assert not extra, f"{what}: {len(extra)} ids below the tie band, e.g. {sorted(extra)[:5]}"
+    # number of ids decided by near-ties (informational)
+    ref_set = set(ref_ids[order[:kk]].tolist())
+    return len(ref_set ^ got) // 2
+
+
+def row_error(o, ref):
+    o = np.asarray(o, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.maximum(np.max(np.abs(ref), axis=-1), 1e-6)
+    return np.max(np.abs(o - ref), axis=-1) / den
+
+
+def check_attention(o, ref, what="attention", tol=ATOL_ROW):
+    err = row_error(o, ref)
+    assert np.all(np.isfinite(o)), f"{what}: non-finite output"
+    assert err.max() <= tol, f"{what}: row error {err.max():.3e} > {tol} (head {int(err.argmax())})"
+    return float(err.max())

@@ -1,0 +1,61 @@
+"""CPU checks of the C-ABI library: it builds, loads without a GPU, exports
+every function include/csa2.h declares, and rejects bad arguments on the host
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    path = g._builder().build(verbose=False)
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "csa2.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(csa2_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    import fp4_kv_cache_rope_gb300 as K
+    assert sorted(K.EXPORTED) == names
+
+
+def test_host_validation_without_gpu(lib):
+    import fp4_kv_cache_rope_gb300 as K
+    c = K.Csa2Cache()
+    assert K.workspace_size(c, 1, 64) == 0                 # all-zero description
+    c = K.Csa2Cache(2, 576, 64, 128, 0, 0, 1024, 0, 16, 288, 32, 48, 48, 128, None, 64, 80, 96)
+    assert K.workspace_size(c, 2, 64) > 0
+    assert K.workspace_size(c, 2, 65) == 0                 # more than 64 heads
+    bad = K.Csa2Cache.from_buffer_copy(c)
+    bad.dim = 100                                          # not a multiple of 64
+    assert K.workspace_size(bad, 2, 64) == 0
+    bad = K.Csa2Cache.from_buffer_copy(c)
+    bad.scale_stride = 40                                  # < round_up(36, 16)
+    assert K.workspace_size(bad, 2, 64) == 0
+    bad = K.Csa2Cache.from_buffer_copy(c)
+    bad.page_size = 24                                     # divides neither way into 128
+    assert K.workspace_size(bad, 2, 64) == 0
+    # null pointers and out-of-range k are rejected before any launch
+    r = K._index_full(ctypes.byref(c), None, None, 64, 1, None, None, 2, 64, None, None, None,
+                      None, None, None)
+    assert r == K.CSA2_ERR_INVALID
+    r = K._index_full(ctypes.byref(c), 16, 16, 64, 1, None, None, 2, 4096, 16, 16, None, None,
+                      16, None)
+    assert r == K.CSA2_ERR_INVALID
+    r = K._attn_decode(ctypes.byref(c), 16, 65, 16, 16, 64, 16, None, 128, 0.0, 16, 16, None)
+    assert r == K.CSA2_ERR_INVALID
+    assert K.entry_bytes(512) == 288 and K.entry_bytes(576) == 324
+    assert K.status_string(K.CSA2_ERR_INVALID) == "invalid argument"
