@@ -1,0 +1,464 @@
+"""Benchmark of the CSA2 decode layer-step on GB300 (one JSON line on stdout).
+
+A step is one pass of the whole path over the batch: append the new token's
+main-KV and indexer-key rows (RoPE + FP4 quantisation), score and select
+(Full: every visible position; Reindex: the pool), and attend over the
+selected FP4 rows plus the FP8 window.  The default workload is the
+128K-context Full-layer decode (B = 32, N = 131,072, D = 576, k = 2,048).
+
+  python bench.py [--steps K] [--warmup W] [--workload 2|3|5|1] [--impl reference]
+
+`value` is layer-steps/s with inputs resident in HBM (CUDA events around K
+steps); `e2e` repeats the K steps through the same C-ABI calls with the
+step's inputs copied from pinned host memory and the attention output read
+back every step.  `roofline` is for the indexer kernel (the dominant one),
+timed live with CUDA events around each of its launches.  Under torchrun
+every rank runs an independent replica (the path does not shard: one GPU per
+problem); the JSON line reports the whole job.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HBM_FALLBACK_GBS = 6800.0
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workloads
+def build_run(wid, extra_capacity, batch=None):
+    import torch
+    import fp4_kv_cache_rope_gb300 as K
+    from synth.device import DeviceWorkload, supplied_pool, supplied_prior
+    from synth.workloads import FULL, REINDEX, REUSE, get_workload
+
+    wl = get_workload(wid)
+    wl.extra_capacity = extra_capacity   # room for the tokens appended by the steps
+    if batch:                            # smaller batch of the same shapes (profiling)
+        wl.batch = batch
+        wl.lengths = list(wl.lengths)[:batch]
+        if wl.modes is not None:
+            wl.modes = list(wl.modes)[:batch]
+        wl.name = wl.name + "-first" + str(batch)
+    dw = DeviceWorkload(wl)
+    B, k = wl.batch, wl.topk
+    layers = wl.layers if wl.modes is None else [FULL]
+    inputs = [dw.layer_inputs(L) for L in range(len(layers) if wl.modes is None else 3)]
+    n0 = torch.tensor(wl.lengths, dtype=torch.int32, device="cuda")
+    new_kv, new_idx = dw.new_token_inputs(wl.lengths)
+    new_kv = new_kv.view(B, 1, wl.dim).contiguous()
+    new_idx = new_idx.view(B, 1, wl.idx_dim).contiguous()
+    st = dict(wl=wl, dw=dw, K=K, inputs=inputs, n0=n0, new_kv=new_kv, new_idx=new_idx)
+    st["idx"] = [torch.zeros((B, 1, k), dtype=torch.int32, device="cuda") for _ in range(3)]
+    st["cnt"] = [torch.zeros((B, 1), dtype=torch.int32, device="cuda") for _ in range(3)]
+    st["pool"] = torch.zeros((B, 1, K.POOL_BLOCKS), dtype=torch.int32, device="cuda")
+    st["pool_cnt"] = torch.zeros((B, 1), dtype=torch.int32, device="cuda")
+    st["out"] = [torch.empty((B, wl.heads, wl.dim), dtype=torch.float32, device="cuda")
+                 for _ in range(3)]
+    if wl.modes is not None:
+        modes = wl.modes
+        full_ids = [b for b in range(B) if modes[b] == FULL]
+        re_ids = [b for b in range(B) if modes[b] == REINDEX]
+        ru_ids = [b for b in range(B) if modes[b] == REUSE]
+        st["full_ids"] = torch.tensor(full_ids, dtype=torch.int32, device="cuda")
+        st["re_ids"] = torch.tensor(re_ids, dtype=torch.int32, device="cuda")
+        pool = torch.zeros((B, 1, K.POOL_BLOCKS), dtype=torch.int32)
+        pcnt = torch.zeros((B, 1), dtype=torch.int32)
+        for b in re_ids:
+            pb = supplied_pool(wl, b, wl.lengths[b])
+            pool[b, 0, : len(pb)] = torch.from_numpy(pb)
+            pcnt[b, 0] = len(pb)
+        idx = torch.zeros((B, 1, k), dtype=torch.int32)
+        cnt = torch.zeros((B, 1), dtype=torch.int32)
+        for b in ru_ids:
+            pr = supplied_prior(wl, b, wl.lengths[b])
+            idx[b, 0, : len(pr)] = torch.from_numpy(pr)
+            cnt[b, 0] = len(pr)
+        st["pool"].copy_(pool)
+        st["pool_cnt"].copy_(pcnt)
+        st["idx"][0].copy_(idx)
+        st["cnt"][0].copy_(cnt)
+        st["counts"] = dict(full=len(full_ids), reindex=len(re_ids), reuse=len(ru_ids))
+    torch.cuda.synchronize()
+    return st
+
+
+def step(st, ev=None, ev_attn=None):
+    """One layer-step (or one CSA2 group step for the group workload)."""
+    K, wl, dw, ins = st["K"], st["wl"], st["dw"], st["inputs"]
+    B, k, ws, c = wl.batch, wl.topk, dw.ws, dw.cache
+    K.quant_append(c, st["new_kv"], st["new_idx"], 1, ws)
+    launches = 2
+    if ev is not None:
+        K.set_launch_events(K.KERNEL_INDEXER, ev[0], ev[1])
+    if wl.modes is None:
+        # Full layer (layer 0); the group workload adds Reindex and Reuse
+        K.index_full(c, ins[0]["q_idx"], ins[0]["w"], wl.idx_heads, 1, None, None, B, k,
+                     st["idx"][0], st["cnt"][0], st["pool"], st["pool_cnt"], ws)
+        if ev is not None:
+            K.set_launch_events(K.KERNEL_INDEXER)
+        launches += 3
+        if ev_attn is not None:
+            K.set_launch_events(K.KERNEL_ATTENTION, ev_attn[0], ev_attn[1])
+        K.attn_decode(c, ins[0]["q"].view(st["q_dtype"]), wl.heads, st["idx"][0].view(B, k),
+                      st["cnt"][0].view(B), k, ins[0]["swa"], None, wl.window, 0.0, st["out"][0], ws)
+        if ev_attn is not None:
+            K.set_launch_events(K.KERNEL_ATTENTION)
+        launches += st["attn_launches"]
+        if len(wl.layers) > 1:
+            K.index_reindex(c, ins[1]["q_idx"], ins[1]["w"], wl.idx_heads, 1, None, st["pool"],
+                            st["pool_cnt"], None, B, k, st["idx"][1], st["cnt"][1], ws)
+            launches += 3
+            for L in (1, 2):
+                K.attn_decode(c, ins[L]["q"].view(st["q_dtype"]), wl.heads, st["idx"][1].view(B, k),
+                              st["cnt"][1].view(B), k, ins[L]["swa"], None, wl.window, 0.0,
+                              st["out"][L], ws)
+                launches += st["attn_launches"]
+    else:
+        nf, nr = st["counts"]["full"], st["counts"]["reindex"]
+        if nf:
+            K.index_full(c, ins[0]["q_idx"], ins[0]["w"], wl.idx_heads, 1, None, st["full_ids"],
+                         nf, k, st["idx"][0], st["cnt"][0], None, None, ws)
+            launches += 3
+        if ev is not None:
+            K.set_launch_events(K.KERNEL_INDEXER)
+        if nr:
+            K.index_reindex(c, ins[1]["q_idx"], ins[1]["w"], wl.idx_heads, 1, None, st["pool"],
+                            st["pool_cnt"], st["re_ids"], nr, k, st["idx"][0], st["cnt"][0], ws)
+            launches += 3
+        K.attn_decode(c, ins[2]["q"].view(st["q_dtype"]), wl.heads, st["idx"][0].view(B, k),
+                      st["cnt"][0].view(B), k, ins[2]["swa"], None, wl.window, 0.0, st["out"][0], ws)
+        launches += st["attn_launches"]
+    return launches
+
+
+def layers_per_step(wl):
+    return len(wl.layers) if wl.modes is None else 1
+
+
+def indexer_bytes_per_launch(wl, n_at):
+    """Algorithmic bytes of the (first) indexer launch of a step: every scored
+    position's E4M3 indexer key (di bytes)."""
+    if wl.modes is None:
+        return sum(n_at) * wl.idx_dim
+    return sum(n for n, m in zip(n_at, wl.modes) if m == 0) * wl.idx_dim
+
+
+def roofline_bytes_per_step(wl, n_at):
+    """Roofline bytes of one step: indexer keys read + gathered FP4 entries
+    (D/2 + D/16 B) + FP8 window rows, per layer of the step."""
+    e = wl.dim // 2 + wl.dim // 16
+    total = 0
+    for L, mode in enumerate(wl.layers if wl.modes is None else [None]):
+        for b, n in enumerate(n_at):
+            m = mode if mode is not None else wl.modes[b]
+            if m == 0:
+                total += n * wl.idx_dim
+            elif m == 1:
+                total += min(2048, -(-n // 8)) * 8 * wl.idx_dim
+            total += min(wl.topk, n) * e + wl.window * wl.dim
+    return total
+
+
+# ------------------------------------------------------------- CPU baseline
+def oracle_sample(wl, b, n, layer=0):
+    """One sequence of a Full layer-step on the oracle: inputs are prepared
+    untimed; the returned callable is the timed work."""
+    import numpy as np
+    import synth
+    from oracle import csa2 as O
+    from oracle.formats import bf16_bits_to_f64
+    from oracle.workload import SeqRef
+    from synth.device import host_rows_normal
+    ref = SeqRef(wl, b, n=n)
+    ik = ref.idxk_all(n)
+    inp = ref.inputs(layer)
+    newrow = host_rows_normal(wl.seed, synth.T_KV, b, [n], wl.dim, ref.mult)
+    q64 = bf16_bits_to_f64(inp["q_bf16"][0])
+    swa = O.swa_rows_decode(inp["swa"][: wl.window])
+
+    def run():
+        O.quant_append_rows(newrow, np.array([n]), ref.cos, ref.sin, wl.rope_dim)
+        s = O.indexer_scores(inp["q_idx"][0], inp["w"][0], ik)
+        idx, pool = O.full_select(s, wl.topk)
+        # the selected rows' cache bytes (regenerated and quantised here; the
+        # oracle keeps no cache of its own)
+        xh = ref.dequant_rows(idx)
+        return O.sparse_attention(q64, np.concatenate([xh, swa]))
+    return run
+
+
+def cpu_baseline(wl, samples=4, budget_s=20.0):
+    run = None
+    times = []
+    t_start = time.time()
+    for b in range(samples):
+        run = oracle_sample(wl, b, wl.lengths[b])
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+        if time.time() - t_start > budget_s:
+            break
+    per_seq = statistics.mean(times)
+    value = 1.0 / (per_seq * wl.batch)
+    return {"value": value, "unit": "layer-steps/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{len(times)} of {wl.batch} sequences of one Full layer-step (quantise the "
+                      f"new row, score {wl.lengths[0]} positions, select, re-quantise and "
+                      f"dequantise the selected rows, attend) in numpy fp64 with the host BLAS "
+                      f"threads; scaled to the whole batch",
+            "seconds_per_sequence": per_seq}
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from synth.workloads import get_workload
+    wl = get_workload(args.workload)
+    prepared = [oracle_sample(wl, b % wl.batch, wl.lengths[b % wl.batch])
+                for b in range(max(1, min(args.steps, 2)))]
+    for i in range(args.warmup):
+        prepared[i % len(prepared)]()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        prepared[i % len(prepared)]()
+    dt = time.perf_counter() - t0
+    per_seq = dt / args.steps
+    value = 1.0 / (per_seq * wl.batch)
+    cpu = {"value": value, "unit": "layer-steps/s", "cores": os.cpu_count(), "kind": "oracle",
+           "sample": f"each step = one sequence of the {wl.batch}-sequence layer-step, "
+                     f"scaled by 1/{wl.batch}"}
+    line = {"impl": "reference", "metric": "CSA2 decode layer-steps/s", "value": value,
+            "unit": "layer-steps/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per_seq * wl.batch * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "batch": wl.batch, "ctx": max(wl.lengths)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "layer-steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="use only the first B sequences")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import numpy as np
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    st = build_run(args.workload, args.steps + args.warmup + 16, args.batch or None)
+    wl, K = st["wl"], st["K"]
+    st["q_dtype"] = torch.int16
+    st["attn_launches"] = 1 + (1 if torch.cuda.get_device_properties(0).multi_processor_count //
+                                   wl.batch > 1 else 0)
+    B = wl.batch
+
+    def reset():
+        st["dw"].cache.seq_len.copy_(st["n0"])
+        K.reset_status(st["dw"].ws)
+        torch.cuda.synchronize()
+
+    # ---- device-resident timed loop
+    reset()
+    for _ in range(args.warmup):
+        step(st)
+    reset()
+    n_start = list(wl.lengths)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in ev + eva:   # torch creates the CUDA event on the first record
+        a.record()
+        b.record()
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_begin.record()
+    launches = 0
+    for i in range(args.steps):
+        launches += step(st, ev[i], eva[i])
+    t_end.record()
+    torch.cuda.synchronize()
+    time.sleep(0.1)
+    clk = clocks.stop()
+    ms = t_begin.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    status = K.get_status(st["dw"].ws)
+    idx_ms = [a.elapsed_time(b) for a, b in ev]
+    attn_ms = [a.elapsed_time(b) for a, b in eva]
+    # bytes of the indexer launches (visible length grows by one per step)
+    idx_bytes = [indexer_bytes_per_launch(wl, [n + i + 1 for n in n_start]) for i in range(args.steps)]
+    roof_bytes = [roofline_bytes_per_step(wl, [n + i + 1 for n in n_start]) for i in range(args.steps)]
+    ach = sum(idx_bytes) / (sum(idx_ms) * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    ms_step = ms / args.steps
+    value = world * layers_per_step(wl) * args.steps / (ms * 1e-3)
+    path_gbs = sum(roof_bytes) / (ms * 1e-3) / 1e9
+
+    # ---- end-to-end through the C ABI with host buffers
+    reset()
+    ins = st["inputs"]
+    host = {}
+    keys = [("new_kv", st["new_kv"]), ("new_idx", st["new_idx"])]
+    for L, d in enumerate(ins):
+        for name in ("q_idx", "w", "q", "swa"):
+            keys.append((f"{name}{L}", d[name]))
+    for name, t in keys:
+        host[name] = t.cpu().pin_memory()
+    dev = {name: torch.empty_like(t) for name, t in keys}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    outs = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in st["out"][: layers_per_step(wl)]]
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    st_e2e = dict(st)
+    st_e2e["new_kv"], st_e2e["new_idx"] = dev["new_kv"], dev["new_idx"]
+    st_e2e["inputs"] = [{n: dev[f"{n}{L}"] for n in ("q_idx", "w", "q", "swa")} for L in range(len(ins))]
+    e_steps = max(args.steps // 4, 20)
+    for _ in range(3):
+        for name in host:
+            dev[name].copy_(host[name], non_blocking=True)
+        step(st_e2e)
+    reset()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(e_steps):
+        for name in host:
+            dev[name].copy_(host[name], non_blocking=True)
+        step(st_e2e)
+        for o, src in zip(outs, st["out"]):
+            o.copy_(src, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e_ms = float(t.item())
+    e2e_value = world * layers_per_step(wl) * e_steps / (e_ms * 1e-3)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl)
+    if rank == 0:
+        line = {
+            "metric": "CSA2 decode layer-steps/s (achieved HBM GB/s vs GB300 peak in roofline)",
+            "value": value, "unit": "layer-steps/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3/e2m1 storage; fp8 and f16 tensor-core MMA, f32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "batch": B, "ctx": max(n_start), "topk": wl.topk,
+                       "window": wl.window, "dim": wl.dim, "idx_heads": wl.idx_heads,
+                       "heads": wl.heads, "parallelism": "replicas" if world > 1 else "single",
+                       "l2": f"inputs exceed L2 ({roof_bytes[0] / 1e6:.0f} MB read per step)"},
+            "roofline": {"bound": "hbm", "kernel": "indexer_kernel", "achieved": ach, "peak": peak,
+                         "unit": "GB/s", "frac": ach / peak, "traffic": None,
+                         "peak_source": peak_kind,
+                         "bytes_per_launch": statistics.mean(idx_bytes),
+                         "launch_us": statistics.mean(idx_ms) * 1e3},
+            "path_hbm": {"bytes_per_step": statistics.mean(roof_bytes), "achieved_gbs": path_gbs,
+                         "frac": path_gbs / peak},
+            "kernels_us": {"indexer": statistics.mean(idx_ms) * 1e3,
+                           "attention": statistics.mean(attn_ms) * 1e3},
+            "e2e": {"value": e2e_value, "unit": "layer-steps/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e_steps},
+            "gpu_launches": launches,
+            "clocks": clk,
+            "device_status": status,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

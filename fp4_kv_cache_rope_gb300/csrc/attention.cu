@@ -150,9 +150,11 @@ __global__ void __launch_bounds__(192, 1) attention_kernel(AttnParams p) {
   uint64_t* p_full = raw_full + 6;
   uint64_t* pv_done = raw_full + 7;
   uint64_t* drain = raw_full + 8;
+  uint64_t* q_full = raw_full + 9;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 80);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 84);
   uint32_t* vmask = reinterpret_cast<uint32_t*>(misc + 88);     // [2]
+  static_assert(10 * 8 <= 80, "barrier area");
   float* qmul = reinterpret_cast<float*>(misc + 128);            // [64]
   float* alpha = qmul + 64;                                      // [64]
   float* lrow = alpha + 64;                                      // [64] (ends at misc + 896)
@@ -185,8 +187,14 @@ __global__ void __launch_bounds__(192, 1) attention_kernel(AttnParams p) {
     mbar_init(p_full, 4);
     mbar_init(pv_done, 1);
     mbar_init(drain, 1);
+    mbar_init(q_full, 1);
     *abort_flag = 0;
     fence_barrier_init();
+    // the query rows [H, D] bf16 are contiguous: one bulk copy into the X
+    // region, which holds no slab before the first chunk
+    const uint32_t qbytes = (uint32_t)(p.heads * D * 2);
+    mbar_arrive_expect_tx(q_full, qbytes);
+    bulk_load(sx, p.q + (int64_t)row * p.heads * D, qbytes, q_full);
   }
   if (warp == 5) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
@@ -297,34 +305,47 @@ __global__ void __launch_bounds__(192, 1) attention_kernel(AttnParams p) {
   } else {
     // ------------------------------------------- warps 0-3: compute threads
     // Query: per-head power-of-two scale so that the f16 copy is exact.
-    {
-      const int h = tid >> 1, half = tid & 1;
-      const uint16_t* qr = p.q + ((int64_t)row * p.heads + h) * D;
+    // Warp w converts heads 16w .. 16w+15 from the bf16 rows staged in sx.
+    bool ok = mbar_wait(q_full, 0, abort_flag);
+    constexpr int kChunks = D / 8;                 // 16-byte chunks per head row
+    constexpr int kPer = (kChunks + 31) / 32;
+    for (int hh = 0; hh < 16; ++hh) {
+      const int h = 16 * warp + hh;
+      uint4 v[kPer];
       float mx = 0.0f;
-      if (h < p.heads)
-        for (int d = half * (D / 2); d < (half + 1) * (D / 2); ++d)
-          mx = fmaxf(mx, fabsf(__uint_as_float((uint32_t)qr[d] << 16)));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int c = lane + 32 * i;
+        v[i] = make_uint4(0, 0, 0, 0);
+        if (ok && h < p.heads && c < kChunks)
+          v[i] = *reinterpret_cast<const uint4*>(sx + (h * D + c * 8) * 2);
+        const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          mx = fmaxf(mx, fabsf(__uint_as_float(w4[u] << 16)));
+          mx = fmaxf(mx, fabsf(__uint_as_float(w4[u] & 0xFFFF0000u)));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       int e = 0;
       if (mx > 16384.0f) e = (int)ceilf(log2f(mx)) - 14;
       const float inv = exp2f((float)-e);
-      if (half == 0) qmul[h] = p.scale_log2 * exp2f((float)e);
-      for (int c8 = half * (D / 16); c8 < (half + 1) * (D / 16); ++c8) {  // 8 channels each
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (h < p.heads) {
-          const uint4 raw8 = *reinterpret_cast<const uint4*>(qr + c8 * 8);
-          const uint32_t w[4] = {raw8.x, raw8.y, raw8.z, raw8.w};
+      if (lane == 0) qmul[h] = p.scale_log2 * exp2f((float)e);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int c = lane + 32 * i;
+        if (c < kChunks) {
+          const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
           uint32_t o[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const float lo = __uint_as_float(w[u] << 16) * inv;
-            const float hi = __uint_as_float(w[u] & 0xFFFF0000u) * inv;
-            __half2 h2 = __floats2half2_rn(lo, hi);
+            __half2 h2 = __floats2half2_rn(__uint_as_float(w4[u] << 16) * inv,
+                                           __uint_as_float(w4[u] & 0xFFFF0000u) * inv);
             o[u] = *reinterpret_cast<uint32_t*>(&h2);
           }
-          v = make_uint4(o[0], o[1], o[2], o[3]);
+          st_swz(sq + (c >> 3) * C::kSlab, h, c & 7, make_uint4(o[0], o[1], o[2], o[3]));
         }
-        st_swz(sq + (c8 >> 3) * C::kSlab, h, c8 & 7, v);
       }
     }
     fence_async_smem();
@@ -337,7 +358,7 @@ __global__ void __launch_bounds__(192, 1) attention_kernel(AttnParams p) {
     const int sgrp = tid >> 6;      // slabs sgrp, sgrp+2, ...
     // Every compute thread runs all nloc iterations and the same sequence of
     // named barriers; after a wait gives up (ok == false) the work is skipped.
-    bool ok = true;
+    ok = __all_sync(0xffffffffu, ok);
     for (int it = 0; it < nloc; ++it) {
       const int buf = it & 1;
       if (ok && !mbar_wait(raw_full + buf, (it >> 1) & 1, abort_flag)) ok = false;
@@ -501,7 +522,9 @@ __global__ void __launch_bounds__(192, 1) attention_kernel(AttnParams p) {
         for (int c = 0; c < 64; ++c) v[c] = 0u;
       }
       if (mine) {
-        for (int hh = 0; hh < p.heads; ++hh) {
+#pragma unroll
+        for (int hh = 0; hh < 64; ++hh) {
+          if (hh >= p.heads) break;
           const float acc = __uint_as_float(v[hh]);
           if (direct) {
             const float l = lrow[hh];
@@ -521,28 +544,40 @@ __global__ void __launch_bounds__(192, 1) attention_kernel(AttnParams p) {
 }
 
 // Merge of split-K partials: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-__global__ void attn_combine_kernel(const float* __restrict__ part_o,
-                                    const float* __restrict__ part_ml, float* __restrict__ out,
-                                    int heads, int D, int splits) {
+__global__ void __launch_bounds__(192) attn_combine_kernel(const float* __restrict__ part_o,
+                                                           const float* __restrict__ part_ml,
+                                                           float* __restrict__ out, int heads,
+                                                           int D, int splits) {
+  __shared__ float wgt[kMaxSplits];
+  __shared__ float inv_den;
   const int row = blockIdx.x, h = blockIdx.y;
-  float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) {
-    const int slot = row * splits + s;
-    const float l = part_ml[((int64_t)slot * 64 + h) * 2 + 1];
-    if (l > 0.0f) M = fmaxf(M, part_ml[((int64_t)slot * 64 + h) * 2 + 0]);
-  }
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float num = 0.0f, den = 0.0f;
-    for (int s = 0; s < splits; ++s) {
-      const int slot = row * splits + s;
-      const float l = part_ml[((int64_t)slot * 64 + h) * 2 + 1];
-      if (l > 0.0f) {
-        const float e = exp2f(part_ml[((int64_t)slot * 64 + h) * 2 + 0] - M);
-        num += e * part_o[((int64_t)slot * 64 + h) * D + d];
-        den += e * l;
-      }
+  if (threadIdx.x < 32) {
+    const int s = threadIdx.x;
+    float m = -INFINITY, l = 0.0f;
+    if (s < splits) {
+      const int64_t slot = (int64_t)row * splits + s;
+      m = part_ml[(slot * 64 + h) * 2 + 0];
+      l = part_ml[(slot * 64 + h) * 2 + 1];
     }
-    out[((int64_t)row * heads + h) * D + d] = den > 0.0f ? num / den : 0.0f;
+    float M = l > 0.0f ? m : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = (l > 0.0f) ? exp2f(m - M) : 0.0f;
+    float den = w * l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (s < splits) wgt[s] = w;
+    if (s == 0) inv_den = den > 0.0f ? 1.0f / den : 0.0f;
+  }
+  __syncthreads();
+  const float id = inv_den;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float num = 0.0f;
+    for (int s = 0; s < splits; ++s) {
+      const float w = wgt[s];
+      if (w != 0.0f) num += w * part_o[(((int64_t)row * splits + s) * 64 + h) * D + d];
+    }
+    out[((int64_t)row * heads + h) * D + d] = num * id;
   }
 }
 
@@ -559,7 +594,7 @@ static cudaError_t run_attention(const AttnParams& p, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess || p.splits == 1) return e;
   dim3 g2(p.n_rows, p.heads);
-  attn_combine_kernel<<<g2, 128, 0, s>>>(p.part_o, p.part_ml, p.out, p.heads, C::D, p.splits);
+  attn_combine_kernel<<<g2, 192, 0, s>>>(p.part_o, p.part_ml, p.out, p.heads, C::D, p.splits);
   return cudaGetLastError();
 }
 

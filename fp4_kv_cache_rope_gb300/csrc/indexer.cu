@@ -140,6 +140,29 @@ __device__ __forceinline__ int find_row(const int32_t* prefix, int n_rows, int t
   return lo;
 }
 
+// Walks the query rows of a CTA's tile range; the row's bounds and visible
+// length are reloaded only when the row changes.
+struct RowCursor {
+  int row, begin, end, len;
+  __device__ __forceinline__ void init(const IndexerParams& p, int t) {
+    row = find_row(p.tile_prefix, p.n_rows, t);
+    begin = p.tile_prefix[row];
+    end = p.tile_prefix[row + 1];
+    len = p.row_len[row];
+  }
+  // Returns true when tile t starts a new row.
+  __device__ __forceinline__ bool advance(const IndexerParams& p, int t) {
+    if (t < end) return false;
+    do {
+      ++row;
+      begin = end;
+      end = p.tile_prefix[row + 1];
+    } while (t >= end);
+    len = p.row_len[row];
+    return true;
+  }
+};
+
 template <int HP, int DI>
 __global__ void __launch_bounds__(192, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
@@ -197,25 +220,26 @@ __global__ void __launch_bounds__(192, 1)
   if (t_begin < t_end) {
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------ TMA producer
-      int row = find_row(p.tile_prefix, p.n_rows, t_begin);
-      int cur = -1, qn = 0, stage = 0;
+      RowCursor rc;
+      rc.init(p, t_begin);
+      int qn = 0, stage = 0;
       uint32_t phase = 0;
+      int b = row_seq(p, rc.row), tq = rc.row % p.tq;
       for (int t = t_begin; t < t_end; ++t) {
-        while (t >= p.tile_prefix[row + 1]) ++row;
-        const int b = row_seq(p, row);
-        const int tq = row % p.tq;
-        if (row != cur) {
+        const bool fresh = rc.advance(p, t) || t == t_begin;
+        if (fresh) {
+          b = row_seq(p, rc.row);
+          tq = rc.row % p.tq;
           const int qs = qn & 1;
           if (!mbar_wait(qempty + qs, ((qn >> 1) & 1) ^ 1, abort_flag)) break;
           mbar_arrive_expect_tx(qfull + qs, (uint32_t)(p.hi * DI));
           tma_load_2d(qbuf + qs * C::kQBytes, &tm_q, 0, (int)(((int64_t)b * p.tq + tq) * p.hi),
                       qfull + qs);
-          cur = row;
           ++qn;
         }
         if (!mbar_wait(empty + stage, phase ^ 1, abort_flag)) break;
-        const int j = t - p.tile_prefix[row];
-        const int len = p.row_len[row];
+        const int j = t - rc.begin;
+        const int len = rc.len;
         uint8_t* dst = stages + stage * C::kStageBytes;
         uint32_t bytes = 0;
         if (p.mode == 0) {
@@ -274,16 +298,16 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1 && lane == 0) {
       // --------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = instr_desc(0, 0, false, false, 128, HP);
-      int row = find_row(p.tile_prefix, p.n_rows, t_begin);
-      int cur = -1, qn = 0, stage = 0, acc = 0;
+      RowCursor rc;
+      rc.init(p, t_begin);
+      int qn = 0, stage = 0, acc = 0;
       uint32_t phase = 0, aphase = 0;
       const uint32_t st_base = smem_u32(stages), q_base = smem_u32(qbuf);
       for (int t = t_begin; t < t_end; ++t) {
-        while (t >= p.tile_prefix[row + 1]) ++row;
-        if (row != cur) {
-          if (cur >= 0) mma_commit(qempty + ((qn - 1) & 1));
+        const bool fresh = rc.advance(p, t) || t == t_begin;
+        if (fresh) {
+          if (qn > 0) mma_commit(qempty + ((qn - 1) & 1));
           if (!mbar_wait(qfull + (qn & 1), (qn >> 1) & 1, abort_flag)) break;
-          cur = row;
           ++qn;
         }
         const int qs = (qn - 1) & 1;
@@ -306,19 +330,24 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp >= 2) {
       // ----------------------------------------------------------- epilogue
       const int quad = warp & 3;  // TMEM lane quadrant this warp may access
-      int row = find_row(p.tile_prefix, p.n_rows, t_begin);
-      int cur = -1, acc = 0;
+      RowCursor rc;
+      rc.init(p, t_begin);
+      int acc = 0;
       uint32_t aphase = 0;
       float wv[HP];
+      float* out_row = nullptr;
+      float* bm_row = nullptr;
       for (int t = t_begin; t < t_end; ++t) {
-        while (t >= p.tile_prefix[row + 1]) ++row;
-        const int b = row_seq(p, row);
-        const int tq = row % p.tq;
-        if (row != cur) {
+        const bool fresh = rc.advance(p, t) || t == t_begin;
+        if (fresh) {
+          const int b = row_seq(p, rc.row);
+          const int tq = rc.row % p.tq;
           const float* wr = p.w + ((int64_t)b * p.tq + tq) * p.hi;
 #pragma unroll
           for (int h = 0; h < HP; ++h) wv[h] = h < p.hi ? __ldg(wr + h) : 0.0f;
-          cur = row;
+          out_row = p.mode == 0 ? p.scores + (int64_t)rc.row * p.score_stride
+                                : p.cand + (int64_t)rc.row * kPoolPositions;
+          bm_row = p.blockmax + (int64_t)rc.row * p.bm_stride;
         }
         if (!mbar_wait(tfull + acc, aphase, abort_flag)) break;
         tc_fence_after();
@@ -334,24 +363,25 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty + acc);
-        float s = 0.0f;
+        // four independent partial sums over the heads, then their sum
+        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int h = 0; h < HP; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(r[h]), 0.0f), s);
-        const int j = t - p.tile_prefix[row];
-        const int len = p.row_len[row];
+        for (int h = 0; h < HP; ++h)
+          s4[h & 3] = fmaf(wv[h], fmaxf(__uint_as_float(r[h]), 0.0f), s4[h & 3]);
+        const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        const int j = t - rc.begin;
         const int local = 32 * quad + lane;
         if (p.mode == 0) {
-          const int64_t pos = (int64_t)j * 128 + local;
-          const bool valid = pos < len;
-          if (valid) p.scores[(int64_t)row * p.score_stride + pos] = s;
+          const int pos = j * 128 + local;
+          const bool valid = pos < rc.len;
+          if (valid) out_row[pos] = s;
           float m = valid ? s : -INFINITY;
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-          if ((lane & 7) == 0 && valid) p.blockmax[(int64_t)row * p.bm_stride + pos / kBlock] = m;
+          if ((lane & 7) == 0 && valid) bm_row[pos / kBlock] = m;
         } else {
-          const int c = j * 128 + local;
-          p.cand[(int64_t)row * kPoolPositions + c] = s;
+          out_row[j * 128 + local] = s;
         }
         if (++acc == 2) { acc = 0; aphase ^= 1; }
       }

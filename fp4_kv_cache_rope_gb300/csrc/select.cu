@@ -13,18 +13,25 @@
 // distinct positions ranked at least as high as the P-th block maximum; the
 // k <= P best positions therefore all lie in pool blocks.  The same argument
 // one level up (groups of 8 blocks ranked by their maximum) bounds the block
-// selection for long sequences.  Each selection then runs over at most 32,768
-// candidates held in registers by one CTA of 1,024 threads:
-//   * a 32-step bisection on the order-preserving uint32 image of the fp32
-//     score finds the k-th largest key T (each step is one block-wide count);
-//   * keys > T are all taken, keys == T are taken in ascending id order until
-//     k are chosen; a block-wide exclusive scan writes them in id order.
+// selection for long sequences (and again for groups of 64 blocks when even
+// the groups of 8 are too many).  Each selection then runs over at most
+// 24,576 candidates held in registers by one CTA of 512 threads:
+//   * keys are the order-preserving uint32 image of the fp32 scores; a radix
+//     select finds the k-th largest key: the bits above the highest bit where
+//     the block's largest and smallest keys differ are common, and the rest is
+//     resolved 8 bits at a time with a shared-memory histogram (at most four
+//     passes, stopping early once the boundary bin holds exactly the keys
+//     still needed);
+//   * keys above the boundary are all taken, keys on it are taken in
+//     ascending id order until k are chosen; a block-wide exclusive scan
+//     writes them in id order.
 #include "launch.h"
 
 namespace csa2 {
 
-constexpr int kSelThreads = 1024;
-constexpr int kSelE = 32;  // candidates per thread (capacity 32,768)
+constexpr int kSelThreads = 512;
+constexpr int kSelE = 48;  // candidates per thread (capacity 24,576)
+constexpr int kSelCap = kSelThreads * kSelE;
 
 struct SelectParams {
   int32_t mode;  // 0 = Full (pool + top-k from scores), 1 = top-k over pool candidates
@@ -48,8 +55,12 @@ struct SelectParams {
 struct SelSmem {
   int red[32];
   int scan[32];
-  int list[kPoolPositions];      // selected ids of the current stage
+  uint32_t ured[2][32];
+  int hist[256];
+  int digit, above;
+  int list[kPoolPositions];      // selected group ids of the current level
   int list2[kPoolBlocks];        // pool block ids
+  int list3[kPoolBlocks];        // staging of a level's selection
 };
 
 __device__ __forceinline__ int block_sum(int v, int* red) {
@@ -57,7 +68,7 @@ __device__ __forceinline__ int block_sum(int v, int* red) {
   v = __reduce_add_sync(0xffffffffu, v);
   if (lane == 0) red[warp] = v;
   __syncthreads();
-  int t = red[lane];
+  int t = lane < kSelThreads / 32 ? red[lane] : 0;
   t = __reduce_add_sync(0xffffffffu, t);
   __syncthreads();
   return t;
@@ -76,7 +87,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scan, int* total) {
   if (lane == 31) scan[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int t = scan[lane];
+    int t = lane < kSelThreads / 32 ? scan[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int u = __shfl_up_sync(0xffffffffu, t, o);
@@ -86,44 +97,105 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scan, int* total) {
   }
   __syncthreads();
   const int before = (warp > 0 ? scan[warp - 1] : 0) + x - v;
-  *total = scan[31];
+  *total = scan[kSelThreads / 32 - 1];
   __syncthreads();
   return before;
 }
 
 // Select the k best of the block's candidates (key 0 = absent).  Candidate
 // e of thread i has id i*kSelE + e.  Writes the selected ids, ascending, to
-// out[0..k) (shared or global) and returns k.
+// out[0..k) (shared or global) and returns k.  k must not exceed the number
+// of present keys.
 template <typename Out>
 __device__ int block_select(const uint32_t (&key)[kSelE], int k, SelSmem& sm, Out out) {
   if (k <= 0) return 0;
-  // k-th largest key by bisection: largest T with count(key >= T) >= k.
-  uint32_t T = 0;
-  for (int bit = 31; bit >= 0; --bit) {
-    const uint32_t cand = T | (1u << bit);
-    int c = 0;
-#pragma unroll
-    for (int e = 0; e < kSelE; ++e) c += key[e] >= cand;
-    if (block_sum(c, sm.red) >= k) T = cand;
-  }
-  int gt = 0, eq = 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // ---- largest and smallest present key
+  uint32_t mx = 0u, mn = 0xFFFFFFFFu;
 #pragma unroll
   for (int e = 0; e < kSelE; ++e) {
-    gt += key[e] > T;
-    eq += key[e] == T;
+    if (key[e]) {
+      mx = max(mx, key[e]);
+      mn = min(mn, key[e]);
+    }
   }
-  const int n_gt = block_sum(gt, sm.red);
-  const int need = k - n_gt;  // how many keys equal to T are taken
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  if (lane == 0) {
+    sm.ured[0][warp] = mx;
+    sm.ured[1][warp] = mn;
+  }
+  __syncthreads();
+  constexpr int kWarps = kSelThreads / 32;
+  mx = __reduce_max_sync(0xffffffffu, lane < kWarps ? sm.ured[0][lane] : 0u);
+  mn = __reduce_min_sync(0xffffffffu, lane < kWarps ? sm.ured[1][lane] : 0xFFFFFFFFu);
+  // ---- radix passes below the common high bits
+  uint32_t prefix = mx, mask = 0xFFFFFFFFu;
+  int remaining = k;
+  if (mx != mn) {
+    int hi = 31 - __clz(mx ^ mn);
+    mask = hi == 31 ? 0u : ~((2u << hi) - 1u);
+    prefix = mx & mask;
+    for (; hi >= 0; hi -= 8) {
+      const int lo = hi >= 7 ? hi - 7 : 0;
+      const int nbin = 1 << (hi - lo + 1);
+      for (int i = threadIdx.x; i < 256; i += kSelThreads) sm.hist[i] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int e = 0; e < kSelE; ++e)
+        if (key[e] && (key[e] & mask) == prefix)
+          atomicAdd(&sm.hist[(key[e] >> lo) & (uint32_t)(nbin - 1)], 1);
+      __syncthreads();
+      if (warp == 0) {
+        // lane holds bins 8*lane .. 8*lane+7; find the bin holding the
+        // remaining-th largest key, scanning from the top
+        int c[8], tot = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          c[u] = sm.hist[8 * lane + u];
+          tot += c[u];
+        }
+        int above = tot;  // inclusive suffix over lanes >= lane
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_down_sync(0xffffffffu, above, o);
+          if (lane + o < 32) above += v;
+        }
+        int cum = above - tot;  // keys in bins of higher lanes
+#pragma unroll
+        for (int u = 7; u >= 0; --u) {
+          if (cum < remaining && remaining <= cum + c[u]) {
+            sm.digit = 8 * lane + u;
+            sm.above = cum;
+          }
+          cum += c[u];
+        }
+      }
+      __syncthreads();
+      const int d = sm.digit;
+      remaining -= sm.above;
+      prefix |= (uint32_t)d << lo;
+      mask |= (uint32_t)(nbin - 1) << lo;
+      const bool exact = sm.hist[d] == remaining;
+      __syncthreads();
+      if (exact) break;
+    }
+  }
+  // ---- take keys above the boundary, and the first `remaining` on it
+  int eq = 0;
+#pragma unroll
+  for (int e = 0; e < kSelE; ++e) eq += key[e] != 0u && (key[e] & mask) == prefix;
   int tot;
-  int eq_before = block_excl_scan(eq, sm.scan, &tot);
+  const int eq_before = block_excl_scan(eq, sm.scan, &tot);
   int take = 0;
   {
     int eb = eq_before;
 #pragma unroll
     for (int e = 0; e < kSelE; ++e) {
-      const bool isq = key[e] == T;
-      take += (key[e] > T) || (isq && eb < need);
-      eb += isq;
+      const uint32_t km = key[e] & mask;
+      const bool on = key[e] != 0u && km == prefix;
+      take += (key[e] != 0u && km > prefix) || (on && eb < remaining);
+      eb += on;
     }
   }
   int pos = block_excl_scan(take, sm.scan, &tot);
@@ -132,9 +204,10 @@ __device__ int block_select(const uint32_t (&key)[kSelE], int k, SelSmem& sm, Ou
     const int base = threadIdx.x * kSelE;
 #pragma unroll
     for (int e = 0; e < kSelE; ++e) {
-      const bool isq = key[e] == T;
-      if ((key[e] > T) || (isq && eb < need)) out(pos++, base + e);
-      eb += isq;
+      const uint32_t km = key[e] & mask;
+      const bool on = key[e] != 0u && km == prefix;
+      if ((key[e] != 0u && km > prefix) || (on && eb < remaining)) out(pos++, base + e);
+      eb += on;
     }
   }
   __syncthreads();
@@ -159,45 +232,54 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelectParams p) 
     const int nb = (len + kBlock - 1) / kBlock;
     const int P = nb < kPoolBlocks ? nb : kPoolBlocks;
     const int kk = p.k < len ? p.k : len;
-    // ---- pool: top-P blocks by block maximum
-    if (nb <= kSelThreads * kSelE) {
+    // ---- pool: top-P blocks by block maximum.  Groups of 8^level blocks are
+    // ranked by their maximum first when there are more blocks than the
+    // block-wide selection holds; each level then expands the P best groups
+    // into their 8 sub-groups and keeps the P best of those.
+    int level = 0;
+    for (int64_t ng = nb; ng > kSelCap; ng = (ng + kBlock - 1) / kBlock) ++level;
+    auto group_key = [&](int64_t g, int span) -> uint32_t {
+      uint32_t m = 0u;
+      const int64_t first = g * span;
+      for (int u = 0; u < span; ++u) {
+        const int64_t i = first + u;
+        if (i < nb) m = max(m, order_key(__ldg(bm + i)));
+      }
+      return m;
+    };
+    {
+      int span = 1;
+      for (int l = 0; l < level; ++l) span *= kBlock;
+      const int64_t ng = (nb + span - 1) / span;
 #pragma unroll
       for (int e = 0; e < kSelE; ++e) {
-        const int i = base + e;
-        key[e] = i < nb ? order_key(__ldg(bm + i)) : 0u;
+        const int64_t g = base + e;
+        key[e] = g < ng ? (span == 1 ? order_key(__ldg(bm + g)) : group_key(g, span)) : 0u;
       }
-      block_select(key, P, sm, [&](int o, int id) { sm.list2[o] = id; });
-    } else {
-      // groups of 8 blocks ranked by their maximum, then blocks inside the
-      // P best groups
-      const int ng = (nb + kBlock - 1) / kBlock;
-#pragma unroll 4
-      for (int e = 0; e < kSelE; ++e) {
-        const int g = base + e;
-        uint32_t m = 0;
-        if (g < ng) {
-          for (int u = 0; u < kBlock; ++u) {
-            const int i = g * kBlock + u;
-            if (i < nb) m = max(m, order_key(__ldg(bm + i)));
+      int* dst = level == 0 ? sm.list2 : sm.list;
+      block_select(key, P, sm, [&](int o, int id) { dst[o] = id; });
+      for (int l = level; l > 0; --l) {
+        const int sub = span / kBlock;
+#pragma unroll
+        for (int e = 0; e < kSelE; ++e) {
+          const int c = base + e;
+          uint32_t v = 0u;
+          if (c < P * kBlock) {
+            const int64_t g = (int64_t)sm.list[c / kBlock] * kBlock + (c % kBlock);
+            v = group_key(g, sub);
           }
+          key[e] = v;
         }
-        key[e] = m;
+        __syncthreads();
+        int* out_list = l == 1 ? sm.list2 : sm.list;
+        // expanded ids are written to a scratch copy first when overwriting list
+        block_select(key, P, sm, [&](int o, int id) {
+          sm.list3[o] = sm.list[id / kBlock] * kBlock + (id % kBlock);
+        });
+        for (int i = threadIdx.x; i < P; i += kSelThreads) out_list[i] = sm.list3[i];
+        __syncthreads();
+        span = sub;
       }
-      block_select(key, P, sm, [&](int o, int id) { sm.list[o] = id; });
-#pragma unroll
-      for (int e = 0; e < kSelE; ++e) {
-        const int c = base + e;
-        uint32_t v = 0;
-        if (c < P * kBlock) {
-          const int i = sm.list[c / kBlock] * kBlock + (c % kBlock);
-          if (i < nb) v = order_key(__ldg(bm + i));
-        }
-        key[e] = v;
-      }
-      __syncthreads();
-      block_select(key, P, sm, [&](int o, int id) {
-        sm.list2[o] = sm.list[id / kBlock] * kBlock + (id % kBlock);
-      });
     }
     __syncthreads();
     if (p.pool_out) {

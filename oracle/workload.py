@@ -26,6 +26,7 @@ class SeqRef:
             cos, sin = synth.rope_table(wl.max_len, wl.rope_dim, wl.theta)
         self.cos, self.sin = cos, sin
         self._idxk = None
+        self._inputs = {}
 
     # ---- cache contents ----------------------------------------------------
     def cache_rows(self, positions):
@@ -49,10 +50,12 @@ class SeqRef:
 
     # ---- one layer ---------------------------------------------------------
     def inputs(self, layer, tq=1):
-        h = host_layer_inputs(self.wl, layer, self.b, tq)
-        h["q_idx"] = O.fp8_cast(h["q_idx_f32"])
-        h["swa"] = O.fp8_cast(h["swa_f32"])
-        return h
+        if (layer, tq) not in self._inputs:
+            h = host_layer_inputs(self.wl, layer, self.b, tq)
+            h["q_idx"] = O.fp8_cast(h["q_idx_f32"])
+            h["swa"] = O.fp8_cast(h["swa_f32"])
+            self._inputs[(layer, tq)] = h
+        return self._inputs[(layer, tq)]
 
     def scores(self, layer, n=None, tq=0, tq_total=1):
         inp = self.inputs(layer, tq_total)
@@ -67,9 +70,12 @@ class SeqRef:
     def reindex(self, layer, pool, k, n=None):
         inp = self.inputs(layer)
         n = self.n if n is None else n
-        ik = self.idxk_all(n)
         pos = O.pool_positions(pool, n)
-        s = O.indexer_scores(inp["q_idx"][0], inp["w"][0], ik[pos])
+        if self._idxk is not None and len(self._idxk) >= n:
+            kp = self._idxk[pos]
+        else:
+            kp = self.idxk_rows(pos)
+        s = O.indexer_scores(inp["q_idx"][0], inp["w"][0], kp)
         return s, pos, O.topk(s, k, ids=pos)
 
     def attention(self, layer, idx, swa_count=None, tq=0, tq_total=1, scale=None):

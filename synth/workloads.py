@@ -34,10 +34,11 @@ class Workload:
     modes: list | None = None   # per-sequence mode (ragged mixed decode)
     prefill_tokens: int = 0  # T new tokens appended and queried (prefill chunk)
     pool_blocks: int = 2048  # pool capacity in 8-position blocks
+    extra_capacity: int = 0  # positions reserved for tokens appended by decode steps
 
     @property
     def max_len(self) -> int:
-        return int(max(self.lengths)) + max(self.prefill_tokens, 0) + 64
+        return int(max(self.lengths)) + max(self.prefill_tokens, 0) + 64 + self.extra_capacity
 
     def entry_bytes(self) -> int:
         return self.dim // 2 + self.dim // 16
