@@ -52,16 +52,28 @@ struct SelectParams {
   uint32_t* status;
 };
 
+// Candidate id i = t * kSelE + e (thread t owns a contiguous run of ids, so a
+// thread-order scan emits ids in ascending order) is stored at keys[e *
+// kSelThreads + t], so that a warp reading its e-th candidates touches 32
+// consecutive words.
+constexpr int kDigitBits = 11;                 // radix digit width
+constexpr int kBins = 1 << kDigitBits;         // 2,048 bins
 struct SelSmem {
+  uint32_t keys[kSelCap];
+  int sel[kPoolBlocks];          // ids chosen by the last selection, ascending
+  int list[kPoolBlocks];         // group / block ids kept by the current level
   int red[32];
   int scan[32];
   uint32_t ured[2][32];
-  int hist[256];
+  // per-warp histograms, two 16-bit counters per word (a warp adds at most
+  // 32 * kSelE < 65,536 to one bin)
+  uint32_t whist[kSelThreads / 32][kBins / 2];
   int digit, above;
-  int list[kPoolPositions];      // selected group ids of the current level
-  int list2[kPoolBlocks];        // pool block ids
-  int list3[kPoolBlocks];        // staging of a level's selection
 };
+
+__device__ __forceinline__ uint32_t& key_at(SelSmem& sm, int t, int e) {
+  return sm.keys[e * kSelThreads + t];
+}
 
 __device__ __forceinline__ int block_sum(int v, int* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -74,9 +86,8 @@ __device__ __forceinline__ int block_sum(int v, int* red) {
   return t;
 }
 
-// Exclusive scan of one int per thread in thread order; returns the thread's
-// offset, and the total through *total.
-__device__ __forceinline__ int block_excl_scan(int v, int* scan, int* total) {
+// Exclusive scan of one int per thread in thread order.
+__device__ __forceinline__ int block_excl_scan(int v, int* scan) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -97,26 +108,24 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scan, int* total) {
   }
   __syncthreads();
   const int before = (warp > 0 ? scan[warp - 1] : 0) + x - v;
-  *total = scan[kSelThreads / 32 - 1];
   __syncthreads();
   return before;
 }
 
-// Select the k best of the block's candidates (key 0 = absent).  Candidate
-// e of thread i has id i*kSelE + e.  Writes the selected ids, ascending, to
-// out[0..k) (shared or global) and returns k.  k must not exceed the number
-// of present keys.
-template <typename Out>
-__device__ int block_select(const uint32_t (&key)[kSelE], int k, SelSmem& sm, Out out) {
-  if (k <= 0) return 0;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Selects the k best of the n first candidates in sm.keys (key 0 = absent)
+// and writes their ids, ascending, to sm.sel[0..k).  k must not exceed the
+// number of present keys.
+__device__ __noinline__ void block_select(SelSmem& sm, int n, int k) {
+  if (k <= 0) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, t = threadIdx.x;
+  const int e_end = min(kSelE, max(0, n - t * kSelE));  // candidates of this thread
   // ---- largest and smallest present key
   uint32_t mx = 0u, mn = 0xFFFFFFFFu;
-#pragma unroll
-  for (int e = 0; e < kSelE; ++e) {
-    if (key[e]) {
-      mx = max(mx, key[e]);
-      mn = min(mn, key[e]);
+  for (int e = 0; e < e_end; ++e) {
+    const uint32_t v = key_at(sm, t, e);
+    if (v) {
+      mx = max(mx, v);
+      mn = min(mn, v);
     }
   }
   mx = __reduce_max_sync(0xffffffffu, mx);
@@ -129,102 +138,129 @@ __device__ int block_select(const uint32_t (&key)[kSelE], int k, SelSmem& sm, Ou
   constexpr int kWarps = kSelThreads / 32;
   mx = __reduce_max_sync(0xffffffffu, lane < kWarps ? sm.ured[0][lane] : 0u);
   mn = __reduce_min_sync(0xffffffffu, lane < kWarps ? sm.ured[1][lane] : 0xFFFFFFFFu);
-  // ---- radix passes below the common high bits
+  // ---- radix passes below the common high bits, kDigitBits at a time
   uint32_t prefix = mx, mask = 0xFFFFFFFFu;
   int remaining = k;
   if (mx != mn) {
     int hi = 31 - __clz(mx ^ mn);
     mask = hi == 31 ? 0u : ~((2u << hi) - 1u);
     prefix = mx & mask;
-    for (; hi >= 0; hi -= 8) {
-      const int lo = hi >= 7 ? hi - 7 : 0;
-      const int nbin = 1 << (hi - lo + 1);
-      for (int i = threadIdx.x; i < 256; i += kSelThreads) sm.hist[i] = 0;
-      __syncthreads();
-#pragma unroll
-      for (int e = 0; e < kSelE; ++e)
-        if (key[e] && (key[e] & mask) == prefix)
-          atomicAdd(&sm.hist[(key[e] >> lo) & (uint32_t)(nbin - 1)], 1);
-      __syncthreads();
-      if (warp == 0) {
-        // lane holds bins 8*lane .. 8*lane+7; find the bin holding the
-        // remaining-th largest key, scanning from the top
-        int c[8], tot = 0;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          c[u] = sm.hist[8 * lane + u];
-          tot += c[u];
-        }
-        int above = tot;  // inclusive suffix over lanes >= lane
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_down_sync(0xffffffffu, above, o);
-          if (lane + o < 32) above += v;
-        }
-        int cum = above - tot;  // keys in bins of higher lanes
-#pragma unroll
-        for (int u = 7; u >= 0; --u) {
-          if (cum < remaining && remaining <= cum + c[u]) {
-            sm.digit = 8 * lane + u;
-            sm.above = cum;
-          }
-          cum += c[u];
+    for (; hi >= 0; hi -= kDigitBits) {
+      const int lo = hi >= kDigitBits - 1 ? hi - (kDigitBits - 1) : 0;
+      const uint32_t bmask = (2u << (hi - lo)) - 1u;
+      const int nword = (int)((bmask + 2u) >> 1);  // words of the used bins
+      uint32_t* wh = sm.whist[warp];
+      for (int i = lane; i < nword; i += 32) wh[i] = 0u;
+      __syncwarp();
+      for (int e = 0; e < e_end; ++e) {
+        const uint32_t v = key_at(sm, t, e);
+        if (v && (v & mask) == prefix) {
+          const uint32_t bin = (v >> lo) & bmask;
+          atomicAdd(&wh[bin >> 1], 1u << ((bin & 1u) << 4));
         }
       }
       __syncthreads();
-      const int d = sm.digit;
-      remaining -= sm.above;
-      prefix |= (uint32_t)d << lo;
-      mask |= (uint32_t)(nbin - 1) << lo;
-      const bool exact = sm.hist[d] == remaining;
+      // thread t owns bins 4t .. 4t+3 (two words)
+      int c[4] = {0, 0, 0, 0};
+      if (2 * t < nword) {
+#pragma unroll 4
+        for (int w = 0; w < kSelThreads / 32; ++w) {
+          const uint32_t a = sm.whist[w][2 * t], b = (2 * t + 1 < nword) ? sm.whist[w][2 * t + 1] : 0u;
+          c[0] += a & 0xFFFFu;
+          c[1] += a >> 16;
+          c[2] += b & 0xFFFFu;
+          c[3] += b >> 16;
+        }
+      }
+      const int mine = c[0] + c[1] + c[2] + c[3];
+      const int before = block_excl_scan(mine, sm.scan);  // keys in lower bins
+      const int total = block_sum(mine, sm.red);
+      int cum = total - before - mine;                     // keys in higher bins
+#pragma unroll
+      for (int u = 3; u >= 0; --u) {
+        if (cum < remaining && remaining <= cum + c[u]) {
+          sm.digit = 4 * t + u;
+          sm.above = cum;
+        }
+        cum += c[u];
+      }
       __syncthreads();
+      const int d = sm.digit;
+      const int above = sm.above;
+      const int dcount = (d >> 2) == t ? c[d & 3] : -1;
+      remaining -= above;
+      prefix |= (uint32_t)d << lo;
+      mask |= bmask << lo;
+      // stop early when the boundary bin holds exactly the keys still needed
+      const bool exact = __syncthreads_or(dcount == remaining);
       if (exact) break;
     }
   }
-  // ---- take keys above the boundary, and the first `remaining` on it
+  // ---- keys above the boundary, then the first `remaining` keys on it
   int eq = 0;
-#pragma unroll
-  for (int e = 0; e < kSelE; ++e) eq += key[e] != 0u && (key[e] & mask) == prefix;
-  int tot;
-  const int eq_before = block_excl_scan(eq, sm.scan, &tot);
+  for (int e = 0; e < e_end; ++e) {
+    const uint32_t v = key_at(sm, t, e);
+    eq += v != 0u && (v & mask) == prefix;
+  }
+  const int eq_before = block_excl_scan(eq, sm.scan);
   int take = 0;
   {
     int eb = eq_before;
-#pragma unroll
-    for (int e = 0; e < kSelE; ++e) {
-      const uint32_t km = key[e] & mask;
-      const bool on = key[e] != 0u && km == prefix;
-      take += (key[e] != 0u && km > prefix) || (on && eb < remaining);
+    for (int e = 0; e < e_end; ++e) {
+      const uint32_t v = key_at(sm, t, e);
+      const bool on = v != 0u && (v & mask) == prefix;
+      take += (v != 0u && (v & mask) > prefix) || (on && eb < remaining);
       eb += on;
     }
   }
-  int pos = block_excl_scan(take, sm.scan, &tot);
+  int pos = block_excl_scan(take, sm.scan);
   {
     int eb = eq_before;
-    const int base = threadIdx.x * kSelE;
-#pragma unroll
-    for (int e = 0; e < kSelE; ++e) {
-      const uint32_t km = key[e] & mask;
-      const bool on = key[e] != 0u && km == prefix;
-      if ((key[e] != 0u && km > prefix) || (on && eb < remaining)) out(pos++, base + e);
+    for (int e = 0; e < e_end; ++e) {
+      const uint32_t v = key_at(sm, t, e);
+      const bool on = v != 0u && (v & mask) == prefix;
+      if ((v != 0u && (v & mask) > prefix) || (on && eb < remaining)) sm.sel[pos++] = t * kSelE + e;
       eb += on;
     }
   }
   __syncthreads();
-  return k;
+}
+
+// Maximum order key over blocks [g*span, g*span + span) of the row.
+__device__ __forceinline__ uint32_t group_key(const float* bm, int64_t nb, int64_t g, int span) {
+  uint32_t m = 0u;
+  const int64_t first = g * span;
+  for (int u = 0; u < span; ++u) {
+    const int64_t i = first + u;
+    if (i < nb) m = max(m, order_key(__ldg(bm + i)));
+  }
+  return m;
+}
+
+// Fills this thread's candidate keys from f(e) (which may load from global
+// memory), 24 candidates at a time so that their loads are in flight together.
+template <typename F>
+__device__ __forceinline__ void fill_keys(SelSmem& sm, int t, F f) {
+#pragma unroll
+  for (int e0 = 0; e0 < kSelE; e0 += 24) {
+    uint32_t v[24];
+#pragma unroll
+    for (int u = 0; u < 24; ++u) v[u] = f(e0 + u);
+#pragma unroll
+    for (int u = 0; u < 24; ++u) key_at(sm, t, e0 + u) = v[u];
+  }
 }
 
 __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelectParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
-  const int row = blockIdx.x;
+  const int row = blockIdx.x, t = threadIdx.x;
   const int bi = row / p.tq, tq = row % p.tq;
   const int b = p.batch_ids ? p.batch_ids[bi] : bi;
   if (b < 0 || b >= p.batch) return;
   const int64_t orow = (int64_t)b * p.tq + tq;  // output row
   const int len = p.row_len[row];
-  const int base = threadIdx.x * kSelE;
-  uint32_t key[kSelE];
+  const int base = t * kSelE;
 
   if (p.mode == 0) {
     const float* bm = p.blockmax + (int64_t)row * p.bm_stride;
@@ -232,104 +268,86 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelectParams p) 
     const int nb = (len + kBlock - 1) / kBlock;
     const int P = nb < kPoolBlocks ? nb : kPoolBlocks;
     const int kk = p.k < len ? p.k : len;
-    // ---- pool: top-P blocks by block maximum.  Groups of 8^level blocks are
-    // ranked by their maximum first when there are more blocks than the
-    // block-wide selection holds; each level then expands the P best groups
-    // into their 8 sub-groups and keeps the P best of those.
-    int level = 0;
-    for (int64_t ng = nb; ng > kSelCap; ng = (ng + kBlock - 1) / kBlock) ++level;
-    auto group_key = [&](int64_t g, int span) -> uint32_t {
-      uint32_t m = 0u;
-      const int64_t first = g * span;
-      for (int u = 0; u < span; ++u) {
-        const int64_t i = first + u;
-        if (i < nb) m = max(m, order_key(__ldg(bm + i)));
-      }
-      return m;
-    };
-    {
-      int span = 1;
-      for (int l = 0; l < level; ++l) span *= kBlock;
-      const int64_t ng = (nb + span - 1) / span;
-#pragma unroll
-      for (int e = 0; e < kSelE; ++e) {
-        const int64_t g = base + e;
-        key[e] = g < ng ? (span == 1 ? order_key(__ldg(bm + g)) : group_key(g, span)) : 0u;
-      }
-      int* dst = level == 0 ? sm.list2 : sm.list;
-      block_select(key, P, sm, [&](int o, int id) { dst[o] = id; });
-      for (int l = level; l > 0; --l) {
-        const int sub = span / kBlock;
-#pragma unroll
-        for (int e = 0; e < kSelE; ++e) {
-          const int c = base + e;
-          uint32_t v = 0u;
-          if (c < P * kBlock) {
-            const int64_t g = (int64_t)sm.list[c / kBlock] * kBlock + (c % kBlock);
-            v = group_key(g, sub);
-          }
-          key[e] = v;
-        }
-        __syncthreads();
-        int* out_list = l == 1 ? sm.list2 : sm.list;
-        // expanded ids are written to a scratch copy first when overwriting list
-        block_select(key, P, sm, [&](int o, int id) {
-          sm.list3[o] = sm.list[id / kBlock] * kBlock + (id % kBlock);
-        });
-        for (int i = threadIdx.x; i < P; i += kSelThreads) out_list[i] = sm.list3[i];
-        __syncthreads();
-        span = sub;
-      }
+    // ---- pool: top-P blocks by block maximum.  When there are more blocks
+    // than one selection holds, groups of 8^level blocks are ranked by their
+    // maximum first; each level expands the P best groups into their 8
+    // sub-groups and keeps the P best of those.
+    int level = 0, span = 1;
+    for (int64_t ng = nb; ng > kSelCap; ng = (ng + kBlock - 1) / kBlock) {
+      ++level;
+      span *= kBlock;
     }
+    const int64_t ng = (nb + span - 1) / span;
+    fill_keys(sm, t, [&](int e) -> uint32_t {
+      const int64_t g = base + e;
+      return g < ng ? (span == 1 ? order_key(__ldg(bm + g)) : group_key(bm, nb, g, span)) : 0u;
+    });
     __syncthreads();
+    block_select(sm, (int)ng, P);
+    for (int i = t; i < P; i += kSelThreads) sm.list[i] = sm.sel[i];
+    __syncthreads();
+    for (; span > 1; span /= kBlock) {
+      const int sub = span / kBlock;
+      fill_keys(sm, t, [&](int e) -> uint32_t {
+        const int c = base + e;
+        return c < P * kBlock ? group_key(bm, nb, (int64_t)sm.list[c / kBlock] * kBlock + c % kBlock, sub)
+                              : 0u;
+      });
+      __syncthreads();
+      block_select(sm, P * kBlock, P);
+      int nid[(kPoolBlocks + kSelThreads - 1) / kSelThreads];
+#pragma unroll
+      for (int u = 0; u < (kPoolBlocks + kSelThreads - 1) / kSelThreads; ++u) {
+        const int i = t + u * kSelThreads;
+        if (i < P) nid[u] = sm.list[sm.sel[i] / kBlock] * kBlock + sm.sel[i] % kBlock;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < (kPoolBlocks + kSelThreads - 1) / kSelThreads; ++u) {
+        const int i = t + u * kSelThreads;
+        if (i < P) sm.list[i] = nid[u];
+      }
+      __syncthreads();
+    }
     if (p.pool_out) {
       int32_t* po = p.pool_out + orow * kPoolBlocks;
-      for (int i = threadIdx.x; i < P; i += kSelThreads) po[i] = sm.list2[i];
+      for (int i = t; i < P; i += kSelThreads) po[i] = sm.list[i];
     }
-    if (p.pool_cnt_out && threadIdx.x == 0) p.pool_cnt_out[orow] = P;
+    if (p.pool_cnt_out && t == 0) p.pool_cnt_out[orow] = P;
     // ---- top-k over the pool's positions
-#pragma unroll
-    for (int e = 0; e < kSelE; ++e) {
+    fill_keys(sm, t, [&](int e) -> uint32_t {
       const int c = base + e;
-      uint32_t v = 0;
-      if (c < P * kBlock) {
-        const int t = sm.list2[c / kBlock] * kBlock + (c % kBlock);
-        if (t < len) v = order_key(__ldg(sc + t));
-      }
-      key[e] = v;
-    }
-    int32_t* oi = p.out_idx + orow * p.k;
-    block_select(key, kk, sm, [&](int o, int id) {
-      oi[o] = sm.list2[id / kBlock] * kBlock + (id % kBlock);
+      if (c >= P * kBlock) return 0u;
+      const int pos = sm.list[c / kBlock] * kBlock + (c % kBlock);
+      return pos < len ? order_key(__ldg(sc + pos)) : 0u;
     });
-    if (threadIdx.x == 0) p.out_cnt[orow] = kk;
+    __syncthreads();
+    block_select(sm, P * kBlock, kk);
+    int32_t* oi = p.out_idx + orow * p.k;
+    for (int i = t; i < kk; i += kSelThreads) oi[i] = sm.list[sm.sel[i] / kBlock] * kBlock + sm.sel[i] % kBlock;
+    if (t == 0) p.out_cnt[orow] = kk;
   } else {
     int pc = p.pool_cnt_in[orow];
     pc = pc < 0 ? 0 : (pc > kPoolBlocks ? kPoolBlocks : pc);
     const int32_t* pool = p.pool_in + orow * kPoolBlocks;
     const float* cd = p.cand + (int64_t)row * kPoolPositions;
-    for (int i = threadIdx.x; i < pc; i += kSelThreads) sm.list2[i] = pool[i];
+    for (int i = t; i < pc; i += kSelThreads) sm.list[i] = pool[i];
     __syncthreads();
-    int nvalid = 0;
-#pragma unroll
-    for (int e = 0; e < kSelE; ++e) {
+    fill_keys(sm, t, [&](int e) -> uint32_t {
       const int c = base + e;
-      uint32_t v = 0;
-      if (c < pc * kBlock) {
-        const int blk = sm.list2[c / kBlock];
-        const int64_t t = (int64_t)blk * kBlock + (c % kBlock);
-        if (blk >= 0 && t < len) v = order_key(__ldg(cd + c));
-      }
-      key[e] = v;
-      nvalid += v != 0u;
-    }
-    nvalid = block_sum(nvalid, sm.red);
-    const int kk = p.k < nvalid ? p.k : nvalid;
-    int32_t* oi = p.out_idx + orow * p.k;
-    block_select(key, kk, sm, [&](int o, int id) {
-      oi[o] = sm.list2[id / kBlock] * kBlock + (id % kBlock);
+      if (c >= pc * kBlock) return 0u;
+      const int blk = sm.list[c / kBlock];
+      const int64_t pos = (int64_t)blk * kBlock + (c % kBlock);
+      return (blk >= 0 && pos < len) ? order_key(__ldg(cd + c)) : 0u;
     });
-    if (threadIdx.x == 0) p.out_cnt[orow] = kk;
+    int nvalid = 0;
+    for (int e = 0; e < kSelE; ++e) nvalid += key_at(sm, t, e) != 0u;
+    nvalid = block_sum(nvalid, sm.red);  // includes a barrier
+    const int kk = p.k < nvalid ? p.k : nvalid;
+    block_select(sm, pc * kBlock, kk);
+    int32_t* oi = p.out_idx + orow * p.k;
+    for (int i = t; i < kk; i += kSelThreads) oi[i] = sm.list[sm.sel[i] / kBlock] * kBlock + sm.sel[i] % kBlock;
+    if (t == 0) p.out_cnt[orow] = kk;
   }
 }
 
