@@ -15,7 +15,7 @@
 // one level up (groups of 8 blocks ranked by their maximum) bounds the block
 // selection for long sequences (and again for groups of 64 blocks when even
 // the groups of 8 are too many).  Each selection then runs over at most
-// 24,576 candidates held in registers by one CTA of 512 threads:
+// 18,432 candidates held in registers by one CTA of 512 threads:
 //   * keys are the order-preserving uint32 image of the fp32 scores; a radix
 //     select finds the k-th largest key: the bits above the highest bit where
 //     the block's largest and smallest keys differ are common, and the rest is
@@ -30,7 +30,7 @@
 namespace csa2 {
 
 constexpr int kSelThreads = 512;
-constexpr int kSelE = 48;  // candidates per thread (capacity 24,576)
+constexpr int kSelE = 36;  // candidates per thread (capacity 18,432)
 constexpr int kSelCap = kSelThreads * kSelE;
 
 struct SelectParams {
@@ -52,16 +52,21 @@ struct SelectParams {
   uint32_t* status;
 };
 
-// Candidate id i = t * kSelE + e (thread t owns a contiguous run of ids, so a
-// thread-order scan emits ids in ascending order) is stored at keys[e *
-// kSelThreads + t], so that a warp reading its e-th candidates touches 32
-// consecutive words.
+// Candidate id i is owned by thread i / kSelE (a contiguous run of ids per
+// thread, so a thread-order scan emits ids in ascending order) and stored at
+// keys[i + i / kSelE]: one pad word per thread makes both the coalesced
+// fills (consecutive ids) and the per-thread reads (stride kSelE + 1, an odd
+// number of banks) free of bank conflicts.
 constexpr int kDigitBits = 11;                 // radix digit width
 constexpr int kBins = 1 << kDigitBits;         // 2,048 bins
+constexpr int kRefineMax = 256;                // boundary keys ranked by counting
 struct SelSmem {
-  uint32_t keys[kSelCap];
+  uint32_t keys[kSelThreads * (kSelE + 1)];
   int sel[kPoolBlocks];          // ids chosen by the last selection, ascending
   int list[kPoolBlocks];         // group / block ids kept by the current level
+  uint32_t bkey[kRefineMax];     // boundary-bin keys and ids (ascending id)
+  int bid[kRefineMax];
+  uint8_t bsel[kSelCap];         // refinement verdict per id
   int red[32];
   int scan[32];
   uint32_t ured[2][32];
@@ -71,9 +76,7 @@ struct SelSmem {
   int digit, above;
 };
 
-__device__ __forceinline__ uint32_t& key_at(SelSmem& sm, int t, int e) {
-  return sm.keys[e * kSelThreads + t];
-}
+__device__ __forceinline__ int key_slot(int i) { return i + i / kSelE; }
 
 __device__ __forceinline__ int block_sum(int v, int* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -112,17 +115,29 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scan) {
   return before;
 }
 
-// Selects the k best of the n first candidates in sm.keys (key 0 = absent)
-// and writes their ids, ascending, to sm.sel[0..k).  k must not exceed the
-// number of present keys.
+// Selects the k best of the n first candidates (key 0 = absent) and writes
+// their ids, ascending, to sm.sel[0..k).  k must not exceed the number of
+// present keys.
+//  1. largest / smallest present key: the bits above their highest
+//     differing bit are common;
+//  2. histograms of the next kDigitBits bits, restricted to the keys still
+//     on the boundary, narrow the boundary bin (keys in higher bins are all
+//     taken) until it holds exactly the keys still needed, or few enough to
+//     rank exactly (larger key first, lower id on equal keys) by counting;
+//  3. one ordered compaction writes the ids.
+// Each CTA runs this code only a few times, so it is written as short loops
+// (instruction lines are reused) rather than unrolled straight-line code.
 __device__ __noinline__ void block_select(SelSmem& sm, int n, int k) {
   if (k <= 0) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, t = threadIdx.x;
   const int e_end = min(kSelE, max(0, n - t * kSelE));  // candidates of this thread
-  // ---- largest and smallest present key
+  const uint32_t* my = sm.keys + t * (kSelE + 1);       // this thread's keys
+  constexpr int kWarps = kSelThreads / 32;
+  // ---- 1. range of the present keys
   uint32_t mx = 0u, mn = 0xFFFFFFFFu;
+#pragma unroll 4
   for (int e = 0; e < e_end; ++e) {
-    const uint32_t v = key_at(sm, t, e);
+    const uint32_t v = my[e];
     if (v) {
       mx = max(mx, v);
       mn = min(mn, v);
@@ -135,36 +150,38 @@ __device__ __noinline__ void block_select(SelSmem& sm, int n, int k) {
     sm.ured[1][warp] = mn;
   }
   __syncthreads();
-  constexpr int kWarps = kSelThreads / 32;
   mx = __reduce_max_sync(0xffffffffu, lane < kWarps ? sm.ured[0][lane] : 0u);
   mn = __reduce_min_sync(0xffffffffu, lane < kWarps ? sm.ured[1][lane] : 0xFFFFFFFFu);
-  // ---- radix passes below the common high bits, kDigitBits at a time
+  // Selection state: keys with (key & mask) > prefix are taken; keys with
+  // (key & mask) == prefix are on the boundary and `remaining` of them are
+  // taken -- the first ones by id, or those marked in sm.bsel when refine.
   uint32_t prefix = mx, mask = 0xFFFFFFFFu;
   int remaining = k;
+  bool refine = false;
   if (mx != mn) {
     int hi = 31 - __clz(mx ^ mn);
     mask = hi == 31 ? 0u : ~((2u << hi) - 1u);
     prefix = mx & mask;
-    for (; hi >= 0; hi -= kDigitBits) {
+    while (hi >= 0) {
       const int lo = hi >= kDigitBits - 1 ? hi - (kDigitBits - 1) : 0;
       const uint32_t bmask = (2u << (hi - lo)) - 1u;
-      const int nword = (int)((bmask + 2u) >> 1);  // words of the used bins
+      const int nword = (int)((bmask + 2u) >> 1);
+      // ---- 2. histogram of bits [lo, hi] of the keys on the boundary
       uint32_t* wh = sm.whist[warp];
       for (int i = lane; i < nword; i += 32) wh[i] = 0u;
       __syncwarp();
+#pragma unroll 4
       for (int e = 0; e < e_end; ++e) {
-        const uint32_t v = key_at(sm, t, e);
+        const uint32_t v = my[e];
         if (v && (v & mask) == prefix) {
           const uint32_t bin = (v >> lo) & bmask;
           atomicAdd(&wh[bin >> 1], 1u << ((bin & 1u) << 4));
         }
       }
       __syncthreads();
-      // thread t owns bins 4t .. 4t+3 (two words)
-      int c[4] = {0, 0, 0, 0};
+      int c[4] = {0, 0, 0, 0};  // thread t owns bins 4t .. 4t+3
       if (2 * t < nword) {
-#pragma unroll 4
-        for (int w = 0; w < kSelThreads / 32; ++w) {
+        for (int w = 0; w < kWarps; ++w) {
           const uint32_t a = sm.whist[w][2 * t], b = (2 * t + 1 < nword) ? sm.whist[w][2 * t + 1] : 0u;
           c[0] += a & 0xFFFFu;
           c[1] += a >> 16;
@@ -173,55 +190,82 @@ __device__ __noinline__ void block_select(SelSmem& sm, int n, int k) {
         }
       }
       const int mine = c[0] + c[1] + c[2] + c[3];
-      const int before = block_excl_scan(mine, sm.scan);  // keys in lower bins
+      const int before = block_excl_scan(mine, sm.scan);
       const int total = block_sum(mine, sm.red);
-      int cum = total - before - mine;                     // keys in higher bins
-#pragma unroll
+      int cum = total - before - mine;  // keys in higher bins
       for (int u = 3; u >= 0; --u) {
         if (cum < remaining && remaining <= cum + c[u]) {
           sm.digit = 4 * t + u;
           sm.above = cum;
+          sm.scan[31] = c[u];  // size of the boundary bin
         }
         cum += c[u];
       }
       __syncthreads();
       const int d = sm.digit;
-      const int above = sm.above;
-      const int dcount = (d >> 2) == t ? c[d & 3] : -1;
-      remaining -= above;
+      remaining -= sm.above;
+      const int nbd = sm.scan[31];
       prefix |= (uint32_t)d << lo;
       mask |= bmask << lo;
-      // stop early when the boundary bin holds exactly the keys still needed
-      const bool exact = __syncthreads_or(dcount == remaining);
-      if (exact) break;
+      __syncthreads();
+      if (nbd == remaining) break;  // the whole boundary bin is taken
+      if (nbd <= kRefineMax) {
+        // rank the few boundary keys exactly by counting
+        refine = true;
+        int nb_mine = 0;
+        for (int e = 0; e < e_end; ++e) nb_mine += my[e] != 0u && (my[e] & mask) == prefix;
+        int o = block_excl_scan(nb_mine, sm.scan);
+        for (int e = 0; e < e_end; ++e) {
+          const uint32_t v = my[e];
+          if (v != 0u && (v & mask) == prefix) {
+            sm.bkey[o] = v;
+            sm.bid[o] = t * kSelE + e;
+            ++o;
+          }
+        }
+        __syncthreads();
+        // rank = keys above + equal keys with a lower id (list is in id order)
+        if (t < nbd) {
+          const uint32_t ki = sm.bkey[t];
+          int rank = 0;
+          for (int j = 0; j < nbd; ++j) {
+            const uint32_t kj = sm.bkey[j];
+            rank += (kj > ki) | ((kj == ki) & (j < t));
+          }
+          sm.bsel[sm.bid[t]] = rank < remaining ? 1 : 0;
+        }
+        __syncthreads();
+        break;
+      }
+      hi = lo - 1;
     }
   }
-  // ---- keys above the boundary, then the first `remaining` keys on it
+  // ---- 3. keys above the boundary, then the boundary keys that are taken
   int eq = 0;
-  for (int e = 0; e < e_end; ++e) {
-    const uint32_t v = key_at(sm, t, e);
-    eq += v != 0u && (v & mask) == prefix;
+  if (!refine) {
+    for (int e = 0; e < e_end; ++e) eq += my[e] != 0u && (my[e] & mask) == prefix;
   }
-  const int eq_before = block_excl_scan(eq, sm.scan);
-  int take = 0;
-  {
-    int eb = eq_before;
-    for (int e = 0; e < e_end; ++e) {
-      const uint32_t v = key_at(sm, t, e);
-      const bool on = v != 0u && (v & mask) == prefix;
-      take += (v != 0u && (v & mask) > prefix) || (on && eb < remaining);
-      eb += on;
-    }
+  const int eq_before = refine ? 0 : block_excl_scan(eq, sm.scan);
+  int take = 0, eb = eq_before;
+#pragma unroll 4
+  for (int e = 0; e < e_end; ++e) {
+    const uint32_t v = my[e];
+    const uint32_t km = v & mask;
+    const bool on = v != 0u && km == prefix;
+    const bool pick = refine ? (on && sm.bsel[t * kSelE + e]) : (on && eb < remaining);
+    take += (v != 0u && km > prefix) || pick;
+    eb += on;
   }
   int pos = block_excl_scan(take, sm.scan);
-  {
-    int eb = eq_before;
-    for (int e = 0; e < e_end; ++e) {
-      const uint32_t v = key_at(sm, t, e);
-      const bool on = v != 0u && (v & mask) == prefix;
-      if ((v != 0u && (v & mask) > prefix) || (on && eb < remaining)) sm.sel[pos++] = t * kSelE + e;
-      eb += on;
-    }
+  eb = eq_before;
+#pragma unroll 4
+  for (int e = 0; e < e_end; ++e) {
+    const uint32_t v = my[e];
+    const uint32_t km = v & mask;
+    const bool on = v != 0u && km == prefix;
+    const bool pick = refine ? (on && sm.bsel[t * kSelE + e]) : (on && eb < remaining);
+    if ((v != 0u && km > prefix) || pick) sm.sel[pos++] = t * kSelE + e;
+    eb += on;
   }
   __syncthreads();
 }
@@ -237,18 +281,25 @@ __device__ __forceinline__ uint32_t group_key(const float* bm, int64_t nb, int64
   return m;
 }
 
-// Fills this thread's candidate keys from f(e) (which may load from global
-// memory), 24 candidates at a time so that their loads are in flight together.
+// Fills the keys of candidates 0 .. n-1 from f(i), consecutive threads on
+// consecutive ids (coalesced loads), four loads in flight per thread.
 template <typename F>
-__device__ __forceinline__ void fill_keys(SelSmem& sm, int t, F f) {
+__device__ __forceinline__ void fill_keys(SelSmem& sm, int n, F f) {
+#pragma unroll 1
+  for (int r0 = 0; r0 < kSelE; r0 += 4) {
+    uint32_t v[4];
 #pragma unroll
-  for (int e0 = 0; e0 < kSelE; e0 += 24) {
-    uint32_t v[24];
+    for (int u = 0; u < 4; ++u) {
+      const int i = (r0 + u) * kSelThreads + threadIdx.x;
+      v[u] = i < n ? f(i) : 0u;
+    }
 #pragma unroll
-    for (int u = 0; u < 24; ++u) v[u] = f(e0 + u);
-#pragma unroll
-    for (int u = 0; u < 24; ++u) key_at(sm, t, e0 + u) = v[u];
+    for (int u = 0; u < 4; ++u) {
+      const int i = (r0 + u) * kSelThreads + threadIdx.x;
+      sm.keys[key_slot(i)] = v[u];
+    }
   }
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelectParams p) {
@@ -260,7 +311,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelectParams p) 
   if (b < 0 || b >= p.batch) return;
   const int64_t orow = (int64_t)b * p.tq + tq;  // output row
   const int len = p.row_len[row];
-  const int base = t * kSelE;
 
   if (p.mode == 0) {
     const float* bm = p.blockmax + (int64_t)row * p.bm_stride;
@@ -272,28 +322,20 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelectParams p) 
     // than one selection holds, groups of 8^level blocks are ranked by their
     // maximum first; each level expands the P best groups into their 8
     // sub-groups and keeps the P best of those.
-    int level = 0, span = 1;
-    for (int64_t ng = nb; ng > kSelCap; ng = (ng + kBlock - 1) / kBlock) {
-      ++level;
-      span *= kBlock;
-    }
-    const int64_t ng = (nb + span - 1) / span;
-    fill_keys(sm, t, [&](int e) -> uint32_t {
-      const int64_t g = base + e;
-      return g < ng ? (span == 1 ? order_key(__ldg(bm + g)) : group_key(bm, nb, g, span)) : 0u;
+    int span = 1;
+    for (int64_t ng = nb; ng > kSelCap; ng = (ng + kBlock - 1) / kBlock) span *= kBlock;
+    const int ng = (int)((nb + span - 1) / span);
+    fill_keys(sm, ng, [&](int g) -> uint32_t {
+      return span == 1 ? order_key(__ldg(bm + g)) : group_key(bm, nb, g, span);
     });
-    __syncthreads();
-    block_select(sm, (int)ng, P);
+    block_select(sm, ng, P);
     for (int i = t; i < P; i += kSelThreads) sm.list[i] = sm.sel[i];
     __syncthreads();
     for (; span > 1; span /= kBlock) {
       const int sub = span / kBlock;
-      fill_keys(sm, t, [&](int e) -> uint32_t {
-        const int c = base + e;
-        return c < P * kBlock ? group_key(bm, nb, (int64_t)sm.list[c / kBlock] * kBlock + c % kBlock, sub)
-                              : 0u;
+      fill_keys(sm, P * kBlock, [&](int c) -> uint32_t {
+        return group_key(bm, nb, (int64_t)sm.list[c / kBlock] * kBlock + c % kBlock, sub);
       });
-      __syncthreads();
       block_select(sm, P * kBlock, P);
       int nid[(kPoolBlocks + kSelThreads - 1) / kSelThreads];
 #pragma unroll
@@ -315,13 +357,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelectParams p) 
     }
     if (p.pool_cnt_out && t == 0) p.pool_cnt_out[orow] = P;
     // ---- top-k over the pool's positions
-    fill_keys(sm, t, [&](int e) -> uint32_t {
-      const int c = base + e;
-      if (c >= P * kBlock) return 0u;
+    fill_keys(sm, P * kBlock, [&](int c) -> uint32_t {
       const int pos = sm.list[c / kBlock] * kBlock + (c % kBlock);
       return pos < len ? order_key(__ldg(sc + pos)) : 0u;
     });
-    __syncthreads();
     block_select(sm, P * kBlock, kk);
     int32_t* oi = p.out_idx + orow * p.k;
     for (int i = t; i < kk; i += kSelThreads) oi[i] = sm.list[sm.sel[i] / kBlock] * kBlock + sm.sel[i] % kBlock;
@@ -333,16 +372,14 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelectParams p) 
     const float* cd = p.cand + (int64_t)row * kPoolPositions;
     for (int i = t; i < pc; i += kSelThreads) sm.list[i] = pool[i];
     __syncthreads();
-    fill_keys(sm, t, [&](int e) -> uint32_t {
-      const int c = base + e;
-      if (c >= pc * kBlock) return 0u;
+    int nvalid = 0;
+    fill_keys(sm, pc * kBlock, [&](int c) -> uint32_t {
       const int blk = sm.list[c / kBlock];
       const int64_t pos = (int64_t)blk * kBlock + (c % kBlock);
       return (blk >= 0 && pos < len) ? order_key(__ldg(cd + c)) : 0u;
     });
-    int nvalid = 0;
-    for (int e = 0; e < kSelE; ++e) nvalid += key_at(sm, t, e) != 0u;
-    nvalid = block_sum(nvalid, sm.red);  // includes a barrier
+    for (int i = t; i < pc * kBlock; i += kSelThreads) nvalid += sm.keys[key_slot(i)] != 0u;
+    nvalid = block_sum(nvalid, sm.red);
     const int kk = p.k < nvalid ? p.k : nvalid;
     block_select(sm, pc * kBlock, kk);
     int32_t* oi = p.out_idx + orow * p.k;
