@@ -59,6 +59,9 @@ _fp8_quant = _sig("csa2_fp8_quant", [_p, _i64, _p, _p])
 _quant_append = _sig("csa2_quant_append", [_CP, _p, _p, _i32, _p, _p])
 _index_full = _sig("csa2_index_full", [_CP, _p, _p, _i32, _i32, _p, _p, _i32, _i32,
                                        _p, _p, _p, _p, _p, _p])
+_index_full_noalloc = _sig("csa2_index_full_noalloc", [_CP, _p, _p, _i32, _i32, _p, _p, _i32,
+                                                       _i32, _p, _p, _p, _p, _p, _p])
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 _index_reindex = _sig("csa2_index_reindex", [_CP, _p, _p, _i32, _i32, _p, _p, _p, _p, _i32,
                                              _i32, _p, _p, _p, _p])
 _attn_decode = _sig("csa2_attn_decode", [_CP, _p, _i32, _p, _p, _i32, _p, _p, _i32,
@@ -74,7 +77,7 @@ KERNEL_QUANT, KERNEL_INDEXER, KERNEL_SELECT, KERNEL_ATTENTION = 0, 1, 2, 3
 EXPORTED = ["csa2_workspace_size", "csa2_entry_bytes", "csa2_fp8_quant", "csa2_quant_append",
             "csa2_index_full", "csa2_index_reindex", "csa2_attn_decode", "csa2_attn_prefill",
             "csa2_get_status", "csa2_reset_status", "csa2_status_string",
-            "csa2_set_launch_events"]
+            "csa2_set_launch_events", "csa2_index_full_noalloc"]
 
 
 class Csa2Error(RuntimeError):
@@ -133,6 +136,17 @@ def index_full(cache, q_idx, w, hi, tq, q_pos, batch_ids, n_batch, k, out_idx, o
                        _ptr(batch_ids), n_batch, k, _ptr(out_idx), _ptr(out_cnt),
                        _ptr(pool_blocks), _ptr(pool_cnt), _ptr(ws), _stream(stream)),
            "csa2_index_full")
+
+
+def index_full_noalloc(cache, q_idx, w, hi, tq, q_pos, batch_ids, n_batch, k, out_idx, out_cnt,
+                       pool_blocks, pool_cnt, status, stream=None):
+    """index_full for callers that may not allocate device memory: the scratch
+    is a fixed array inside the library; ``status`` (a 4-byte device tensor or
+    None) receives the call's device status word."""
+    _check(_index_full_noalloc(ctypes.byref(cache.struct), _ptr(q_idx), _ptr(w), hi, tq,
+                               _ptr(q_pos), _ptr(batch_ids), n_batch, k, _ptr(out_idx),
+                               _ptr(out_cnt), _ptr(pool_blocks), _ptr(pool_cnt), _ptr(status),
+                               _stream(stream)), "csa2_index_full_noalloc")
 
 
 def index_reindex(cache, q_idx, w, hi, tq, q_pos, pool_blocks, pool_cnt, batch_ids, n_batch, k,

@@ -3,6 +3,8 @@
 #include <math.h>
 #include <stdio.h>
 
+#include <mutex>
+
 #include "launch.h"
 
 using namespace csa2;
@@ -222,3 +224,73 @@ const char* csa2_status_string(csa2_status status) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- index_full without a workspace
+//
+// csa2_index_full_noalloc serves callers that are handed their device buffers
+// and may not create more: a host engine that reserves the GPU's memory for
+// its own pools at start-up and forbids side allocations, or a hot loop that
+// cannot take the implicit device synchronisation and unbounded latency of a
+// cudaMalloc.  Its scratch (status word, per-row lengths, scores, block
+// maxima) lives in one fixed array of CSA2_NOALLOC_SCRATCH_BYTES bytes that
+// every GPU loading this library's device code holds until the process exits.
+// All calls on a device share that array and it keeps the previous call's
+// contents; only the status word must start at zero and each call clears it.
+// Two calls whose work overlaps on the GPU (different streams, or threads that
+// do not order their streams) race on the array.
+namespace {
+
+__device__ __align__(256) uint8_t g_noalloc_scratch[CSA2_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoallocMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  Looked up once
+// per device (with that device current); the first lookup may load this
+// library's device code onto the device.
+cudaError_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    // The host-side name of the array only identifies it; the device address
+    // comes from the runtime.
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    if ((reinterpret_cast<uintptr_t>(p) & 255) != 0) return cudaErrorMisalignedAddress;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" csa2_status csa2_index_full_noalloc(
+    const csa2_cache* cache, const uint8_t* q_idx, const float* w, int32_t Hi, int32_t Tq,
+    const int32_t* q_pos, const int32_t* batch_ids, int32_t n_batch, int32_t k, int32_t* out_idx,
+    int32_t* out_cnt, int32_t* pool_blocks, int32_t* pool_cnt, uint32_t* status, void* stream) {
+  if (!cache_ok(cache) || Tq < 1 || n_batch < 0 || n_batch > cache->batch) return CSA2_ERR_INVALID;
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3) != 0) return CSA2_ERR_INVALID;
+  // The indexer and the selection use the workspace only up to the split-K
+  // partials of the attention, so that prefix is what must fit.
+  const int64_t rows = (int64_t)n_batch * Tq;
+  if (rows > (1 << 24)) return CSA2_ERR_INVALID;
+  if (rows > 0 && layout_for(cache, rows).part_o > (size_t)CSA2_NOALLOC_SCRATCH_BYTES)
+    return CSA2_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return CSA2_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s) != cudaSuccess) return CSA2_ERR_CUDA;
+  const csa2_status r = csa2_index_full(cache, q_idx, w, Hi, Tq, q_pos, batch_ids, n_batch, k,
+                                        out_idx, out_cnt, pool_blocks, pool_cnt, scratch, stream);
+  if (r != CSA2_OK) return r;
+  if (status && cudaMemcpyAsync(status, scratch, sizeof(uint32_t), cudaMemcpyDefault, s) !=
+                    cudaSuccess)
+    return CSA2_ERR_CUDA;
+  return CSA2_OK;
+}

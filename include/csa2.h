@@ -153,7 +153,7 @@ csa2_status csa2_quant_append(const csa2_cache *cache, const float *kv, const fl
  * Steps 2-3, Full layer: score every visible position and select.
  * q_idx:    device E4M3 [B, Tq, Hi, di] indexer queries.
  * w:        device fp32 [B, Tq, Hi] head weights.
- * Hi:       indexer heads, 1..128.
+ * Hi:       indexer heads, 1..64.
  * q_pos:    device int32 [B, Tq] inclusive causal limit per query, or NULL for
  *           decode (visible = [0, seq_len[b])).
  * batch_ids, n_batch: device int32 subset of sequences to process, or NULL
@@ -176,6 +176,38 @@ csa2_status csa2_index_full(const csa2_cache *cache, const uint8_t *q_idx, const
                             const int32_t *batch_ids, int32_t n_batch, int32_t k,
                             int32_t *out_idx, int32_t *out_cnt, int32_t *pool_blocks,
                             int32_t *pool_cnt, void *ws, void *stream);
+
+/*
+ * csa2_index_full without a caller workspace.  The paper has no counterpart:
+ * this entry point exists for callers that may not allocate device memory --
+ * an engine that hands this library only the buffers it reserved for it at
+ * start-up, or a latency-critical loop that cannot afford cudaMalloc's
+ * implicit synchronisation.  Arguments and results are those of
+ * csa2_index_full, with `ws` replaced by:
+ *   status: device (or pinned host) uint32, 4-byte aligned, or NULL; receives
+ *           this call's device status word (CSA2_DEV_* bits), stream ordered.
+ * The scratch is one fixed array of CSA2_NOALLOC_SCRATCH_BYTES inside the
+ * library, held by every GPU that loads the library's device code until the
+ * process exits; the call allocates no memory (no cudaMalloc, no library
+ * allocator).  With S = max_len rounded up to 128 and M = S/8 rounded up to
+ * 32, a call on rows = n_batch*Tq query rows needs about
+ * rows*(4*S + 4*M + 65536) + 1024 bytes (each part rounded up to 256 B),
+ * e.g. 32 rows at max_len 131,136 need 21 MB and one row at CSA2_MAX_LEN
+ * needs 9.5 MB; larger requests return CSA2_ERR_UNSUPPORTED with nothing
+ * launched.
+ * The first call on a device looks up the array's device address (and may
+ * load the library's device code there); make that first call before any
+ * stream capture.  Every call on a device shares the array and finds the
+ * previous call's contents in it; each call clears the status word it needs
+ * at zero.  Calls whose GPU work overlaps (other streams, unordered threads)
+ * race on the array: order them on one stream.
+ */
+#define CSA2_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+csa2_status csa2_index_full_noalloc(const csa2_cache *cache, const uint8_t *q_idx,
+                                    const float *w, int32_t Hi, int32_t Tq, const int32_t *q_pos,
+                                    const int32_t *batch_ids, int32_t n_batch, int32_t k,
+                                    int32_t *out_idx, int32_t *out_cnt, int32_t *pool_blocks,
+                                    int32_t *pool_cnt, uint32_t *status, void *stream);
 
 /*
  * Steps 2-3, Reindex layer: score only the pool's visible positions with this
