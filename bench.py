@@ -8,10 +8,12 @@ selected FP4 rows plus the FP8 window.  The default workload is the
 
   python bench.py [--steps K] [--warmup W] [--workload 2|3|5|1] [--impl reference]
 
-`value` is layer-steps/s with inputs resident in HBM (CUDA events around K
-steps); `e2e` repeats the K steps through the same C-ABI calls with the
-step's inputs copied from pinned host memory and the attention output read
-back every step.  `roofline` is for the indexer kernel (the dominant one),
+`value` is layer-steps/s with inputs resident in HBM: the K steps' C-ABI
+calls are captured once into a CUDA graph, which is replayed between CUDA
+events (`--eager` issues every call from the host instead).  `e2e` repeats
+the steps through the same calls with each step's inputs copied from pinned
+host memory and the attention output read back, also as a graph (the eager
+figure is reported beside it).  `roofline` is for the indexer kernel (the dominant one),
 timed live with CUDA events around each of its launches.  Under torchrun
 every rank runs an independent replica (the path does not shard: one GPU per
 problem); the JSON line reports the whole job.
@@ -314,6 +316,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="use only the first B sequences")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every step from the host instead of replaying a CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -340,9 +344,14 @@ def main():
         torch.cuda.synchronize()
 
     # ---- device-resident timed loop
+    def run_steps(n, evs=None, evas=None, state=None):
+        count = 0
+        for i in range(n):
+            count += step(state or st, evs[i] if evs else None, evas[i] if evas else None)
+        return count
+
     reset()
-    for _ in range(args.warmup):
-        step(st)
+    run_steps(args.warmup)            # eager warm-up: loads every kernel before any capture
     reset()
     n_start = list(wl.lengths)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -352,6 +361,18 @@ def main():
     for a, b in ev + eva:   # torch creates the CUDA event on the first record
         a.record()
         b.record()
+    torch.cuda.synchronize()
+    graph = None
+    if not args.eager:
+        # The K timed steps, unrolled into one CUDA graph; the per-step kernel
+        # events are external records, i.e. event nodes timed on every replay.
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            launches = run_steps(args.steps, ev, eva)
+        reset()
+        graph.replay()                # warm-up replay (untimed)
+        torch.cuda.synchronize()
+        reset()
     t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     if world > 1:
@@ -360,9 +381,10 @@ def main():
     clocks.start()
     time.sleep(0.3)
     t_begin.record()
-    launches = 0
-    for i in range(args.steps):
-        launches += step(st, ev[i], eva[i])
+    if graph is not None:
+        graph.replay()
+    else:
+        launches = run_steps(args.steps, ev, eva)
     t_end.record()
     torch.cuda.synchronize()
     time.sleep(0.1)
@@ -383,6 +405,7 @@ def main():
     ms_step = ms / args.steps
     value = world * layers_per_step(wl) * args.steps / (ms * 1e-3)
     path_gbs = sum(roof_bytes) / (ms * 1e-3) / 1e9
+    del graph
 
     # ---- end-to-end through the C ABI with host buffers
     reset()
@@ -402,27 +425,46 @@ def main():
     st_e2e["new_kv"], st_e2e["new_idx"] = dev["new_kv"], dev["new_idx"]
     st_e2e["inputs"] = [{n: dev[f"{n}{L}"] for n in ("q_idx", "w", "q", "swa")} for L in range(len(ins))]
     e_steps = max(args.steps // 4, 20)
-    for _ in range(3):
-        for name in host:
-            dev[name].copy_(host[name], non_blocking=True)
-        step(st_e2e)
+
+    def e2e_steps(n):
+        for _ in range(n):
+            for name in host:
+                dev[name].copy_(host[name], non_blocking=True)
+            step(st_e2e)
+            for o, src in zip(outs, st["out"]):
+                o.copy_(src, non_blocking=True)
+
+    def timed(fn):
+        reset()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e_ms], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        return world * layers_per_step(wl) * e_steps / (e_ms * 1e-3)
+
     reset()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(e_steps):
-        for name in host:
-            dev[name].copy_(host[name], non_blocking=True)
-        step(st_e2e)
-        for o, src in zip(outs, st["out"]):
-            o.copy_(src, non_blocking=True)
-    e1.record()
-    torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e_ms = float(t.item())
-    e2e_value = world * layers_per_step(wl) * e_steps / (e_ms * 1e-3)
+    e2e_steps(3)
+    e2e_eager = timed(lambda: e2e_steps(e_steps))
+    e2e_graph, e2e_note = None, None
+    if not args.eager:
+        try:
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g2, capture_error_mode="thread_local"):
+                e2e_steps(e_steps)
+            reset()
+            g2.replay()
+            e2e_graph = timed(g2.replay)
+            del g2
+        except Exception as exc:   # report the eager figure and why
+            e2e_note = f"graph capture of the copies failed: {type(exc).__name__}: {exc}"[:200]
+            torch.cuda.synchronize()
+    e2e_value = e2e_graph if e2e_graph is not None else e2e_eager
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -438,6 +480,7 @@ def main():
             "config": {"workload": wl.name, "batch": B, "ctx": max(n_start), "topk": wl.topk,
                        "window": wl.window, "dim": wl.dim, "idx_heads": wl.idx_heads,
                        "heads": wl.heads, "parallelism": "replicas" if world > 1 else "single",
+                       "launch": "eager" if args.eager else "cuda_graph",
                        "l2": f"inputs exceed L2 ({roof_bytes[0] / 1e6:.0f} MB read per step)"},
             "roofline": {"bound": "hbm", "kernel": "indexer_kernel", "achieved": ach, "peak": peak,
                          "unit": "GB/s", "frac": ach / peak, "traffic": None,
@@ -449,7 +492,9 @@ def main():
             "kernels_us": {"indexer": statistics.mean(idx_ms) * 1e3,
                            "attention": statistics.mean(attn_ms) * 1e3},
             "e2e": {"value": e2e_value, "unit": "layer-steps/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e_steps},
+                    "d2h_bytes_per_step": d2h, "steps": e_steps,
+                    "cuda_graph": e2e_graph is not None, "eager_value": e2e_eager,
+                    **({"note": e2e_note} if e2e_note else {})},
             "gpu_launches": launches,
             "clocks": clk,
             "device_status": status,

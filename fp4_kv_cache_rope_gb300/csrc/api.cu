@@ -60,11 +60,21 @@ cudaEvent_t g_events[4][2] = {};
 }  // namespace
 
 namespace csa2 {
+// Under stream capture the records are external, so that they become event
+// nodes timing every replay instead of capture-internal dependencies; the
+// external flag is only valid while the stream is capturing.
+static void record_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, s);
+}
 void record_launch_begin(int family, cudaStream_t s) {
-  if (g_events[family][0]) cudaEventRecord(g_events[family][0], s);
+  if (g_events[family][0]) record_event(g_events[family][0], s);
 }
 void record_launch_end(int family, cudaStream_t s) {
-  if (g_events[family][1]) cudaEventRecord(g_events[family][1], s);
+  if (g_events[family][1]) record_event(g_events[family][1], s);
 }
 }  // namespace csa2
 

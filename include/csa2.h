@@ -267,7 +267,9 @@ csa2_status csa2_reset_status(void *ws, void *stream);
  * on the stream of the call that launches it.  Families:
  *   CSA2_KERNEL_QUANT (step 1), CSA2_KERNEL_INDEXER (step 2),
  *   CSA2_KERNEL_SELECT (step 3), CSA2_KERNEL_ATTENTION (steps 4-5).
- * begin/end are cudaEvent_t passed as void*; NULL/NULL turns it off.
+ * begin/end are cudaEvent_t passed as void*; NULL/NULL turns it off.  While
+ * the stream is being captured the records are external
+ * (cudaEventRecordExternal): event nodes that time every replay of the graph.
  * Process-wide setting, not thread safe; it does not change any result.
  */
 #define CSA2_KERNEL_QUANT 0
