@@ -33,6 +33,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HBM_FALLBACK_GBS = 6800.0
+# DRAM bytes (read + write) per visible position of indexer_kernel<64,128>,
+# from one ncu capture of that kernel on 8 of the 32 sequences of the 128K
+# decode workload (134.51 MB read + 5.00 MB written for 1,048,584 positions;
+# profiles/indexer_kernel_full-decode-b8-n131072.md).  Scaled to a launch by
+# its visible positions; must be re-measured whenever the kernel changes.
+INDEXER_TRAFFIC_B_PER_POS = 139.5133e6 / 1048584
 
 
 def peaks():
@@ -401,6 +407,9 @@ def main():
     idx_bytes = [indexer_bytes_per_launch(wl, [n + i + 1 for n in n_start]) for i in range(args.steps)]
     roof_bytes = [roofline_bytes_per_step(wl, [n + i + 1 for n in n_start]) for i in range(args.steps)]
     ach = sum(idx_bytes) / (sum(idx_ms) * 1e-3) / 1e9
+    traffic = None
+    if wl.idx_heads == 64 and wl.idx_dim == 128:
+        traffic = INDEXER_TRAFFIC_B_PER_POS * statistics.mean(idx_bytes) / wl.idx_dim
     peak, peak_kind = peaks()
     ms_step = ms / args.steps
     value = world * layers_per_step(wl) * args.steps / (ms * 1e-3)
@@ -483,7 +492,7 @@ def main():
                        "launch": "eager" if args.eager else "cuda_graph",
                        "l2": f"inputs exceed L2 ({roof_bytes[0] / 1e6:.0f} MB read per step)"},
             "roofline": {"bound": "hbm", "kernel": "indexer_kernel", "achieved": ach, "peak": peak,
-                         "unit": "GB/s", "frac": ach / peak, "traffic": None,
+                         "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
                          "peak_source": peak_kind,
                          "bytes_per_launch": statistics.mean(idx_bytes),
                          "launch_us": statistics.mean(idx_ms) * 1e3},
