@@ -138,7 +138,7 @@ static csa2_status index_common(const csa2_cache* cache, int mode, const uint8_t
                                  num_sms(), s);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
   e = launch_select(*cache, rs, mode, k, pool_in, pool_cnt_in, out_idx, out_cnt, pool_out,
-                    pool_cnt_out, L, wsb, s);
+                    pool_cnt_out, L, wsb, num_sms(), s);
   return from_cuda(e);
 }
 

@@ -39,7 +39,7 @@ cudaError_t launch_indexer(const csa2_cache& c, const RowSet& rows, int mode,
 cudaError_t launch_select(const csa2_cache& c, const RowSet& rows, int mode, int32_t k,
                           const int32_t* pool_in, const int32_t* pool_cnt_in, int32_t* out_idx,
                           int32_t* out_cnt, int32_t* pool_out, int32_t* pool_cnt_out,
-                          const WsLayout& L, uint8_t* ws, cudaStream_t s);
+                          const WsLayout& L, uint8_t* ws, int num_sms, cudaStream_t s);
 
 // attention.cu
 struct AttnArgs {
