@@ -35,10 +35,10 @@ sys.path.insert(0, ROOT)
 HBM_FALLBACK_GBS = 6800.0
 # DRAM bytes (read + write) per visible position of indexer_kernel<64,128>,
 # from one ncu capture of that kernel on 8 of the 32 sequences of the 128K
-# decode workload (134.51 MB read + 5.00 MB written for 1,048,584 positions;
+# decode workload (134.51 MB read + 4.80 MB written for 1,048,584 positions;
 # the indexer summary under profiles/).  Scaled to a launch by its visible
 # positions; must be re-measured whenever the kernel changes.
-INDEXER_TRAFFIC_B_PER_POS = 139.5133e6 / 1048584
+INDEXER_TRAFFIC_B_PER_POS = 139.305472e6 / 1048584
 
 
 def peaks():

@@ -127,8 +127,25 @@ struct IdxCfg {
   static constexpr int kAccCols = 2 * HP < 32 ? 32 : 2 * HP;
   static constexpr int kTmemCols = kAccCols <= 32 ? 32 : (kAccCols <= 64 ? 64 : (kAccCols <= 128 ? 128 : 256));
   static constexpr int kBarOff = kStages * kStageBytes + 2 * kQBytes;
-  static constexpr int kSmem = kBarOff + 256;
+  // mbarriers: full/empty per stage, qfull/qempty/tfull/tempty x2, drain;
+  // then the abort flag and the TMEM address slot (one word each)
+  static constexpr int kNumBars = 2 * kStages + 8 + 1;
+  static constexpr int kBarBytes = (kNumBars * 8 + 8 + 127) / 128 * 128;
+  static constexpr int kSmem = kBarOff + kBarBytes;
+  static_assert(kSmem <= 227 * 1024, "indexer shared memory exceeds the per-CTA limit");
 };
+
+// (d0, d1) += (w0, w1) * (max(x0, 0), max(x1, 0)) with one packed fp32 FMA
+// (fma.rn per element, the same rounding as two fmaf calls).
+__device__ __forceinline__ void fma2_relu(float& d0, float& d1, float w0, float w1, float x0,
+                                          float x1) {
+  const float a0 = fmaxf(x0, 0.0f), a1 = fmaxf(x1, 0.0f);
+  asm("{\n\t.reg .b64 xa, xb, xc;\n\t"
+      "mov.b64 xa, {%2, %3};\n\tmov.b64 xb, {%4, %5};\n\tmov.b64 xc, {%0, %1};\n\t"
+      "fma.rn.f32x2 xc, xa, xb, xc;\n\tmov.b64 {%0, %1}, xc;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(w0), "f"(w1), "f"(a0), "f"(a1));
+}
 
 // First row whose tile range contains tile t (tile_prefix is non-decreasing).
 __device__ __forceinline__ int find_row(const int32_t* prefix, int n_rows, int t) {
@@ -363,11 +380,14 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty + acc);
-        // four independent partial sums over the heads, then their sum
+        // four independent partial sums over the heads (head h into s4[h % 4]),
+        // two at a time with the packed fp32 FMA, then their sum.  The
+        // epilogue's instruction count is on the kernel's critical path.
         float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int h = 0; h < HP; ++h)
-          s4[h & 3] = fmaf(wv[h], fmaxf(__uint_as_float(r[h]), 0.0f), s4[h & 3]);
+        for (int h = 0; h < HP; h += 2)
+          fma2_relu(s4[h & 3], s4[(h & 3) + 1], wv[h], wv[h + 1], __uint_as_float(r[h]),
+                    __uint_as_float(r[h + 1]));
         const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         const int j = t - rc.begin;
         const int local = 32 * quad + lane;
