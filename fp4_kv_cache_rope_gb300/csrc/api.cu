@@ -52,7 +52,7 @@ int num_sms() {
 csa2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
 
 WsLayout layout_for(const csa2_cache* c, int64_t rows) {
-  return ws_layout(c->max_len, rows, 64, c->dim);
+  return ws_layout(c->max_len, rows);
 }
 
 cudaEvent_t g_events[4][2] = {};
@@ -167,7 +167,8 @@ static csa2_status attn_common(const csa2_cache* cache, const uint16_t* q, int32
   if (!cache_ok(cache) || !q || !idx || !cnt || !out || !ws) return CSA2_ERR_INVALID;
   if (H < 1 || H > 64 || kcap < 0 || W < 0 || Tq < 1) return CSA2_ERR_INVALID;
   if (W > 0 && !swa) return CSA2_ERR_INVALID;
-  if (!aligned16(q) || !aligned16(ws) || (swa && !aligned16(swa))) return CSA2_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(ws) || !aligned16(out) || (swa && !aligned16(swa)))
+    return CSA2_ERR_INVALID;
   if (isnan(scale)) return CSA2_ERR_INVALID;
   const int64_t rows = (int64_t)cache->batch * Tq;
   AttnArgs a;
@@ -286,11 +287,9 @@ extern "C" csa2_status csa2_index_full_noalloc(
     int32_t* out_cnt, int32_t* pool_blocks, int32_t* pool_cnt, uint32_t* status, void* stream) {
   if (!cache_ok(cache) || Tq < 1 || n_batch < 0 || n_batch > cache->batch) return CSA2_ERR_INVALID;
   if (status && (reinterpret_cast<uintptr_t>(status) & 3) != 0) return CSA2_ERR_INVALID;
-  // The indexer and the selection use the workspace only up to the split-K
-  // partials of the attention, so that prefix is what must fit.
   const int64_t rows = (int64_t)n_batch * Tq;
   if (rows > (1 << 24)) return CSA2_ERR_INVALID;
-  if (rows > 0 && layout_for(cache, rows).part_o > (size_t)CSA2_NOALLOC_SCRATCH_BYTES)
+  if (rows > 0 && layout_for(cache, rows).total > (size_t)CSA2_NOALLOC_SCRATCH_BYTES)
     return CSA2_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   if (noalloc_scratch(&scratch) != cudaSuccess) return CSA2_ERR_CUDA;

@@ -17,7 +17,11 @@
 // rounded weights are summed for the normaliser.
 //
 // One CTA handles a contiguous range of 64-key chunks of one query row
-// (split-K over chunks; attn_combine_kernel merges the partial results).
+// (split-K over chunks).  The split CTAs of a row form one thread-block
+// cluster: each stages its unnormalised output and its per-head running
+// maximum and sum in shared memory, and after a cluster barrier every CTA
+// merges a slice of the channels from all of them through distributed
+// shared memory and writes the output.
 // Nine warps, three roles:
 //   data warps 4-7     gather each key's code and scale bytes (or window row)
 //                      with plain vector loads one chunk ahead (index
@@ -51,7 +55,9 @@ struct AttnCfg {
   static constexpr int kXOff = kXBytes;          // two X tiles follow Q
   static constexpr int kPOff = 3 * kXBytes;
   static constexpr int kMiscOff = kPOff + kSlab;
-  static constexpr int kSmem = kMiscOff + 1024;
+  static constexpr int kMiscBytes = 2048;
+  static constexpr int kSmem = kMiscOff + kMiscBytes;
+  static_assert(2 * kXBytes >= 64 * D * 4, "the X tiles hold the merge stage");
   static constexpr int kSCols = 2 * 64;          // two S buffers
   static constexpr int kCols = kSCols + 64 * NT;
   static constexpr int kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
@@ -70,9 +76,7 @@ struct AttnParams {
   int32_t window;
   float scale_log2;  // softmax scale * log2(e)
   float* out;
-  float* part_o;
-  float* part_ml;
-  int32_t splits;
+  int32_t splits;    // CTAs per query row (the cluster size)
   const uint8_t* codes;
   const uint8_t* scales;
   int64_t code_stride, scale_stride;
@@ -115,6 +119,8 @@ __device__ __forceinline__ RowKeys row_keys(const AttnParams& p, int row, int D)
   return r;
 }
 
+constexpr int kLrowOff = 128 + 2 * 64 * 4;  // lrow's byte offset in the misc area
+
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -141,6 +147,27 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // a slab at chunk position c (0..7).
 __device__ __forceinline__ void st_swz(uint8_t* slab, int row, int c, uint4 v) {
   *reinterpret_cast<uint4*>(slab + row * 128 + ((c ^ (row & 7)) << 4)) = v;
+}
+
+// 4-byte store at byte `b` (a multiple of 4) of 16-byte column c of a
+// swizzled slab row.
+__device__ __forceinline__ void st_swz4(uint8_t* slab, int row, int c, int b, uint32_t v) {
+  *reinterpret_cast<uint32_t*>(slab + row * 128 + ((c ^ (row & 7)) << 4) + b) = v;
+}
+
+// 16 tensor-memory lanes x 64 columns (16x256b shape, 8 repeats): thread t
+// gets lanes t/4 (registers 4k, 4k+1) and t/4 + 8 (registers 4k+2, 4k+3),
+// columns 8k + 2(t%4) and 8k + 2(t%4) + 1.
+__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
 }
 
 // Where one key's bytes live: kind 0 = absent, 1 = FP4 cache row, 2 = FP8
@@ -181,6 +208,98 @@ __device__ __forceinline__ void rescale_output(uint32_t tO, int quad, const floa
   tc_fence_before();
 }
 
+// Split-K merge over the cluster of a query row:
+//   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s   per head,
+// M the largest m_s with l_s > 0.  Every CTA has staged its unnormalised
+// output [64][D] fp32 over its X tiles and its per-head (m, l); this CTA
+// writes the channels [D*r/C, D*(r+1)/C) (in float4 columns).  Kept out of
+// line so that nothing of it is live in the main loops.
+template <int NSLAB>
+__device__ __noinline__ void merge_splits(const AttnParams& p) {
+  using C_ = AttnCfg<NSLAB>;
+  constexpr int D = C_::D;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const float* st = reinterpret_cast<const float*>(smem + C_::kXOff);
+  float* wgt = reinterpret_cast<float*>(smem + C_::kPOff);  // [kMaxSplits][64] merge weights
+  float* inv_den = wgt + kMaxSplits * 64;                  // [64]
+  const float* lrow = reinterpret_cast<const float*>(smem + C_::kMiscOff + kLrowOff);
+  const float* mrow = lrow + 64;
+  const int tid = threadIdx.x, row = blockIdx.y, r = blockIdx.x, C = p.splits;
+  cluster_sync();  // every CTA's stage, mrow and lrow are written
+  if (tid < 64) {
+    float m[kMaxSplits], l[kMaxSplits];
+    float M = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kMaxSplits; ++u) {
+      m[u] = -INFINITY;
+      l[u] = 0.0f;
+      if (u < C) {
+        m[u] = peer_f32(&mrow[tid], u);
+        l[u] = peer_f32(&lrow[tid], u);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kMaxSplits; ++u)
+      if (l[u] > 0.0f) M = fmaxf(M, m[u]);
+    float den = 0.0f;
+#pragma unroll
+    for (int u = 0; u < kMaxSplits; ++u) {
+      const float w = l[u] > 0.0f ? exp2f(m[u] - M) : 0.0f;
+      wgt[u * 64 + tid] = w;
+      den += w * l[u];
+    }
+    inv_den[tid] = den > 0.0f ? 1.0f / den : 0.0f;
+  }
+  __syncthreads();
+  constexpr int n4 = D / 4;
+  const int q0 = n4 * r / C, q1 = n4 * (r + 1) / C, nq = q1 - q0;
+  const int items = p.heads * nq;
+  // four outputs per thread at a time, each reading the C stages: up to 16
+  // remote float4 loads in flight
+#pragma unroll 1
+  for (int i0 = tid; i0 < items; i0 += 4 * blockDim.x) {
+#pragma unroll 1
+    for (int u0 = 0; u0 < C; u0 += 4) {
+      float4 v[4][4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int i = i0 + a * blockDim.x;
+        const int hh = i / nq, d = 4 * (q0 + i - hh * nq);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (i < items && u0 + j < C) v[a][j] = peer_f32x4(st + hh * D + d, u0 + j);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int i = i0 + a * blockDim.x;
+        if (i >= items) continue;
+        const int hh = i / nq, d = 4 * (q0 + i - hh * nq);
+        float4 num = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        float4* dst = reinterpret_cast<float4*>(p.out + ((int64_t)row * p.heads + hh) * D + d);
+        if (u0 > 0) num = *dst;  // more than four splits: continue the sum
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (u0 + j < C) {
+            const float w = wgt[(u0 + j) * 64 + hh];
+            if (w != 0.0f) {
+              num.x += w * v[a][j].x;
+              num.y += w * v[a][j].y;
+              num.z += w * v[a][j].z;
+              num.w += w * v[a][j].w;
+            }
+          }
+        }
+        if (u0 + 4 >= C) {
+          const float id = inv_den[hh];
+          num = make_float4(num.x * id, num.y * id, num.z * id, num.w * id);
+        }
+        *dst = num;
+      }
+    }
+  }
+  cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+}
+
 template <int NSLAB>
 __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
   using C = AttnCfg<NSLAB>;
@@ -206,7 +325,8 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
   uint32_t* vmask = reinterpret_cast<uint32_t*>(misc + 112);     // [2][2]
   float* qmul = reinterpret_cast<float*>(misc + 128);            // [64]
   float* alpha = qmul + 64;                                      // [64]
-  float* lrow = alpha + 64;                                      // [64]  (ends at misc + 896)
+  float* lrow = alpha + 64;                                      // [64] at misc + kLrowOff
+  float* mrow = lrow + 64;                                       // [64]  (ends at misc + 1152)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   if ((smem_u32(smem) & 1023u) != 0) {
@@ -252,6 +372,56 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
     // =============================================================== data warps
     const int dt = tid - 128;     // 0..127
     const int quad = warp & 3;    // TMEM lane quadrant of this warp
+    // ---- gather / dequantise pipeline (its first index entries and rows are
+    // requested before the query conversion, which hides their latency)
+    const int j = dt & 63, sgrp = dt >> 6;
+    auto resolve_pos = [&](int c) -> int {  // chunk-local c -> index entry (or -1)
+      const int g = (c0 + c) * C::kKeys + j;
+      return (c < nloc && g < rk.n_global) ? __ldg(p.idx + (int64_t)row * p.kcap + g) : -1;
+    };
+    auto resolve_src = [&](int c, int pos) -> KeySrc {
+      KeySrc k{nullptr, nullptr, 0};
+      if (c >= nloc) return k;
+      const int g = (c0 + c) * C::kKeys + j;
+      if (g < rk.n_global) {
+        if (pos >= 0 && pos < rk.vis) {
+          const int64_t r = p.map.row(rk.b, pos);
+          if (r >= 0) {
+            k.a = p.codes + r * p.code_stride;
+            k.s = p.scales + r * p.scale_stride;
+            k.kind = 1;
+          } else if (sgrp == 0) {
+            set_status(p.status, CSA2_DEV_BAD_PAGE);
+          }
+        } else if (sgrp == 0) {
+          set_status(p.status, CSA2_DEV_BAD_INDEX);
+        }
+      } else if (g < nk) {
+        k.a = rk.swa0 + (int64_t)(g - rk.n_global) * D;
+        k.kind = 2;
+      }
+      return k;
+    };
+    auto load_raw = [&](const KeySrc& k, RawKey<NP>& raw) {
+      if (k.kind == 1) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+          const int s = sgrp + 2 * i;
+          if (s < NSLAB) {
+            raw.c0[i] = __ldg(reinterpret_cast<const uint4*>(k.a + s * 32));
+            raw.c1[i] = __ldg(reinterpret_cast<const uint4*>(k.a + s * 32 + 16));
+            raw.sc[i] = __ldg(reinterpret_cast<const uint32_t*>(k.s + s * 4));
+          }
+        }
+      }
+    };
+    // pipeline registers: raw bytes of chunk it+1, source of chunk it+2,
+    // index entry of chunk it+3
+    RawKey<NP> raw;
+    KeySrc src_next = resolve_src(0, resolve_pos(0));
+    load_raw(src_next, raw);
+    KeySrc src_n1 = resolve_src(1, resolve_pos(1));
+    int pos3 = resolve_pos(2);
     // ---- query: f16 copy of the bf16 rows.  When some |q| >= 2^14 the head
     // is scaled by a power of two so that its f16 copy stays exact.
     bool ok = mbar_wait(q_full, 0, abort_flag);
@@ -340,55 +510,6 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
     fence_async_smem();
     named_sync(1, 288);  // Q slabs written; X tile 1 free again
 
-    // ---- gather / dequantise pipeline
-    const int j = dt & 63, sgrp = dt >> 6;
-    auto resolve_pos = [&](int c) -> int {  // chunk-local c -> index entry (or -1)
-      const int g = (c0 + c) * C::kKeys + j;
-      return (c < nloc && g < rk.n_global) ? __ldg(p.idx + (int64_t)row * p.kcap + g) : -1;
-    };
-    auto resolve_src = [&](int c, int pos) -> KeySrc {
-      KeySrc k{nullptr, nullptr, 0};
-      if (c >= nloc) return k;
-      const int g = (c0 + c) * C::kKeys + j;
-      if (g < rk.n_global) {
-        if (pos >= 0 && pos < rk.vis) {
-          const int64_t r = p.map.row(rk.b, pos);
-          if (r >= 0) {
-            k.a = p.codes + r * p.code_stride;
-            k.s = p.scales + r * p.scale_stride;
-            k.kind = 1;
-          } else if (sgrp == 0) {
-            set_status(p.status, CSA2_DEV_BAD_PAGE);
-          }
-        } else if (sgrp == 0) {
-          set_status(p.status, CSA2_DEV_BAD_INDEX);
-        }
-      } else if (g < nk) {
-        k.a = rk.swa0 + (int64_t)(g - rk.n_global) * D;
-        k.kind = 2;
-      }
-      return k;
-    };
-    auto load_raw = [&](const KeySrc& k, RawKey<NP>& raw) {
-      if (k.kind == 1) {
-#pragma unroll
-        for (int i = 0; i < NP; ++i) {
-          const int s = sgrp + 2 * i;
-          if (s < NSLAB) {
-            raw.c0[i] = __ldg(reinterpret_cast<const uint4*>(k.a + s * 32));
-            raw.c1[i] = __ldg(reinterpret_cast<const uint4*>(k.a + s * 32 + 16));
-            raw.sc[i] = __ldg(reinterpret_cast<const uint32_t*>(k.s + s * 4));
-          }
-        }
-      }
-    };
-    // pipeline registers: raw bytes of chunk it+1, source of chunk it+2,
-    // index entry of chunk it+3
-    RawKey<NP> raw;
-    KeySrc src_next = resolve_src(0, resolve_pos(0));
-    load_raw(src_next, raw);
-    KeySrc src_n1 = resolve_src(1, resolve_pos(1));
-    int pos3 = resolve_pos(2);
     for (int it = 0; it < nloc; ++it) {
       const int buf = it & 1;
       const KeySrc src_cur = src_next;
@@ -479,8 +600,10 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
     }
     tc_fence_after();
     named_sync(2, 288);  // lrow written by the softmax warps
-    // ---- epilogue: O^T tiles, 32 channels per warp per tile
-    const int slot = row * p.splits + split;
+    // ---- epilogue: O^T tiles, 32 channels per warp per tile; with several
+    // CTAs per row the unnormalised output goes to the stage [64][D] fp32
+    // (the X tiles, free now) for the cluster merge
+    float* stage = reinterpret_cast<float*>(sx);
 #pragma unroll 1
     for (int t = 0; t < C::NT; ++t) {
       const int s0 = (2 * t + 1 < NSLAB) ? 2 * t : NSLAB - 2;
@@ -508,7 +631,7 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
                 const float l = lrow[hh];
                 p.out[((int64_t)row * p.heads + hh) * D + d] = l > 0.0f ? acc / l : 0.0f;
               } else {
-                p.part_o[((int64_t)slot * 64 + hh) * D + d] = acc;
+                stage[hh * D + d] = acc;
               }
             }
           }
@@ -518,12 +641,16 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
   } else if (warp < 4) {
     // ============================================================ softmax warps
     // Row h of an M=64 accumulator sits in tensor-memory lane
-    // 32 * (h / 16) + h % 16: warp q, lanes 0-15, hold heads 16 q .. 16 q + 15.
-    const bool act = lane < 16;
-    const int h = 16 * warp + (lane & 15);
+    // 32 * (h / 16) + h % 16.  A 16x256b load gives thread t of warp q the
+    // rows (heads) hA = 16 q + t / 4 and hB = hA + 8, columns (keys)
+    // 8 k + 2 (t % 4) + {0, 1}: each head is spread over the four threads
+    // t % 4 = 0..3, each holding 16 of its 64 keys.  Running maxima agree
+    // over the four threads; the sums stay per thread until the end.
+    const int hA = 16 * warp + (lane >> 2), hB = hA + 8;
+    const int cq = 2 * (lane & 3);  // this thread's first key in each group of 8
     named_sync(1, 288);  // Q slabs written
-    float m_h = -INFINITY, l_h = 0.0f;
-    const float qm = qmul[h];
+    float mA = -INFINITY, mB = -INFINITY, lA = 0.0f, lB = 0.0f;
+    const float qmA = qmul[hA], qmB = qmul[hB];
     bool ok = true;
     int n_resc = 0;
     for (int it = 0; it < nloc; ++it) {
@@ -531,35 +658,52 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
       if (ok && !mbar_wait(s_full + buf, (it >> 1) & 1, abort_flag)) ok = false;
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after();
-      uint32_t sr[64];
-      float mx = -INFINITY;
+      uint32_t sr[32];
+      float mxA = -INFINITY, mxB = -INFINITY;
       if (ok) {
-#pragma unroll
-        for (int c = 0; c < 64; c += 16)
-          tmem_ld16(tmem + 64 * buf + c + ((uint32_t)(32 * warp) << 16),
-                    *reinterpret_cast<uint32_t(*)[16]>(&sr[c]));
+        tmem_ld_16x256b_x8(tmem + 64 * buf + ((uint32_t)(32 * warp) << 16), sr);
         tmem_ld_wait();
+        reg_fence(*reinterpret_cast<uint32_t(*)[16]>(&sr[0]));
+        reg_fence(*reinterpret_cast<uint32_t(*)[16]>(&sr[16]));
+        const uint64_t mask = (uint64_t)vmask[buf * 2] | ((uint64_t)vmask[buf * 2 + 1] << 32);
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) reg_fence(*reinterpret_cast<uint32_t(*)[16]>(&sr[c]));
-        const uint64_t mask = act ? ((uint64_t)vmask[buf * 2] | ((uint64_t)vmask[buf * 2 + 1] << 32)) : 0ull;
+        for (int k = 0; k < 8; ++k) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float v = ((mask >> c) & 1) ? __uint_as_float(sr[c]) * qm : -INFINITY;
-          sr[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          for (int e = 0; e < 2; ++e) {
+            const bool valid = (mask >> (8 * k + cq + e)) & 1;
+            const float vA = valid ? __uint_as_float(sr[4 * k + e]) * qmA : -INFINITY;
+            const float vB = valid ? __uint_as_float(sr[4 * k + 2 + e]) * qmB : -INFINITY;
+            sr[4 * k + e] = __float_as_uint(vA);
+            sr[4 * k + 2 + e] = __float_as_uint(vB);
+            mxA = fmaxf(mxA, vA);
+            mxB = fmaxf(mxB, vB);
+          }
         }
+        mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
+        mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
+        mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
+        mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
       }
       tc_fence_before();
       // lazily raised running maximum: rescale only when it jumps by > 2^8
       bool need = false;
-      float a = 1.0f;
-      if (mx > -INFINITY && (m_h == -INFINITY || mx > m_h + 8.0f)) {
+      float aA = 1.0f, aB = 1.0f;
+      if (mxA > -INFINITY && (mA == -INFINITY || mxA > mA + 8.0f)) {
         need = true;
-        a = (m_h == -INFINITY) ? 0.0f : fast_exp2(m_h - mx);
-        m_h = mx;
-        l_h *= a;
+        aA = (mA == -INFINITY) ? 0.0f : fast_exp2(mA - mxA);
+        mA = mxA;
+        lA *= aA;
       }
-      if (act) alpha[h] = a;
+      if (mxB > -INFINITY && (mB == -INFINITY || mxB > mB + 8.0f)) {
+        need = true;
+        aB = (mB == -INFINITY) ? 0.0f : fast_exp2(mB - mxB);
+        mB = mxB;
+        lB *= aB;
+      }
+      if ((lane & 3) == 0) {
+        alpha[hA] = aA;
+        alpha[hB] = aB;
+      }
       const bool resc_needed = named_sync_or(3, 128, need) && it > 0;
       if (tid == 0) need_resc[buf] = resc_needed ? 1 : 0;
       named_sync(3, 128);
@@ -572,22 +716,21 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
         ++n_resc;
       }
       ok = __all_sync(0xffffffffu, ok);
-      if (ok && act) {
+      if (ok) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t o[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float v0 = __uint_as_float(sr[8 * c + 2 * u]);
-            const float v1 = __uint_as_float(sr[8 * c + 2 * u + 1]);
-            const float e0 = v0 == -INFINITY ? 0.0f : fast_exp2(v0 - m_h);
-            const float e1 = v1 == -INFINITY ? 0.0f : fast_exp2(v1 - m_h);
-            __half2 h2 = __floats2half2_rn(e0, e1);
-            const float2 back = __half22float2(h2);
-            l_h += back.x + back.y;
-            o[u] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-          st_swz(sp, h, c, make_uint4(o[0], o[1], o[2], o[3]));
+        for (int k = 0; k < 8; ++k) {
+          const float vA0 = __uint_as_float(sr[4 * k]), vA1 = __uint_as_float(sr[4 * k + 1]);
+          const float vB0 = __uint_as_float(sr[4 * k + 2]), vB1 = __uint_as_float(sr[4 * k + 3]);
+          const float eA0 = vA0 == -INFINITY ? 0.0f : fast_exp2(vA0 - mA);
+          const float eA1 = vA1 == -INFINITY ? 0.0f : fast_exp2(vA1 - mA);
+          const float eB0 = vB0 == -INFINITY ? 0.0f : fast_exp2(vB0 - mB);
+          const float eB1 = vB1 == -INFINITY ? 0.0f : fast_exp2(vB1 - mB);
+          const __half2 pA = __floats2half2_rn(eA0, eA1), pB = __floats2half2_rn(eB0, eB1);
+          const float2 bA = __half22float2(pA), bB = __half22float2(pB);
+          lA += bA.x + bA.y;
+          lB += bB.x + bB.y;
+          st_swz4(sp, hA, k, 2 * cq, *reinterpret_cast<const uint32_t*>(&pA));
+          st_swz4(sp, hB, k, 2 * cq, *reinterpret_cast<const uint32_t*>(&pB));
         }
       }
       fence_async_smem();
@@ -595,13 +738,16 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
       named_sync(3, 128);
       if (lane == 0) mbar_arrive(p_full);
     }
-    if (act) {
-      lrow[h] = l_h;
-      if (!direct) {
-        const int slot = row * p.splits + split;
-        p.part_ml[((int64_t)slot * 64 + h) * 2 + 0] = (nloc > 0 && ok) ? m_h : -INFINITY;
-        p.part_ml[((int64_t)slot * 64 + h) * 2 + 1] = (nloc > 0 && ok) ? l_h : 0.0f;
-      }
+    // per-head sums over the four threads that hold the head
+    lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+    lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+    lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+    lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+    if ((lane & 3) == 0) {
+      lrow[hA] = (nloc > 0 && ok) ? lA : 0.0f;
+      mrow[hA] = (nloc > 0 && ok) ? mA : -INFINITY;
+      lrow[hB] = (nloc > 0 && ok) ? lB : 0.0f;
+      mrow[hB] = (nloc > 0 && ok) ? mB : -INFINITY;
     }
     named_sync(2, 288);
   } else {
@@ -676,44 +822,7 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
   tc_fence_after();
   if (warp == 8) tmem_dealloc(tmem, C::kTmemCols);
   if (tid == 0 && *abort_flag) set_status(p.status, CSA2_DEV_TIMEOUT);
-}
-
-// Merge of split-K partials: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-__global__ void __launch_bounds__(192) attn_combine_kernel(const float* __restrict__ part_o,
-                                                           const float* __restrict__ part_ml,
-                                                           float* __restrict__ out, int heads,
-                                                           int D, int splits) {
-  __shared__ float wgt[kMaxSplits];
-  __shared__ float inv_den;
-  const int row = blockIdx.x, h = blockIdx.y;
-  if (threadIdx.x < 32) {
-    const int s = threadIdx.x;
-    float m = -INFINITY, l = 0.0f;
-    if (s < splits) {
-      const int64_t slot = (int64_t)row * splits + s;
-      m = part_ml[(slot * 64 + h) * 2 + 0];
-      l = part_ml[(slot * 64 + h) * 2 + 1];
-    }
-    float M = l > 0.0f ? m : -INFINITY;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float w = (l > 0.0f) ? exp2f(m - M) : 0.0f;
-    float den = w * l;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    if (s < splits) wgt[s] = w;
-    if (s == 0) inv_den = den > 0.0f ? 1.0f / den : 0.0f;
-  }
-  __syncthreads();
-  const float id = inv_den;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float num = 0.0f;
-    for (int s = 0; s < splits; ++s) {
-      const float w = wgt[s];
-      if (w != 0.0f) num += w * part_o[(((int64_t)row * splits + s) * 64 + h) * D + d];
-    }
-    out[((int64_t)row * heads + h) * D + d] = num * id;
-  }
+  if (p.splits > 1) merge_splits<NSLAB>(p);
 }
 
 template <int NSLAB>
@@ -722,14 +831,22 @@ static cudaError_t run_attention(const AttnParams& p, cudaStream_t s) {
   auto kern = attention_kernel<NSLAB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.splits, p.n_rows);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.splits, (unsigned)p.n_rows, 1);
+  cfg.blockDim = dim3(288, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;  // the split CTAs of a row
+  attr[0].val.clusterDim.x = (unsigned)p.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   record_launch_begin(CSA2_KERNEL_ATTENTION, s);
-  kern<<<grid, 288, C::kSmem, s>>>(p);
+  e = cudaLaunchKernelEx(&cfg, kern, p);
   record_launch_end(CSA2_KERNEL_ATTENTION, s);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || p.splits == 1) return e;
-  dim3 g2(p.n_rows, p.heads);
-  attn_combine_kernel<<<g2, 192, 0, s>>>(p.part_o, p.part_ml, p.out, p.heads, C::D, p.splits);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -752,13 +869,10 @@ cudaError_t launch_attention(const csa2_cache& c, const AttnArgs& a, const WsLay
   const float scale = a.scale > 0.0f ? a.scale : 1.0f / sqrtf((float)c.dim);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.out = a.out;
-  p.part_o = reinterpret_cast<float*>(ws + L.part_o);
-  p.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
   int splits = num_sms / a.n_rows;
   splits = splits < 1 ? 1 : (splits > kMaxSplits ? kMaxSplits : splits);
   const int max_chunks = (a.kcap + a.window + 63) / 64;
   if (splits > max_chunks) splits = max_chunks < 1 ? 1 : max_chunks;
-  if ((int64_t)splits * a.n_rows > L.slots) splits = 1;
   p.splits = splits;
   p.codes = c.kv_codes;
   p.scales = c.kv_scales;

@@ -17,8 +17,7 @@ constexpr int kBlock = CSA2_BLOCK;          // positions per pool block
 constexpr int kPoolBlocks = CSA2_POOL_BLOCKS;
 constexpr int kMaxTopk = CSA2_MAX_TOPK;
 constexpr int kPoolPositions = kPoolBlocks * kBlock;   // 16,384 candidates
-constexpr int kMaxSplits = 16;              // attention split-K limit
-constexpr int kSplitSlots = 160;            // CTA budget used to size split-K partials
+constexpr int kMaxSplits = 8;               // attention split-K limit (one cluster per query row)
 constexpr uint64_t kWaitNs = 2000000000ull; // bounded on-chip waits give up after ~2 s
 
 // ------------------------------------------------------------------ workspace
@@ -30,22 +29,16 @@ struct WsLayout {
   size_t scores;       // fp32 [max_rows, score_stride]
   size_t blockmax;     // fp32 [max_rows, bm_stride]
   size_t cand;         // fp32 [max_rows, kPoolPositions] Reindex candidate scores
-  size_t part_o;       // fp32 [kslots, heads_pad, D] split-K partial outputs
-  size_t part_ml;      // fp32 [kslots, heads_pad, 2] split-K (max, sum)
   size_t total;
   int64_t score_stride, bm_stride;
-  int64_t slots;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-inline WsLayout ws_layout(int64_t max_len, int64_t max_rows, int64_t heads, int64_t dim) {
+inline WsLayout ws_layout(int64_t max_len, int64_t max_rows) {
   WsLayout L{};
   L.score_stride = (max_len + 127) / 128 * 128;
   L.bm_stride = (L.score_stride / kBlock + 31) / 32 * 32;
-  L.slots = max_rows > kSplitSlots ? max_rows : kSplitSlots;
-  const int64_t hp = 64;
-  (void)heads;
   size_t off = 0;
   L.status = off; off = align256(off + 256);
   L.row_len = off; off = align256(off + 4 * max_rows);
@@ -53,8 +46,6 @@ inline WsLayout ws_layout(int64_t max_len, int64_t max_rows, int64_t heads, int6
   L.scores = off; off = align256(off + 4 * (size_t)max_rows * L.score_stride);
   L.blockmax = off; off = align256(off + 4 * (size_t)max_rows * L.bm_stride);
   L.cand = off; off = align256(off + 4 * (size_t)max_rows * kPoolPositions);
-  L.part_o = off; off = align256(off + 4 * (size_t)L.slots * hp * dim);
-  L.part_ml = off; off = align256(off + 4 * (size_t)L.slots * hp * 2);
   L.total = off;
   return L;
 }
@@ -72,6 +63,55 @@ __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// ------------------------------------------------------------ clusters
+__device__ __forceinline__ int cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return (int)r;
+}
+__device__ __forceinline__ int cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return (int)r;
+}
+// Barrier over every thread of the cluster; orders shared-memory writes
+// before it with reads after it across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Load from the same shared-memory variable of CTA `rank` of the cluster.
+// Ordering with the peer's writes comes from the cluster barrier between
+// them, so independent loads may be in flight together.
+__device__ __forceinline__ uint32_t peer_u32(const void* p, int rank) {
+  uint32_t a = smem_u32(p), r, v;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(r));
+  return v;
+}
+
+__device__ __forceinline__ uint4 peer_u32x4(const void* p, int rank) {
+  uint32_t a = smem_u32(p), r;
+  uint4 v;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(r));
+  return v;
+}
+
+__device__ __forceinline__ float4 peer_f32x4(const void* p, int rank) {
+  uint32_t a = smem_u32(p), r;
+  float4 v;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(r));
+  return v;
+}
+__device__ __forceinline__ float peer_f32(const void* p, int rank) {
+  return __uint_as_float(peer_u32(p, rank));
 }
 
 // Physical cache row of (sequence b, position t); -1 when the page id is bad.

@@ -95,43 +95,6 @@ struct SelSmem {
   int digit, above, nbd, nloc, nb_local, n_above;
 };
 
-// ---------------------------------------------------------------- cluster
-__device__ __forceinline__ int cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return (int)r;
-}
-__device__ __forceinline__ int cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return (int)r;
-}
-// Barrier over every thread of the cluster; orders shared-memory writes
-// before it with reads after it across the cluster.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Load from the same shared-memory variable of CTA `rank` of the cluster.
-// Ordering with the peer's writes comes from the cluster barrier between
-// them, so independent loads may be in flight together.
-__device__ __forceinline__ uint32_t peer_u32(const void* p, int rank) {
-  uint32_t a = smem_u32(p), r, v;
-  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(r));
-  return v;
-}
-
-__device__ __forceinline__ uint4 peer_u32x4(const void* p, int rank) {
-  uint32_t a = smem_u32(p), r;
-  uint4 v;
-  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(r));
-  return v;
-}
-
 // Publishes m, synchronises the cluster and gathers every CTA's Mail into
 // sm.pm.  Each exchange flips `par`, so a buffer is rewritten only after the
 // cluster has passed another barrier (every peer has read it).

@@ -231,9 +231,13 @@ csa2_status csa2_index_reindex(const csa2_cache *cache, const uint8_t *q_idx, co
  * q:    device bf16 bits [B, H, D], already rotated; H <= 64.
  * idx:  device int32 [B, kcap]; cnt: device int32 [B] (clamped to kcap).
  * swa:  device E4M3 [B, W, D]; swa_cnt: device int32 [B] or NULL (= W).
- * softmax_scale <= 0 selects 1/sqrt(D).  out: device fp32 [B, H, D].
+ * softmax_scale <= 0 selects 1/sqrt(D).  out: device fp32 [B, H, D],
+ * 16-byte aligned.
  * A row with no keys gives zeros.  An index outside [0, seq_len[b]) sets
  * CSA2_DEV_BAD_INDEX and is left out of the softmax.
+ * When the SMs outnumber the query rows, the keys of a row are split over a
+ * thread-block cluster of up to 8 CTAs whose partial results are merged in
+ * distributed shared memory; the workspace holds no partial outputs.
  */
 csa2_status csa2_attn_decode(const csa2_cache *cache, const uint16_t *q, int32_t H,
                              const int32_t *idx, const int32_t *cnt, int32_t kcap,
@@ -247,7 +251,7 @@ csa2_status csa2_attn_decode(const csa2_cache *cache, const uint16_t *q, int32_t
  * swa: E4M3 band [B, Tq + W - 1, D]; band row r holds position
  * q_pos[b][0] - (W - 1) + r, and query tq attends to band rows tq .. tq+W-1
  * whose positions are >= 0 (the W most recent positions up to itself).
- * out: fp32 [B, Tq, H, D].
+ * out: fp32 [B, Tq, H, D], 16-byte aligned.
  */
 csa2_status csa2_attn_prefill(const csa2_cache *cache, const uint16_t *q, int32_t H, int32_t Tq,
                               const int32_t *q_pos, const int32_t *idx, const int32_t *cnt,
