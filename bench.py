@@ -33,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HBM_FALLBACK_GBS = 6800.0
+EVENT_EVERY = 25  # timed steps per sampled pair of kernel events
 # DRAM bytes (read + write) per visible position of indexer_kernel<64,128>,
 # from one ncu capture of that kernel on 8 of the 32 sequences of the 128K
 # decode workload (134.51 MB read + 4.80 MB written for 1,048,584 positions;
@@ -161,7 +162,7 @@ def step(st, ev=None, ev_attn=None):
     K, wl, dw, ins = st["K"], st["wl"], st["dw"], st["inputs"]
     B, k, ws, c = wl.batch, wl.topk, dw.ws, dw.cache
     K.quant_append(c, st["new_kv"], st["new_idx"], 1, ws)
-    launches = 2
+    launches = 1  # quant_append (one cluster launch that also advances seq_len)
     if ev is not None:
         K.set_launch_events(K.KERNEL_INDEXER, ev[0], ev[1])
     if wl.modes is None:
@@ -170,7 +171,7 @@ def step(st, ev=None, ev_attn=None):
                      st["idx"][0], st["cnt"][0], st["pool"], st["pool_cnt"], ws)
         if ev is not None:
             K.set_launch_events(K.KERNEL_INDEXER)
-        launches += 3
+        launches += 2
         if ev_attn is not None:
             K.set_launch_events(K.KERNEL_ATTENTION, ev_attn[0], ev_attn[1])
         K.attn_decode(c, ins[0]["q"].view(st["q_dtype"]), wl.heads, st["idx"][0].view(B, k),
@@ -181,7 +182,7 @@ def step(st, ev=None, ev_attn=None):
         if len(wl.layers) > 1:
             K.index_reindex(c, ins[1]["q_idx"], ins[1]["w"], wl.idx_heads, 1, None, st["pool"],
                             st["pool_cnt"], None, B, k, st["idx"][1], st["cnt"][1], ws)
-            launches += 3
+            launches += 2
             for L in (1, 2):
                 K.attn_decode(c, ins[L]["q"].view(st["q_dtype"]), wl.heads, st["idx"][1].view(B, k),
                               st["cnt"][1].view(B), k, ins[L]["swa"], None, wl.window, 0.0,
@@ -192,13 +193,13 @@ def step(st, ev=None, ev_attn=None):
         if nf:
             K.index_full(c, ins[0]["q_idx"], ins[0]["w"], wl.idx_heads, 1, None, st["full_ids"],
                          nf, k, st["idx"][0], st["cnt"][0], None, None, ws)
-            launches += 3
+            launches += 2
         if ev is not None:
             K.set_launch_events(K.KERNEL_INDEXER)
         if nr:
             K.index_reindex(c, ins[1]["q_idx"], ins[1]["w"], wl.idx_heads, 1, None, st["pool"],
                             st["pool_cnt"], st["re_ids"], nr, k, st["idx"][0], st["cnt"][0], ws)
-            launches += 3
+            launches += 2
         K.attn_decode(c, ins[2]["q"].view(st["q_dtype"]), wl.heads, st["idx"][0].view(B, k),
                       st["cnt"][0].view(B), k, ins[2]["swa"], None, wl.window, 0.0, st["out"][0], ws)
         launches += st["attn_launches"]
@@ -349,27 +350,38 @@ def main():
         torch.cuda.synchronize()
 
     # ---- device-resident timed loop
+    # The indexer and attention launches of every EVENT_EVERY-th timed step
+    # are bracketed by CUDA events (each event record costs a few us of GPU
+    # time, so they are sampled rather than put on every step).
+    every = max(1, min(EVENT_EVERY, args.steps))
+
+    def sampled(i):
+        return i % every == every // 2
+
     def run_steps(n, evs=None, evas=None, state=None):
         count = 0
         for i in range(n):
-            count += step(state or st, evs[i] if evs else None, evas[i] if evas else None)
+            j = i // every
+            take = evs is not None and sampled(i)
+            count += step(state or st, evs[j] if take else None, evas[j] if take else None)
         return count
 
     reset()
     run_steps(args.warmup)            # eager warm-up: loads every kernel before any capture
     reset()
     n_start = list(wl.lengths)
+    n_ev = sum(1 for i in range(args.steps) if sampled(i))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+          for _ in range(max(n_ev, 1))]
     eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+           for _ in range(max(n_ev, 1))]
     for a, b in ev + eva:   # torch creates the CUDA event on the first record
         a.record()
         b.record()
     torch.cuda.synchronize()
     graph = None
     if not args.eager:
-        # The K timed steps, unrolled into one CUDA graph; the per-step kernel
+        # The K timed steps, unrolled into one CUDA graph; the sampled kernel
         # events are external records, i.e. event nodes timed on every replay.
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, capture_error_mode="thread_local"):
@@ -400,10 +412,11 @@ def main():
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
     status = K.get_status(st["dw"].ws)
-    idx_ms = [a.elapsed_time(b) for a, b in ev]
-    attn_ms = [a.elapsed_time(b) for a, b in eva]
-    # bytes of the indexer launches (visible length grows by one per step)
-    idx_bytes = [indexer_bytes_per_launch(wl, [n + i + 1 for n in n_start]) for i in range(args.steps)]
+    idx_ms = [a.elapsed_time(b) for a, b in ev[:n_ev]]
+    attn_ms = [a.elapsed_time(b) for a, b in eva[:n_ev]]
+    # bytes of the sampled indexer launches (visible length grows by one per step)
+    idx_bytes = [indexer_bytes_per_launch(wl, [n + i + 1 for n in n_start])
+                 for i in range(args.steps) if sampled(i)]
     roof_bytes = [roofline_bytes_per_step(wl, [n + i + 1 for n in n_start]) for i in range(args.steps)]
     ach = sum(idx_bytes) / (sum(idx_ms) * 1e-3) / 1e9
     traffic = None
@@ -494,7 +507,9 @@ def main():
                          "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
                          "peak_source": peak_kind,
                          "bytes_per_launch": statistics.mean(idx_bytes),
-                         "launch_us": statistics.mean(idx_ms) * 1e3},
+                         "launch_us": statistics.mean(idx_ms) * 1e3,
+                         "timed_launches": len(idx_ms),
+                         "sampling": f"CUDA events on every {every}th timed step"},
             "path_hbm": {"bytes_per_step": statistics.mean(roof_bytes), "achieved_gbs": path_gbs,
                          "frac": path_gbs / peak},
             "kernels_us": {"indexer": statistics.mean(idx_ms) * 1e3,

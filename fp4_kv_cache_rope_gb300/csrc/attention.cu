@@ -266,8 +266,13 @@ __device__ __noinline__ void merge_splits(const AttnParams& p) {
         const int i = i0 + a * blockDim.x;
         const int hh = i / nq, d = 4 * (q0 + i - hh * nq);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (i < items && u0 + j < C) v[a][j] = peer_f32x4(st + hh * D + d, u0 + j);
+        for (int j = 0; j < 4; ++j) {
+          if (i >= items || u0 + j >= C) continue;
+          if (u0 + j == r)  // this CTA's own stage: a plain shared-memory load
+            v[a][j] = *reinterpret_cast<const float4*>(st + hh * D + d);
+          else
+            v[a][j] = peer_f32x4(st + hh * D + d, u0 + j);
+        }
       }
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
@@ -830,6 +835,7 @@ static cudaError_t run_attention(const AttnParams& p, cudaStream_t s) {
   using C = AttnCfg<NSLAB>;
   auto kern = attention_kernel<NSLAB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e == cudaSuccess) e = prefer_max_shared(kern);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.splits, (unsigned)p.n_rows, 1);

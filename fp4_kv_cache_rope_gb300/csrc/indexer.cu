@@ -55,8 +55,30 @@ __device__ __forceinline__ int row_seq(const IndexerParams& p, int row) {
   return p.batch_ids ? p.batch_ids[bi] : bi;
 }
 
-// Visible length and 128-wide tile count of every query row, then the prefix
-// sum of tile counts (one block of 1024 threads).
+// Visible length of query row `row` and its number of 128-wide tiles (Full:
+// 128 positions per tile; Reindex: 16 pool blocks per tile).
+__device__ __forceinline__ int row_tiles(const IndexerParams& p, int row, int& len_out) {
+  const int b = row_seq(p, row);
+  const int tq = row % p.tq;
+  int len = 0;
+  if (b >= 0 && b < p.batch) {
+    len = p.seq_len[b];
+    if (p.q_pos) {
+      const int lim = p.q_pos[(int64_t)b * p.tq + tq] + 1;
+      len = lim < len ? lim : len;
+    }
+    len = len < 0 ? 0 : (len > p.map.max_len ? p.map.max_len : len);
+  }
+  len_out = len;
+  if (p.mode == 0) return (len + 127) / 128;
+  int pc = (b >= 0 && b < p.batch) ? p.pool_cnt[(int64_t)b * p.tq + tq] : 0;
+  pc = pc < 0 ? 0 : (pc > kPoolBlocks ? kPoolBlocks : pc);
+  return (pc + 15) / 16;
+}
+
+// Visible length and tile count of every query row, then the prefix sum of
+// tile counts (one block of 1024 threads).  Used when there are more query
+// rows than the indexer computes in its own prologue.
 __global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerParams p) {
   __shared__ int warp_tot[32];
   __shared__ int carry;
@@ -67,25 +89,9 @@ __global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerParams p) {
     const int row = base + threadIdx.x;
     int tiles = 0;
     if (row < p.n_rows) {
-      const int b = row_seq(p, row);
-      const int tq = row % p.tq;
-      int len = 0;
-      if (b >= 0 && b < p.batch) {
-        len = p.seq_len[b];
-        if (p.q_pos) {
-          const int lim = p.q_pos[(int64_t)b * p.tq + tq] + 1;
-          len = lim < len ? lim : len;
-        }
-        len = len < 0 ? 0 : (len > p.map.max_len ? p.map.max_len : len);
-      }
+      int len;
+      tiles = row_tiles(p, row, len);
       p.row_len[row] = len;
-      if (p.mode == 0) {
-        tiles = (len + 127) / 128;
-      } else {
-        int pc = (b >= 0 && b < p.batch) ? p.pool_cnt[(int64_t)b * p.tq + tq] : 0;
-        pc = pc < 0 ? 0 : (pc > kPoolBlocks ? kPoolBlocks : pc);
-        tiles = (pc + 15) / 16;
-      }
     }
     // block-wide inclusive scan of tiles
     int v = tiles;
@@ -115,6 +121,9 @@ __global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerParams p) {
   if (threadIdx.x == 0) p.tile_prefix[0] = 0;
 }
 
+// Query rows up to which every indexer CTA plans the rows itself.
+constexpr int kInlinePlanRows = 1024;
+
 template <int HP, int DI>
 struct IdxCfg {
   static constexpr int kTile = 128;
@@ -131,7 +140,8 @@ struct IdxCfg {
   // then the abort flag and the TMEM address slot (one word each)
   static constexpr int kNumBars = 2 * kStages + 8 + 1;
   static constexpr int kBarBytes = (kNumBars * 8 + 8 + 127) / 128 * 128;
-  static constexpr int kSmem = kBarOff + kBarBytes;
+  static constexpr int kPlanOff = kBarOff + kBarBytes;  // row lengths, tile prefix
+  static constexpr int kSmem = kPlanOff + 4 * (2 * kInlinePlanRows + 4);
   static_assert(kSmem <= 227 * 1024, "indexer shared memory exceeds the per-CTA limit");
 };
 
@@ -160,22 +170,26 @@ __device__ __forceinline__ int find_row(const int32_t* prefix, int n_rows, int t
 // Walks the query rows of a CTA's tile range; the row's bounds and visible
 // length are reloaded only when the row changes.
 struct RowCursor {
+  const int32_t* prefix;  // tile prefix [n_rows + 1] (shared or global memory)
+  const int32_t* lens;    // visible length per row
   int row, begin, end, len;
-  __device__ __forceinline__ void init(const IndexerParams& p, int t) {
-    row = find_row(p.tile_prefix, p.n_rows, t);
-    begin = p.tile_prefix[row];
-    end = p.tile_prefix[row + 1];
-    len = p.row_len[row];
+  __device__ __forceinline__ void init(const int32_t* pre, const int32_t* ln, int n_rows, int t) {
+    prefix = pre;
+    lens = ln;
+    row = find_row(prefix, n_rows, t);
+    begin = prefix[row];
+    end = prefix[row + 1];
+    len = lens[row];
   }
   // Returns true when tile t starts a new row.
-  __device__ __forceinline__ bool advance(const IndexerParams& p, int t) {
+  __device__ __forceinline__ bool advance(const IndexerParams&, int t) {
     if (t < end) return false;
     do {
       ++row;
       begin = end;
-      end = p.tile_prefix[row + 1];
+      end = prefix[row + 1];
     } while (t >= end);
-    len = p.row_len[row];
+    len = lens[row];
     return true;
   }
 };
@@ -204,7 +218,43 @@ __global__ void __launch_bounds__(192, 1)
     if (threadIdx.x == 0) set_status(p.status, CSA2_DEV_BAD_ALIGN);
     return;
   }
-  const int total = p.tile_prefix[p.n_rows];
+  // ---- rows: visible lengths and the tile prefix (planned here for up to
+  // kInlinePlanRows rows; CTA 0 publishes them for the selection kernel)
+  const int32_t* pre = p.tile_prefix;
+  const int32_t* lens = p.row_len;
+  if (p.n_rows <= kInlinePlanRows) {
+    int32_t* s_len = reinterpret_cast<int32_t*>(smem + C::kPlanOff);
+    int32_t* s_pre = s_len + kInlinePlanRows;
+    for (int row = threadIdx.x; row < p.n_rows; row += blockDim.x) {
+      int len;
+      s_pre[row + 1] = row_tiles(p, row, len);
+      s_len[row] = len;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int carry = 0;
+      for (int base = 0; base < p.n_rows; base += 32) {
+        const int i = base + lane;
+        int v = i < p.n_rows ? s_pre[i + 1] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += u;
+        }
+        if (i < p.n_rows) s_pre[i + 1] = v + carry;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+      if (lane == 0) s_pre[0] = 0;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+      for (int i = threadIdx.x; i < p.n_rows; i += blockDim.x) p.row_len[i] = s_len[i];
+      for (int i = threadIdx.x; i <= p.n_rows; i += blockDim.x) p.tile_prefix[i] = s_pre[i];
+    }
+    pre = s_pre;
+    lens = s_len;
+  }
+  const int total = pre[p.n_rows];
   const int t_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
   const int t_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
 
@@ -238,7 +288,7 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------ TMA producer
       RowCursor rc;
-      rc.init(p, t_begin);
+      rc.init(pre, lens, p.n_rows, t_begin);
       int qn = 0, stage = 0;
       uint32_t phase = 0;
       int b = row_seq(p, rc.row), tq = rc.row % p.tq;
@@ -316,7 +366,7 @@ __global__ void __launch_bounds__(192, 1)
       // --------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = instr_desc(0, 0, false, false, 128, HP);
       RowCursor rc;
-      rc.init(p, t_begin);
+      rc.init(pre, lens, p.n_rows, t_begin);
       int qn = 0, stage = 0, acc = 0;
       uint32_t phase = 0, aphase = 0;
       const uint32_t st_base = smem_u32(stages), q_base = smem_u32(qbuf);
@@ -348,7 +398,7 @@ __global__ void __launch_bounds__(192, 1)
       // ----------------------------------------------------------- epilogue
       const int quad = warp & 3;  // TMEM lane quadrant this warp may access
       RowCursor rc;
-      rc.init(p, t_begin);
+      rc.init(pre, lens, p.n_rows, t_begin);
       int acc = 0;
       uint32_t aphase = 0;
       float wv[HP];
@@ -466,6 +516,7 @@ static cudaError_t run_indexer(const CUtensorMap& tk, const CUtensorMap& tq, con
   using C = IdxCfg<HP, DI>;
   auto kern = indexer_kernel<HP, DI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e == cudaSuccess) e = prefer_max_shared(kern);
   if (e != cudaSuccess) return e;
   record_launch_begin(CSA2_KERNEL_INDEXER, s);
   kern<<<num_sms, 192, C::kSmem, s>>>(tk, tq, p);
@@ -517,9 +568,12 @@ cudaError_t launch_indexer(const csa2_cache& c, const RowSet& rows, int mode, co
   const int64_t q_rows = (int64_t)c.batch * rows.tq * hi;
   if (!make_map(&tq, q_idx, q_rows, di, di, hi)) return cudaErrorInvalidValue;
 
-  indexer_plan_kernel<<<1, 1024, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (rows.n_rows > kInlinePlanRows) {
+    prefer_max_shared(indexer_plan_kernel);
+    indexer_plan_kernel<<<1, 1024, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
 
   const int hp = hi <= 16 ? 16 : (hi <= 32 ? 32 : 64);
 #define CSA2_IDX_CASE(HPV, DIV) \

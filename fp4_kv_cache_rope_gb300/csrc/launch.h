@@ -11,6 +11,15 @@
 
 namespace csa2 {
 
+// Every kernel of the path asks for the largest shared-memory carveout, so
+// that consecutive kernels of a step never make an SM change its L1/shared
+// split between launches.
+template <typename Kernel>
+inline cudaError_t prefer_max_shared(Kernel kern) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
+}
+
 // Benchmark instrumentation (api.cu): records the family's begin/end events
 // on stream s when they are set.
 void record_launch_begin(int family, cudaStream_t s);

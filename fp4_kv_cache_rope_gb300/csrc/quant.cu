@@ -20,6 +20,10 @@
 
 namespace csa2 {
 
+// Appends of at most this many 16-channel groups run as one cluster of up to
+// 8 CTAs that also advances seq_len (decode steps: B x (D + di) / 16 groups).
+constexpr int64_t kSmallAppendGroups = 8 * 512;
+
 struct QuantParams {
   const float* kv;
   const float* idx_in;
@@ -27,7 +31,7 @@ struct QuantParams {
   uint8_t* scales;
   uint8_t* idx_k;
   int64_t code_stride, scale_stride, idxk_stride;
-  const int32_t* seq_len;
+  int32_t* seq_len;
   const float* rope_cos;
   const float* rope_sin;
   RowMap map;
@@ -36,14 +40,28 @@ struct QuantParams {
   uint32_t* status;
 };
 
-__global__ void __launch_bounds__(256) quant_append_kernel(QuantParams p) {
-  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t rows = (int64_t)p.B * p.T;
-  if (gid >= rows * p.groups_total) return;
+// Quantises group gid (row gid / groups_total, group gid % groups_total).
+__device__ __forceinline__ void quant_group(const QuantParams& p, int64_t gid) {
   const int64_t row = gid / p.groups_total;
   const int g = (int)(gid - row * p.groups_total);
   const int b = (int)(row / p.T);
   const int i = (int)(row - (int64_t)b * p.T);
+  const bool is_idx = g >= p.groups_main;
+  // the input rows do not depend on the position: request them first
+  float y[16];
+  {
+    const float4* src =
+        is_idx ? reinterpret_cast<const float4*>(p.idx_in + row * p.di + 16 * (g - p.groups_main))
+               : reinterpret_cast<const float4*>(p.kv + row * p.D + 16 * g);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const float4 f = __ldg(src + v);
+      y[4 * v + 0] = f.x;
+      y[4 * v + 1] = f.y;
+      y[4 * v + 2] = f.z;
+      y[4 * v + 3] = f.w;
+    }
+  }
   const int64_t pos = (int64_t)p.seq_len[b] + i;
   if (pos >= p.map.max_len || pos < 0) {
     set_status(p.status, CSA2_DEV_OVERFLOW);
@@ -55,31 +73,18 @@ __global__ void __launch_bounds__(256) quant_append_kernel(QuantParams p) {
     return;
   }
 
-  if (g >= p.groups_main) {  // indexer key: plain E4M3 per element
+  if (is_idx) {  // indexer key: plain E4M3 per element
     const int gi = g - p.groups_main;
-    const float4* src = reinterpret_cast<const float4*>(p.idx_in + row * p.di + 16 * gi);
     uint32_t w[4];
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const float4 f = __ldg(src + v);
-      w[v] = e4m3_encode(f.x) | (e4m3_encode(f.y) << 8) | (e4m3_encode(f.z) << 16) |
-             (e4m3_encode(f.w) << 24);
-    }
+    for (int v = 0; v < 4; ++v)
+      w[v] = e4m3_encode(y[4 * v]) | (e4m3_encode(y[4 * v + 1]) << 8) |
+             (e4m3_encode(y[4 * v + 2]) << 16) | (e4m3_encode(y[4 * v + 3]) << 24);
     *reinterpret_cast<uint4*>(p.idx_k + r * p.idxk_stride + 16 * gi) =
         make_uint4(w[0], w[1], w[2], w[3]);
     return;
   }
 
-  float y[16];
-  const float4* src = reinterpret_cast<const float4*>(p.kv + row * p.D + 16 * g);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const float4 f = __ldg(src + v);
-    y[4 * v + 0] = f.x;
-    y[4 * v + 1] = f.y;
-    y[4 * v + 2] = f.z;
-    y[4 * v + 3] = f.w;
-  }
   // RoPE on interleaved pairs of the last R channels: two fp32 products and one
   // add/sub per output, each rounded once (no contraction into an FMA).
   const int c0 = 16 * g;
@@ -113,6 +118,27 @@ __global__ void __launch_bounds__(256) quant_append_kernel(QuantParams p) {
   }
   *reinterpret_cast<uint2*>(p.codes + r * p.code_stride + 8 * g) = make_uint2(lo, hi);
   p.scales[r * p.scale_stride + g] = (uint8_t)sc;
+}
+
+__global__ void __launch_bounds__(256) quant_append_kernel(QuantParams p) {
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid < (int64_t)p.B * p.T * p.groups_total) quant_group(p, gid);
+}
+
+// Small appends (decode): one thread-block cluster of up to 8 CTAs does every
+// group; after a cluster barrier (every read of seq_len precedes it) CTA 0
+// advances seq_len, so no second launch is needed.
+__global__ void __launch_bounds__(512) quant_append_cluster_kernel(QuantParams p) {
+  const int64_t total = (int64_t)p.B * p.T * p.groups_total;
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid < total) quant_group(p, gid);
+  cluster_sync();
+  if (blockIdx.x == 0) {
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+      const int64_t n = (int64_t)p.seq_len[b] + p.T;
+      p.seq_len[b] = (int32_t)(n > p.map.max_len ? p.map.max_len : n);
+    }
+  }
 }
 
 __global__ void advance_len_kernel(int32_t* seq_len, int32_t B, int32_t T, int32_t max_len) {
@@ -169,14 +195,35 @@ cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const floa
   p.groups_total = p.groups_main + (idx_in ? c.idx_dim / 16 : 0);
   p.status = status;
   const int64_t total = (int64_t)c.batch * T * p.groups_total;
-  if (total > 0) {
-    const int64_t blocks = (total + 255) / 256;
-    record_launch_begin(CSA2_KERNEL_QUANT, s);
-    quant_append_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
-    record_launch_end(CSA2_KERNEL_QUANT, s);
-    cudaError_t e = cudaGetLastError();
+  if (total <= kSmallAppendGroups) {
+    const int ctas = (int)((total + 511) / 512);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+    cfg.blockDim = dim3(512, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ctas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = prefer_max_shared(quant_append_cluster_kernel);
     if (e != cudaSuccess) return e;
+    record_launch_begin(CSA2_KERNEL_QUANT, s);
+    e = cudaLaunchKernelEx(&cfg, quant_append_cluster_kernel, p);
+    record_launch_end(CSA2_KERNEL_QUANT, s);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
   }
+  const int64_t blocks = (total + 255) / 256;
+  prefer_max_shared(quant_append_kernel);
+  prefer_max_shared(advance_len_kernel);
+  record_launch_begin(CSA2_KERNEL_QUANT, s);
+  quant_append_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+  record_launch_end(CSA2_KERNEL_QUANT, s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   advance_len_kernel<<<(c.batch + 127) / 128, 128, 0, s>>>(c.seq_len, c.batch, T, c.max_len);
   return cudaGetLastError();
 }

@@ -607,6 +607,7 @@ static cudaError_t launch_select_e(const SelectParams& p, int C, cudaStream_t s)
   const int smem = (int)sizeof(SelSmem);
   cudaError_t e =
       cudaFuncSetAttribute(select_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) e = prefer_max_shared(select_kernel<E>);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.n_rows * C), 1, 1);
