@@ -12,8 +12,9 @@ selected FP4 rows plus the FP8 window.  The default workload is the
 calls are captured once into a CUDA graph, which is replayed between CUDA
 events (`--eager` issues every call from the host instead).  `e2e` repeats
 the steps through the same calls with each step's inputs copied from pinned
-host memory and the attention output read back, also as a graph (the eager
-figure is reported beside it).  `roofline` is for the indexer kernel (the dominant one),
+host memory and the attention output read back (on copy streams that
+overlap the compute, double buffered), also as a graph (the eager figure is
+reported beside it).  `roofline` is for the indexer kernel (the dominant one),
 timed live with CUDA events around each of its launches.  Under torchrun
 every rank runs an independent replica (the path does not shard: one GPU per
 problem); the JSON line reports the whole job.
@@ -428,32 +429,69 @@ def main():
     path_gbs = sum(roof_bytes) / (ms * 1e-3) / 1e9
     del graph
 
-    # ---- end-to-end through the C ABI with host buffers
+    # ---- end-to-end through the C ABI with host buffers.  Every step copies
+    # its inputs from pinned host memory and reads its attention output back.
+    # The copies run on their own streams with double-buffered device tensors,
+    # so step i+1's inputs and step i's outputs move while step i computes.
     reset()
     ins = st["inputs"]
-    host = {}
     keys = [("new_kv", st["new_kv"]), ("new_idx", st["new_idx"])]
     for L, d in enumerate(ins):
         for name in ("q_idx", "w", "q", "swa"):
             keys.append((f"{name}{L}", d[name]))
-    for name, t in keys:
-        host[name] = t.cpu().pin_memory()
-    dev = {name: torch.empty_like(t) for name, t in keys}
+    host = {name: t.cpu().pin_memory() for name, t in keys}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    outs = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in st["out"][: layers_per_step(wl)]]
-    d2h = sum(o.numel() * o.element_size() for o in outs)
-    st_e2e = dict(st)
-    st_e2e["new_kv"], st_e2e["new_idx"] = dev["new_kv"], dev["new_idx"]
-    st_e2e["inputs"] = [{n: dev[f"{n}{L}"] for n in ("q_idx", "w", "q", "swa")} for L in range(len(ins))]
+    nl = layers_per_step(wl)
+    bufs = []
+    for _ in range(2):
+        dev = {name: torch.empty_like(t) for name, t in keys}
+        sb = dict(st)
+        sb["new_kv"], sb["new_idx"] = dev["new_kv"], dev["new_idx"]
+        sb["inputs"] = [{n: dev[f"{n}{L}"] for n in ("q_idx", "w", "q", "swa")}
+                        for L in range(len(ins))]
+        sb["out"] = [torch.empty_like(o) for o in st["out"]]
+        pinned = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in st["out"][:nl]]
+        bufs.append((dev, sb, pinned))
+    d2h = sum(o.numel() * o.element_size() for o in bufs[0][2])
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     e_steps = max(args.steps // 4, 20)
+    pool = [torch.cuda.Event() for _ in range(3 * e_steps + 6)]
+    for e in pool:  # create the CUDA events before any capture
+        e.record()
+    torch.cuda.synchronize()
 
     def e2e_steps(n):
-        for _ in range(n):
-            for name in host:
-                dev[name].copy_(host[name], non_blocking=True)
-            step(st_e2e)
-            for o, src in zip(outs, st["out"]):
-                o.copy_(src, non_blocking=True)
+        comp = torch.cuda.current_stream()
+        s_in.wait_stream(comp)
+        s_out.wait_stream(comp)
+        in_ready, comp_done, out_done = pool[0:n], pool[n:2 * n], pool[2 * n:3 * n]
+
+        def issue_h2d(i):
+            dev = bufs[i % 2][0]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(comp_done[i - 2])  # buffer i % 2 was read by step i-2
+                for name in host:
+                    dev[name].copy_(host[name], non_blocking=True)
+                in_ready[i].record(s_in)
+
+        issue_h2d(0)
+        for i in range(n):
+            if i + 1 < n:
+                issue_h2d(i + 1)
+            sb, pinned = bufs[i % 2][1], bufs[i % 2][2]
+            comp.wait_event(in_ready[i])
+            if i >= 2:
+                comp.wait_event(out_done[i - 2])  # outputs of step i-2 were read back
+            step(sb)
+            comp_done[i].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[i])
+                for o, src in zip(pinned, sb["out"]):
+                    o.copy_(src, non_blocking=True)
+                out_done[i].record(s_out)
+        comp.wait_stream(s_in)
+        comp.wait_stream(s_out)
 
     def timed(fn):
         reset()
@@ -517,6 +555,8 @@ def main():
             "e2e": {"value": e2e_value, "unit": "layer-steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e_steps,
                     "cuda_graph": e2e_graph is not None, "eager_value": e2e_eager,
+                    "copies": "per step, on two copy streams overlapping the compute "
+                              "(double-buffered device inputs and outputs)",
                     **({"note": e2e_note} if e2e_note else {})},
             "gpu_launches": launches,
             "clocks": clk,
