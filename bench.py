@@ -37,10 +37,10 @@ HBM_FALLBACK_GBS = 6800.0
 EVENT_EVERY = 25  # timed steps per sampled pair of kernel events
 # DRAM bytes (read + write) per visible position of indexer_kernel<64,128>,
 # from one ncu capture of that kernel on 8 of the 32 sequences of the 128K
-# decode workload (134.51 MB read + 4.80 MB written for 1,048,584 positions;
+# decode workload (134.53 MB read + 4.71 MB written for 1,048,592 positions;
 # the indexer summary under profiles/).  Scaled to a launch by its visible
 # positions; must be re-measured whenever the kernel changes.
-INDEXER_TRAFFIC_B_PER_POS = 139.305472e6 / 1048584
+INDEXER_TRAFFIC_B_PER_POS = 139.241216e6 / 1048592
 
 
 def peaks():
