@@ -57,6 +57,22 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def max_over_ranks(ms, world, device="cuda"):
+    """The slowest rank's time: every rank runs an independent replica, and
+    the job's throughput is the units of all ranks over this time."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms):
+    """Whole-job units per second for `world` replicas that took `ms` (max over ranks)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -408,10 +424,7 @@ def main():
     time.sleep(0.1)
     clk = clocks.stop()
     ms = t_begin.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
     status = K.get_status(st["dw"].ws)
     idx_ms = [a.elapsed_time(b) for a, b in ev[:n_ev]]
     attn_ms = [a.elapsed_time(b) for a, b in eva[:n_ev]]
@@ -425,7 +438,7 @@ def main():
         traffic = INDEXER_TRAFFIC_B_PER_POS * statistics.mean(idx_bytes) / wl.idx_dim
     peak, peak_kind = peaks()
     ms_step = ms / args.steps
-    value = world * layers_per_step(wl) * args.steps / (ms * 1e-3)
+    value = job_throughput(layers_per_step(wl) * args.steps, world, ms)
     path_gbs = sum(roof_bytes) / (ms * 1e-3) / 1e9
     del graph
 
@@ -501,11 +514,8 @@ def main():
         e1.record()
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        return world * layers_per_step(wl) * e_steps / (e_ms * 1e-3)
+        e_ms = max_over_ranks(e_ms, world)
+        return job_throughput(layers_per_step(wl) * e_steps, world, e_ms)
 
     reset()
     e2e_steps(3)

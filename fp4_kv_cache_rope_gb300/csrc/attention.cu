@@ -792,26 +792,27 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
         }
         mma_commit(pv_done + (c & 1));
       };
-      // Per chunk it: PV(it) once its softmax weights are written and QK(it+1)
-      // once its X tile is dequantised, whichever is ready first.
-      for (int it = 0; it < nloc && ok; ++it) {
-        const int buf = it & 1;
-        bool qk_done = it + 1 >= nloc, pv_done_issued = false;
-        const uint64_t t0 = globaltimer();
-        for (uint32_t spin = 0; !(qk_done && pv_done_issued); ++spin) {
-          if (!pv_done_issued && mbar_try_wait(p_full, it & 1)) {
-            tc_fence_after();
-            issue_pv(it);
-            pv_done_issued = true;
-          } else if (!qk_done && mbar_try_wait(x_full + (buf ^ 1), ((it + 1) >> 1) & 1)) {
-            tc_fence_after();
-            issue_qk(it + 1);
-            qk_done = true;
-          } else if ((spin & 63) == 63 && (*abort_flag || globaltimer() - t0 > kWaitNs)) {
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
+      // Whatever is ready, PV first: PV(c) once chunk c's softmax weights
+      // are written, else the next QK once its X tile is dequantised.  QK can
+      // run two chunks ahead of PV, which keeps the tensor pipe busy during
+      // a chunk's softmax.  This is safe because X(q) is dequantised only
+      // after PV(q-2) has completed, hence after the softmax has read S(q-2),
+      // whose tensor-memory buffer QK(q) reuses.
+      int next_qk = 1, next_pv = 0;
+      const uint64_t t0 = globaltimer();
+      for (uint32_t spin = 0; ok && next_pv < nloc; ++spin) {
+        if (mbar_try_wait(p_full, next_pv & 1)) {
+          tc_fence_after();
+          issue_pv(next_pv);
+          ++next_pv;
+        } else if (next_qk < nloc &&
+                   mbar_try_wait(x_full + (next_qk & 1), (next_qk >> 1) & 1)) {
+          tc_fence_after();
+          issue_qk(next_qk);
+          ++next_qk;
+        } else if ((spin & 63) == 63 && (*abort_flag || globaltimer() - t0 > kWaitNs)) {
+          *abort_flag = 1;
+          ok = false;
         }
       }
       // let every issued MMA land before the tensor memory is freed
