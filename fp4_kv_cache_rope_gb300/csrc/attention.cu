@@ -832,12 +832,25 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
 }
 
 template <int NSLAB>
-static cudaError_t run_attention(const AttnParams& p, cudaStream_t s) {
+static cudaError_t run_attention(AttnParams p, cudaStream_t s) {
   using C = AttnCfg<NSLAB>;
   auto kern = attention_kernel<NSLAB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e == cudaSuccess) e = prefer_max_shared(kern);
   if (e != cudaSuccess) return e;
+  // A CTA takes a whole SM and a cluster must fit inside one GPC, so not every
+  // cluster count runs at once: take the largest split count whose clusters
+  // all run in one wave (the splits of a row must also be co-resident).
+  {
+    static int fits[kMaxSplits + 1] = {};  // clusters of each size that run at once
+    int splits = p.splits;
+    while (splits > 1) {
+      if (!fits[splits]) fits[splits] = max_active_clusters(kern, splits, 288, C::kSmem) + 1;
+      if (fits[splits] - 1 >= p.n_rows) break;
+      --splits;
+    }
+    p.splits = splits;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.splits, (unsigned)p.n_rows, 1);
   cfg.blockDim = dim3(288, 1, 1);

@@ -20,6 +20,29 @@ inline cudaError_t prefer_max_shared(Kernel kern) {
                               (int)cudaSharedmemCarveoutMaxShared);
 }
 
+// How many clusters of `cluster` CTAs (each `threads` threads and `smem`
+// dynamic shared-memory bytes) the GPU runs at once; 0 when unknown.
+template <typename Kernel>
+inline int max_active_clusters(Kernel kern, int cluster, int threads, int smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cluster, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();  // clear the error; the caller falls back
+    return 0;
+  }
+  return n;
+}
+
 // Benchmark instrumentation (api.cu): records the family's begin/end events
 // on stream s when they are set.
 void record_launch_begin(int family, cudaStream_t s);

@@ -649,9 +649,30 @@ cudaError_t launch_select(const csa2_cache& c, const RowSet& rows, int mode, int
   p.pool_out = pool_out;
   p.pool_cnt_out = pool_cnt_out;
   p.status = reinterpret_cast<uint32_t*>(ws + L.status);
-  // as many CTAs per row (one per SM) as the SMs hold, up to 8
+  // as many CTAs per row (one per SM) as the SMs hold, up to 8, with every
+  // cluster running in one wave (a cluster must fit inside one GPC)
   int C = 1;
   while (C < kMaxCluster && (int64_t)rows.n_rows * C * 2 <= num_sms) C *= 2;
+  {
+    static int fits[kMaxCluster + 1] = {};  // clusters of each size that run at once
+    const int smem = (int)sizeof(SelSmem);
+    while (C > 1) {
+      if (!fits[C]) {
+        int n = 0;
+        switch (C) {
+          case 8: cudaFuncSetAttribute(select_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                  n = max_active_clusters(select_kernel<6>, 8, kSelThreads, smem); break;
+          case 4: cudaFuncSetAttribute(select_kernel<10>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                  n = max_active_clusters(select_kernel<10>, 4, kSelThreads, smem); break;
+          default: cudaFuncSetAttribute(select_kernel<18>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                  n = max_active_clusters(select_kernel<18>, 2, kSelThreads, smem); break;
+        }
+        fits[C] = n + 1;
+      }
+      if (fits[C] - 1 >= rows.n_rows) break;
+      C /= 2;
+    }
+  }
   record_launch_begin(CSA2_KERNEL_SELECT, s);
   cudaError_t e;
   switch (C) {
