@@ -52,6 +52,17 @@ def peaks():
         return HBM_FALLBACK_GBS, "fallback"
 
 
+def fp8_peak():
+    """Dense FP8 tensor peak: the measured bf16 burst figure times the nominal
+    fp8/bf16 ratio (4.5 / 2.25 PFLOP/s)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return 2.0 * float(p["bf16_tflops"]), "measured bf16 x nominal fp8/bf16 ratio"
+    except Exception:
+        return 2.0 * 1900.0, "fallback bf16 x nominal fp8/bf16 ratio"
+
+
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
             int(os.environ.get("LOCAL_RANK", 0)))
@@ -124,28 +135,43 @@ def build_run(wid, extra_capacity, batch=None):
     from synth.workloads import FULL, REINDEX, REUSE, get_workload
 
     wl = get_workload(wid)
-    wl.extra_capacity = extra_capacity   # room for the tokens appended by the steps
     if batch:                            # smaller batch of the same shapes (profiling)
         wl.batch = batch
         wl.lengths = list(wl.lengths)[:batch]
         if wl.modes is not None:
             wl.modes = list(wl.modes)[:batch]
         wl.name = wl.name + "-first" + str(batch)
+    T = max(1, wl.prefill_tokens)         # tokens appended and queried per sequence per step
+    wl.extra_capacity = extra_capacity * T
     dw = DeviceWorkload(wl)
     B, k = wl.batch, wl.topk
     layers = wl.layers if wl.modes is None else [FULL]
-    inputs = [dw.layer_inputs(L) for L in range(len(layers) if wl.modes is None else 3)]
+    n_in = len(layers) if wl.modes is None else 3
+    inputs = [dw.layer_inputs(L, tq=T) for L in range(n_in)]
     n0 = torch.tensor(wl.lengths, dtype=torch.int32, device="cuda")
-    new_kv, new_idx = dw.new_token_inputs(wl.lengths)
-    new_kv = new_kv.view(B, 1, wl.dim).contiguous()
-    new_idx = new_idx.view(B, 1, wl.idx_dim).contiguous()
-    st = dict(wl=wl, dw=dw, K=K, inputs=inputs, n0=n0, new_kv=new_kv, new_idx=new_idx)
-    st["idx"] = [torch.zeros((B, 1, k), dtype=torch.int32, device="cuda") for _ in range(3)]
-    st["cnt"] = [torch.zeros((B, 1), dtype=torch.int32, device="cuda") for _ in range(3)]
-    st["pool"] = torch.zeros((B, 1, K.POOL_BLOCKS), dtype=torch.int32, device="cuda")
-    st["pool_cnt"] = torch.zeros((B, 1), dtype=torch.int32, device="cuda")
-    st["out"] = [torch.empty((B, wl.heads, wl.dim), dtype=torch.float32, device="cuda")
-                 for _ in range(3)]
+    if wl.prefill_tokens:
+        from synth import T_IDXK, T_KV
+        from synth.device import gen_rows_normal
+        new_kv = torch.stack([gen_rows_normal(wl.seed, T_KV, b, wl.lengths[b], T, wl.dim, dw.mult)
+                              for b in range(B)]).contiguous()
+        new_idx = torch.stack([gen_rows_normal(wl.seed, T_IDXK, b, wl.lengths[b], T, wl.idx_dim)
+                               for b in range(B)]).contiguous()
+    else:
+        new_kv, new_idx = dw.new_token_inputs(wl.lengths)
+        new_kv = new_kv.view(B, 1, wl.dim).contiguous()
+        new_idx = new_idx.view(B, 1, wl.idx_dim).contiguous()
+    st = dict(wl=wl, dw=dw, K=K, inputs=inputs, n0=n0, new_kv=new_kv, new_idx=new_idx, T=T)
+    if wl.prefill_tokens:
+        # query positions of step i (counted from the last reset): n_b + i*T + t
+        base = torch.tensor(wl.lengths, dtype=torch.int32).view(1, B, 1)
+        steps_i = torch.arange(extra_capacity, dtype=torch.int32).view(-1, 1, 1) * T
+        st["q_pos_all"] = (base + steps_i + torch.arange(T, dtype=torch.int32).view(1, 1, T)).to("cuda")
+    st["idx"] = [torch.zeros((B, T, k), dtype=torch.int32, device="cuda") for _ in range(3)]
+    st["cnt"] = [torch.zeros((B, T), dtype=torch.int32, device="cuda") for _ in range(3)]
+    st["pool"] = torch.zeros((B, T, K.POOL_BLOCKS), dtype=torch.int32, device="cuda")
+    st["pool_cnt"] = torch.zeros((B, T), dtype=torch.int32, device="cuda")
+    out_shape = (B, T, wl.heads, wl.dim) if wl.prefill_tokens else (B, wl.heads, wl.dim)
+    st["out"] = [torch.empty(out_shape, dtype=torch.float32, device="cuda") for _ in range(3)]
     if wl.modes is not None:
         modes = wl.modes
         full_ids = [b for b in range(B) if modes[b] == FULL]
@@ -174,9 +200,56 @@ def build_run(wid, extra_capacity, batch=None):
     return st
 
 
-def step(st, ev=None, ev_attn=None):
+def append_launches(wl, T):
+    """Kernel launches of one quant_append of T tokens per sequence."""
+    groups = wl.batch * T * (wl.dim + wl.idx_dim) // 16
+    return 1 if groups <= 8 * 512 else 2
+
+
+def index_launches(rows):
+    """Kernel launches of one index call over `rows` query rows."""
+    return 2 if rows <= 1024 else 3
+
+
+def step_multi_query(st, i, ev=None, ev_attn=None):
+    """One step of a multi-query workload: T new tokens per sequence appended,
+    then every layer of the chunk (Full, optionally Reindex over the Full
+    layer's per-query pools) indexed and attended for all T queries."""
+    K, wl, dw, ins, T = st["K"], st["wl"], st["dw"], st["inputs"], st["T"]
+    B, k, ws, c = wl.batch, wl.topk, dw.ws, dw.cache
+    q_pos = st["q_pos_buf"] if "q_pos_buf" in st else st["q_pos_all"][i]
+    K.quant_append(c, st["new_kv"], st["new_idx"], T, ws)
+    launches = append_launches(wl, T)
+    reindex = len(wl.layers) > 1
+    if ev is not None:
+        K.set_launch_events(K.KERNEL_INDEXER, ev[0], ev[1])
+    K.index_full(c, ins[0]["q_idx"], ins[0]["w"], wl.idx_heads, T, q_pos, None, B, k,
+                 st["idx"][0], st["cnt"][0], st["pool"] if reindex else None,
+                 st["pool_cnt"] if reindex else None, ws)
+    if ev is not None:
+        K.set_launch_events(K.KERNEL_INDEXER)
+    launches += index_launches(B * T)
+    if reindex:
+        K.index_reindex(c, ins[1]["q_idx"], ins[1]["w"], wl.idx_heads, T, q_pos, st["pool"],
+                        st["pool_cnt"], None, B, k, st["idx"][1], st["cnt"][1], ws)
+        launches += index_launches(B * T)
+    for L in range(len(wl.layers)):
+        sel = 0 if L == 0 else 1
+        if ev_attn is not None and L == 0:
+            K.set_launch_events(K.KERNEL_ATTENTION, ev_attn[0], ev_attn[1])
+        K.attn_prefill(c, ins[L]["q"].view(st["q_dtype"]), wl.heads, T, q_pos, st["idx"][sel],
+                       st["cnt"][sel], k, ins[L]["swa"], wl.window, 0.0, st["out"][L], ws)
+        if ev_attn is not None and L == 0:
+            K.set_launch_events(K.KERNEL_ATTENTION)
+        launches += 1
+    return launches
+
+
+def step(st, ev=None, ev_attn=None, i=0):
     """One layer-step (or one CSA2 group step for the group workload)."""
     K, wl, dw, ins = st["K"], st["wl"], st["dw"], st["inputs"]
+    if wl.prefill_tokens:
+        return step_multi_query(st, i, ev, ev_attn)
     B, k, ws, c = wl.batch, wl.topk, dw.ws, dw.cache
     K.quant_append(c, st["new_kv"], st["new_idx"], 1, ws)
     launches = 1  # quant_append (one cluster launch that also advances seq_len)
@@ -227,9 +300,20 @@ def layers_per_step(wl):
     return len(wl.layers) if wl.modes is None else 1
 
 
+def indexer_flops_per_launch(wl, n_at):
+    """FP8 tensor flops of the Full indexer launch of a multi-query step:
+    2 * Hi * di per (query, visible position); query t of sequence b sees
+    n_b + t + 1 positions once its chunk is appended (n_at = lengths before)."""
+    T = wl.prefill_tokens
+    vis = sum(n * T + T * (T + 1) // 2 for n in n_at)
+    return 2 * wl.idx_heads * wl.idx_dim * vis
+
+
 def indexer_bytes_per_launch(wl, n_at):
     """Algorithmic bytes of the (first) indexer launch of a step: every scored
     position's E4M3 indexer key (di bytes)."""
+    if wl.prefill_tokens:
+        return sum(n + wl.prefill_tokens for n in n_at) * wl.idx_dim
     if wl.modes is None:
         return sum(n_at) * wl.idx_dim
     return sum(n for n, m in zip(n_at, wl.modes) if m == 0) * wl.idx_dim
@@ -240,6 +324,16 @@ def roofline_bytes_per_step(wl, n_at):
     (D/2 + D/16 B) + FP8 window rows, per layer of the step."""
     e = wl.dim // 2 + wl.dim // 16
     total = 0
+    if wl.prefill_tokens:  # keys read once per layer, gathers per query
+        T = wl.prefill_tokens
+        for L, mode in enumerate(wl.layers):
+            for n in n_at:
+                if mode == 0:
+                    total += (n + T) * wl.idx_dim
+                else:
+                    total += T * min(2048, -(-(n + T) // 8)) * 8 * wl.idx_dim
+                total += T * (min(wl.topk, n + T) * e) + (T + wl.window - 1) * wl.dim
+        return total
     for L, mode in enumerate(wl.layers if wl.modes is None else [None]):
         for b, n in enumerate(n_at):
             m = mode if mode is not None else wl.modes[b]
@@ -355,6 +449,10 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
+    from synth.workloads import get_workload
+    T_chunk = max(1, get_workload(args.workload).prefill_tokens)
+    if T_chunk >= 64:  # long chunks: a bounded number of steps keeps the cache in range
+        args.steps = min(args.steps, 64)
     st = build_run(args.workload, args.steps + args.warmup + 16, args.batch or None)
     wl, K = st["wl"], st["K"]
     st["q_dtype"] = torch.int16
@@ -380,7 +478,7 @@ def main():
         for i in range(n):
             j = i // every
             take = evs is not None and sampled(i)
-            count += step(state or st, evs[j] if take else None, evas[j] if take else None)
+            count += step(state or st, evs[j] if take else None, evas[j] if take else None, i)
         return count
 
     reset()
@@ -428,15 +526,38 @@ def main():
     status = K.get_status(st["dw"].ws)
     idx_ms = [a.elapsed_time(b) for a, b in ev[:n_ev]]
     attn_ms = [a.elapsed_time(b) for a, b in eva[:n_ev]]
-    # bytes of the sampled indexer launches (visible length grows by one per step)
-    idx_bytes = [indexer_bytes_per_launch(wl, [n + i + 1 for n in n_start])
-                 for i in range(args.steps) if sampled(i)]
-    roof_bytes = [roofline_bytes_per_step(wl, [n + i + 1 for n in n_start]) for i in range(args.steps)]
+    # bytes of the sampled indexer launches (visible length grows by T per step)
+    T = st["T"]
+    if wl.prefill_tokens:
+        before = lambda i: [n + i * T for n in n_start]  # lengths before step i's append
+        idx_bytes = [indexer_bytes_per_launch(wl, before(i)) for i in range(args.steps) if sampled(i)]
+        roof_bytes = [roofline_bytes_per_step(wl, before(i)) for i in range(args.steps)]
+    else:
+        idx_bytes = [indexer_bytes_per_launch(wl, [n + i + 1 for n in n_start])
+                     for i in range(args.steps) if sampled(i)]
+        roof_bytes = [roofline_bytes_per_step(wl, [n + i + 1 for n in n_start])
+                      for i in range(args.steps)]
     ach = sum(idx_bytes) / (sum(idx_ms) * 1e-3) / 1e9
     traffic = None
-    if wl.idx_heads == 64 and wl.idx_dim == 128:
+    if wl.idx_heads == 64 and wl.idx_dim == 128 and not wl.prefill_tokens:
         traffic = INDEXER_TRAFFIC_B_PER_POS * statistics.mean(idx_bytes) / wl.idx_dim
     peak, peak_kind = peaks()
+    if wl.prefill_tokens:
+        # T query rows per sequence against the same keys: the indexer is a
+        # dense FP8 contraction, reported against the tensor peak
+        flops = [indexer_flops_per_launch(wl, before(i)) for i in range(args.steps) if sampled(i)]
+        tf_ach = sum(flops) / (sum(idx_ms) * 1e-3) / 1e12
+        tf_peak, tf_kind = fp8_peak()
+        roofline = {"bound": "tensor", "kernel": "indexer_kernel", "achieved": tf_ach,
+                    "peak": tf_peak, "unit": "TFLOP/s", "frac": tf_ach / tf_peak,
+                    "traffic": None, "peak_source": tf_kind,
+                    "flops_per_launch": statistics.mean(flops)}
+    else:
+        roofline = {"bound": "hbm", "kernel": "indexer_kernel", "achieved": ach, "peak": peak,
+                    "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
+                    "peak_source": peak_kind, "bytes_per_launch": statistics.mean(idx_bytes)}
+    roofline.update({"launch_us": statistics.mean(idx_ms) * 1e3, "timed_launches": len(idx_ms),
+                     "sampling": f"CUDA events on every {every}th timed step"})
     ms_step = ms / args.steps
     value = job_throughput(layers_per_step(wl) * args.steps, world, ms)
     path_gbs = sum(roof_bytes) / (ms * 1e-3) / 1e9
@@ -449,6 +570,9 @@ def main():
     reset()
     ins = st["inputs"]
     keys = [("new_kv", st["new_kv"]), ("new_idx", st["new_idx"])]
+    if wl.prefill_tokens:  # the step's query positions are an input too
+        keys.append(("q_pos", st["q_pos_all"][0]))
+        host_qpos = st["q_pos_all"].cpu().pin_memory()
     for L, d in enumerate(ins):
         for name in ("q_idx", "w", "q", "swa"):
             keys.append((f"{name}{L}", d[name]))
@@ -460,6 +584,8 @@ def main():
         dev = {name: torch.empty_like(t) for name, t in keys}
         sb = dict(st)
         sb["new_kv"], sb["new_idx"] = dev["new_kv"], dev["new_idx"]
+        if wl.prefill_tokens:
+            sb["q_pos_buf"] = dev["q_pos"]
         sb["inputs"] = [{n: dev[f"{n}{L}"] for n in ("q_idx", "w", "q", "swa")}
                         for L in range(len(ins))]
         sb["out"] = [torch.empty_like(o) for o in st["out"]]
@@ -485,7 +611,8 @@ def main():
                 if i >= 2:
                     s_in.wait_event(comp_done[i - 2])  # buffer i % 2 was read by step i-2
                 for name in host:
-                    dev[name].copy_(host[name], non_blocking=True)
+                    src = host_qpos[i] if name == "q_pos" else host[name]
+                    dev[name].copy_(src, non_blocking=True)
                 in_ready[i].record(s_in)
 
         issue_h2d(0)
@@ -496,7 +623,7 @@ def main():
             comp.wait_event(in_ready[i])
             if i >= 2:
                 comp.wait_event(out_done[i - 2])  # outputs of step i-2 were read back
-            step(sb)
+            step(sb, i=i)
             comp_done[i].record(comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(comp_done[i])
@@ -540,7 +667,9 @@ def main():
         cpu = cpu_baseline(wl)
     if rank == 0:
         line = {
-            "metric": "CSA2 decode layer-steps/s (achieved HBM GB/s vs GB300 peak in roofline)",
+            "metric": ("CSA2 decode layer-steps/s (achieved HBM GB/s vs GB300 peak in roofline)"
+                       if not wl.prefill_tokens else
+                       f"CSA2 multi-query layer-steps/s ({T} tokens per sequence per step)"),
             "value": value, "unit": "layer-steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
@@ -550,14 +679,9 @@ def main():
                        "window": wl.window, "dim": wl.dim, "idx_heads": wl.idx_heads,
                        "heads": wl.heads, "parallelism": "replicas" if world > 1 else "single",
                        "launch": "eager" if args.eager else "cuda_graph",
+                       "tokens_per_step": B * T,
                        "l2": f"inputs exceed L2 ({roof_bytes[0] / 1e6:.0f} MB read per step)"},
-            "roofline": {"bound": "hbm", "kernel": "indexer_kernel", "achieved": ach, "peak": peak,
-                         "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
-                         "peak_source": peak_kind,
-                         "bytes_per_launch": statistics.mean(idx_bytes),
-                         "launch_us": statistics.mean(idx_ms) * 1e3,
-                         "timed_launches": len(idx_ms),
-                         "sampling": f"CUDA events on every {every}th timed step"},
+            "roofline": roofline,
             "path_hbm": {"bytes_per_step": statistics.mean(roof_bytes), "achieved_gbs": path_gbs,
                          "frac": path_gbs / peak},
             "kernels_us": {"indexer": statistics.mean(idx_ms) * 1e3,

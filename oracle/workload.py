@@ -67,15 +67,17 @@ class SeqRef:
         idx, pool = O.full_select(s, k)
         return s, idx, pool
 
-    def reindex(self, layer, pool, k, n=None):
-        inp = self.inputs(layer)
+    def reindex(self, layer, pool, k, n=None, tq=0, tq_total=1):
+        """Reindex query tq of layer `layer` over the positions of `pool`
+        visible below n."""
+        inp = self.inputs(layer, tq_total)
         n = self.n if n is None else n
         pos = O.pool_positions(pool, n)
         if self._idxk is not None and len(self._idxk) >= n:
             kp = self._idxk[pos]
         else:
             kp = self.idxk_rows(pos)
-        s = O.indexer_scores(inp["q_idx"][0], inp["w"][0], kp)
+        s = O.indexer_scores(inp["q_idx"][tq], inp["w"][tq], kp)
         return s, pos, O.topk(s, k, ids=pos)
 
     def attention(self, layer, idx, swa_count=None, tq=0, tq_total=1, scale=None):

@@ -58,7 +58,7 @@ def _modes(seed: int, batch: int) -> list:
 
 
 def get_workload(i: int) -> Workload:
-    """Workload number i (1..5)."""
+    """Workload number i (1..7)."""
     if i == 1:
         return Workload("tiny-full-decode-b1-n2048-d128", 1, [2048], 128, 32, 4, 32,
                         16, 64, 128, seed=0)
@@ -77,7 +77,18 @@ def get_workload(i: int) -> Workload:
         return Workload("ragged-mixed-decode-b64-paged64-d576", 64, lens, 576, 64, 64, 128,
                         64, 2048, 128, seed=4, outlier_frac=0.01, page_size=64,
                         modes=_modes(4, 64))
+    if i == 6:
+        # multi-query decode: a 5-token speculative verify per sequence (each
+        # draft token appended, queried causally up to itself)
+        return Workload("verify5-decode-b32-n131072-d576", 32, [131072] * 32, 576, 64, 64, 128,
+                        64, 2048, 128, seed=5, outlier_frac=0.01, prefill_tokens=5)
+    if i == 7:
+        # pool-aware prefill: a chunk whose Full layer gives every query its own
+        # pool of blocks, followed by a Reindex layer over those pools
+        return Workload("pool-prefill-t256-after-n65536-d576", 2, [65536] * 2, 576, 64, 64, 128,
+                        64, 2048, 128, seed=6, outlier_frac=0.01, prefill_tokens=256,
+                        layers=[FULL, REINDEX])
     raise ValueError(f"no workload {i}")
 
 
-WORKLOADS = {i: get_workload for i in range(1, 6)}
+WORKLOADS = {i: get_workload for i in range(1, 8)}
