@@ -29,6 +29,11 @@ Readings of points the pages leave open (each is also listed in the design doc):
   in the low nibble of byte j.
 * Indexer score s_t = sum_h w_h * max(0, q_h . k_t) over E4M3 operands, no
   extra constant factor.
+* MXFP4 indexer key (the alternative key format): per block of 32 channels
+  the E8M0 scale is 2^(floor(log2 amax) - 2), the OCP Microscaling rule
+  (E2M1's largest binade has exponent 2), clamped below at 2^-127 (code 0,
+  also used for an all-zero block); codes = E2M1(RNE(x / scale)), saturating
+  at 6, sign copied, packed like the main-KV codes.  The query stays E4M3.
 * Ranking order for top-k and for the pool: larger score first, lower index
   on equal scores.  The pool keeps min(2048, ceil(N/8)) blocks of 8
   positions ranked by block maximum.  Outputs are sorted ascending.
@@ -42,9 +47,12 @@ import math
 
 import numpy as np
 
-from .formats import (e2m1_decode, e2m1_encode, e4m3_decode, e4m3_encode)
+from .formats import (E8M0_BIAS, e2m1_decode, e2m1_encode, e4m3_decode, e4m3_encode,
+                      e8m0_decode)
 
 GROUP = 16          # channels per E4M3 scale of the main-KV format
+MX_BLOCK = 32       # channels per E8M0 scale of the MXFP4 indexer key
+E2M1_EMAX = 2       # exponent of E2M1's largest binade (4 <= |v| <= 6)
 BLOCK = 8           # positions per pool block
 POOL_BLOCKS = 2048  # pool capacity in blocks
 
@@ -126,6 +134,44 @@ def fp8_cast(x):
     return e4m3_encode(x)
 
 
+def quantize_mxfp4(x):
+    """fp32 indexer-key rows [n, d] -> (codes uint8 [n, d/2], E8M0 scales uint8 [n, d/32]).
+
+    [ID] "Reconstructing the 890-byte cache budget": the indexer key keeps
+    32-channel groups with E8M0 scales, 128 x 4/8 + 128/32 = 68 bytes;
+    "How the derived numbers were built": MXFP4, one scale per 32.
+    Per block: amax = max|x|; e = floor(log2 amax) - 2 (the OCP Microscaling
+    shared-exponent rule for E2M1), at least -127; scale = 2^e (code e + 127);
+    codes = E2M1(x / scale) (RNE, saturating, sign copied).  An all-zero block
+    takes code 0.  x / scale is exact (a power-of-two division of an fp32
+    value, computed in fp64).
+    Pinned: the exponent against the fp32 bit pattern, saturation between 6
+    and 8 times the scale, grid values reproduced exactly, the per-element
+    error bound, zero and tiny blocks, the pages' byte count.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    n, d = x.shape
+    g = x.reshape(n, d // MX_BLOCK, MX_BLOCK).astype(np.float64)
+    amax = np.max(np.abs(g), axis=-1)
+    _, ex = np.frexp(amax)                  # amax = m * 2^ex, 0.5 <= m < 1
+    e = np.where(amax > 0, ex - 1 - E2M1_EMAX, -E8M0_BIAS)
+    e = np.maximum(e, -E8M0_BIAS)
+    scale = np.ldexp(1.0, e)
+    codes = e2m1_encode(g / scale[..., None]).reshape(n, d)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, (e + E8M0_BIAS).astype(np.uint8)
+
+
+def dequantize_mxfp4(codes, scales, dim):
+    """(codes [n, d/2], E8M0 scales [n, d/32]) -> float64 rows [n, d]."""
+    codes = np.asarray(codes, dtype=np.uint8)[:, : dim // 2]
+    v = np.empty((codes.shape[0], dim), dtype=np.float64)
+    v[:, 0::2] = e2m1_decode(codes & 0xF)
+    v[:, 1::2] = e2m1_decode(codes >> 4)
+    s = e8m0_decode(np.asarray(scales, dtype=np.uint8)[:, : dim // MX_BLOCK])
+    return v * np.repeat(s, MX_BLOCK, axis=1)
+
+
 # -------------------------------------------------------- step 2: indexer score
 def indexer_scores(q_codes, w, k_codes):
     """Lightning-indexer scores of one query against key rows (fp64).
@@ -140,6 +186,19 @@ def indexer_scores(q_codes, w, k_codes):
     """
     q = e4m3_decode(q_codes).reshape(len(w), -1)
     k = e4m3_decode(k_codes).reshape(-1, q.shape[1])
+    return indexer_scores_values(q, w, k)
+
+
+def indexer_scores_values(q, w, k):
+    """s_t = sum_h w_h * max(0, q_h . k_t) for decoded q [Hi, di] and keys k [n, di] (fp64).
+
+    Shared by both key formats: the E4M3 keys above and the MXFP4 keys
+    (decoded by dequantize_mxfp4).  Every product is exact in fp64 (at most
+    6 significant bits times a power of two); with MXFP4 keys whose blocks sit
+    at very different scales the fp64 sum itself may round.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64).reshape(-1, q.shape[1])
     dots = k @ q.T
     return np.maximum(dots, 0.0) @ np.asarray(w, dtype=np.float64)
 

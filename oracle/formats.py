@@ -8,11 +8,16 @@ Formats named by the pages:
   new GEMM"; "Inside DeepSeek V4.1 Flash: CED, CSA2 and the 890-Byte KV Cache",
   section "Reconstructing the 890-byte cache budget".
 * SWA window and indexer operands: FP8 (E4M3), same sections.
+* indexer key, MXFP4 form: E2M1 values with one E8M0 scale per 32 channels
+  (128 x 4/8 + 128/32 = 68 bytes per entry) -- "Inside DeepSeek V4.1 Flash",
+  sections "Reconstructing the 890-byte cache budget" and "How the derived
+  numbers were built".
 
 The bit layouts are those of the OCP 8-bit floating point specification
 (E4M3 "FN": bias 7, no infinities, S.1111.111 is NaN, largest finite 448) and
 of the OCP Microscaling specification (E2M1: bias 1, magnitudes
-0, 0.5, 1, 1.5, 2, 3, 4, 6).
+0, 0.5, 1, 1.5, 2, 3, 4, 6; E8M0: the power of two 2^(code - 127), code 255
+is NaN).
 
 Encoders are written as the definition of rounding: among all finite values
 of the format pick the nearest one; on an exact tie pick the one whose code
@@ -105,3 +110,18 @@ def bf16_bits_to_f64(bits) -> np.ndarray:
 def fp4_entry_bytes(dim: int, group: int = 16, scale_bytes: int = 1) -> int:
     """Algorithmic bytes of one FP4 cache entry: dim/2 codes + one scale per group."""
     return dim // 2 + (dim // group) * scale_bytes
+
+
+E8M0_BIAS = 127
+
+
+def e8m0_decode(codes) -> np.ndarray:
+    """8-bit E8M0 scale codes -> float64 powers of two 2^(code - 127) (NaN for 255)."""
+    c = np.asarray(codes, dtype=np.int64)
+    v = np.ldexp(1.0, c - E8M0_BIAS)
+    return np.where(c == 255, np.nan, v)
+
+
+def mxfp4_entry_bytes(dim: int, block: int = 32) -> int:
+    """Algorithmic bytes of one MXFP4 row: dim/2 codes + one E8M0 byte per block."""
+    return dim // 2 + dim // block
