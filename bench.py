@@ -6,7 +6,12 @@ main-KV and indexer-key rows (RoPE + FP4 quantisation), score and select
 selected FP4 rows plus the FP8 window.  The default workload is the
 128K-context Full-layer decode (B = 32, N = 131,072, D = 576, k = 2,048).
 
-  python bench.py [--steps K] [--warmup W] [--workload 2|3|5|1] [--impl reference]
+  python bench.py [--steps K] [--warmup W] [--workload 1..8] [--impl reference]
+
+Workloads (synth/workloads.py): 1 tiny, 2 the 128K decode (default), 3 a CSA2
+group (Full + Reindex + Reuse) at 1M, 4 a 4,096-token prefill chunk, 5 ragged
+mixed-mode paged decode, 6 a 5-token verify, 7 pool-aware prefill, 8 the 128K
+decode with MXFP4 indexer keys.
 
 `value` is layer-steps/s with inputs resident in HBM: the K steps' C-ABI
 calls are captured once into a CUDA graph, which is replayed between CUDA
@@ -41,6 +46,8 @@ EVENT_EVERY = 25  # timed steps per sampled pair of kernel events
 # the indexer summary under profiles/).  Scaled to a launch by its visible
 # positions; must be re-measured whenever the kernel changes.
 INDEXER_TRAFFIC_B_PER_POS = 139.241216e6 / 1048592
+# The same figure for the MXFP4-key indexer, once an ncu capture gives it.
+MX_INDEXER_TRAFFIC_B_PER_POS = None
 
 
 def peaks():
@@ -311,36 +318,38 @@ def indexer_flops_per_launch(wl, n_at):
 
 def indexer_bytes_per_launch(wl, n_at):
     """Algorithmic bytes of the (first) indexer launch of a step: every scored
-    position's E4M3 indexer key (di bytes)."""
+    position's indexer key (di bytes in E4M3; di/2 + di/32 in MXFP4)."""
+    kb = wl.idx_entry_bytes()
     if wl.prefill_tokens:
-        return sum(n + wl.prefill_tokens for n in n_at) * wl.idx_dim
+        return sum(n + wl.prefill_tokens for n in n_at) * kb
     if wl.modes is None:
-        return sum(n_at) * wl.idx_dim
-    return sum(n for n, m in zip(n_at, wl.modes) if m == 0) * wl.idx_dim
+        return sum(n_at) * kb
+    return sum(n for n, m in zip(n_at, wl.modes) if m == 0) * kb
 
 
 def roofline_bytes_per_step(wl, n_at):
     """Roofline bytes of one step: indexer keys read + gathered FP4 entries
     (D/2 + D/16 B) + FP8 window rows, per layer of the step."""
     e = wl.dim // 2 + wl.dim // 16
+    kb = wl.idx_entry_bytes()
     total = 0
     if wl.prefill_tokens:  # keys read once per layer, gathers per query
         T = wl.prefill_tokens
         for L, mode in enumerate(wl.layers):
             for n in n_at:
                 if mode == 0:
-                    total += (n + T) * wl.idx_dim
+                    total += (n + T) * kb
                 else:
-                    total += T * min(2048, -(-(n + T) // 8)) * 8 * wl.idx_dim
+                    total += T * min(2048, -(-(n + T) // 8)) * 8 * kb
                 total += T * (min(wl.topk, n + T) * e) + (T + wl.window - 1) * wl.dim
         return total
     for L, mode in enumerate(wl.layers if wl.modes is None else [None]):
         for b, n in enumerate(n_at):
             m = mode if mode is not None else wl.modes[b]
             if m == 0:
-                total += n * wl.idx_dim
+                total += n * kb
             elif m == 1:
-                total += min(2048, -(-n // 8)) * 8 * wl.idx_dim
+                total += min(2048, -(-n // 8)) * 8 * kb
             total += min(wl.topk, n) * e + wl.window * wl.dim
     return total
 
@@ -364,7 +373,12 @@ def oracle_sample(wl, b, n, layer=0):
 
     def run():
         O.quant_append_rows(newrow, np.array([n]), ref.cos, ref.sin, wl.rope_dim)
-        s = O.indexer_scores(inp["q_idx"][0], inp["w"][0], ik)
+        if wl.idx_format == "mxfp4":
+            q = O.e4m3_decode(inp["q_idx"][0]).reshape(wl.idx_heads, -1)
+            s = O.indexer_scores_values(q, inp["w"][0], O.dequantize_mxfp4(ik[0], ik[1],
+                                                                           wl.idx_dim))
+        else:
+            s = O.indexer_scores(inp["q_idx"][0], inp["w"][0], ik)
         idx, pool = O.full_select(s, wl.topk)
         # the selected rows' cache bytes (regenerated and quantised here; the
         # oracle keeps no cache of its own)
@@ -540,7 +554,10 @@ def main():
     ach = sum(idx_bytes) / (sum(idx_ms) * 1e-3) / 1e9
     traffic = None
     if wl.idx_heads == 64 and wl.idx_dim == 128 and not wl.prefill_tokens:
-        traffic = INDEXER_TRAFFIC_B_PER_POS * statistics.mean(idx_bytes) / wl.idx_dim
+        per_pos = (MX_INDEXER_TRAFFIC_B_PER_POS if wl.idx_format == "mxfp4"
+                   else INDEXER_TRAFFIC_B_PER_POS)
+        if per_pos is not None:
+            traffic = per_pos * statistics.mean(idx_bytes) / wl.idx_entry_bytes()
     peak, peak_kind = peaks()
     if wl.prefill_tokens:
         # T query rows per sequence against the same keys: the indexer is a

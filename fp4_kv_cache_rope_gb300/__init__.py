@@ -42,7 +42,11 @@ class Csa2Cache(ctypes.Structure):
         ("idx_k", _p), ("idxk_stride", _i64),
         ("page_table", _p), ("seq_len", _p),
         ("rope_cos", _p), ("rope_sin", _p),
+        ("idx_format", _i32), ("idx_scales", _p), ("idx_scale_stride", _i64),
     ]
+
+
+IDX_E4M3, IDX_MXFP4 = 0, 1
 
 
 def _sig(name, args, res=_i32):
@@ -194,17 +198,26 @@ class Cache:
     """Device storage of one shared global cache plus its C description.
 
     Row strides are the smallest multiples of 16 bytes that hold a row:
-    codes D/2, scales round_up(D/16, 16), indexer key di.
+    codes D/2, scales round_up(D/16, 16), indexer key di (E4M3).  With
+    ``idx_format=IDX_MXFP4`` (di = 128) the indexer key is 64 code bytes per
+    row and a separate array holds its 4 E8M0 scale bytes per row.
     """
 
     def __init__(self, batch, dim, rope_dim, idx_dim, max_len, rope_cos, rope_sin,
-                 page_size=0, page_table=None, num_pages=0, device="cuda"):
+                 page_size=0, page_table=None, num_pages=0, device="cuda",
+                 idx_format=IDX_E4M3):
         import torch
         self.batch, self.dim, self.rope_dim, self.idx_dim = batch, dim, rope_dim, idx_dim
         self.max_len, self.page_size = max_len, page_size
+        self.idx_format = idx_format
         self.code_stride = (dim // 2 + 15) // 16 * 16
         self.scale_stride = (dim // 16 + 15) // 16 * 16
-        self.idxk_stride = (idx_dim + 15) // 16 * 16
+        if idx_format == IDX_MXFP4:
+            self.idxk_stride = (idx_dim // 2 + 31) // 32 * 32
+            self.idx_scale_stride = idx_dim // 32
+        else:
+            self.idxk_stride = (idx_dim + 15) // 16 * 16
+            self.idx_scale_stride = 0
         if page_size:
             self.num_pages = num_pages
             rows = num_pages * page_size
@@ -219,6 +232,8 @@ class Cache:
         self.codes = torch.zeros((rows, self.code_stride), dtype=torch.uint8, device=device)
         self.scales = torch.zeros((rows, self.scale_stride), dtype=torch.uint8, device=device)
         self.idx_k = torch.zeros((rows, self.idxk_stride), dtype=torch.uint8, device=device)
+        self.idx_scales = (torch.zeros((rows, self.idx_scale_stride), dtype=torch.uint8,
+                                       device=device) if idx_format == IDX_MXFP4 else None)
         self.seq_len = torch.zeros(batch, dtype=torch.int32, device=device)
         self.rope_cos = rope_cos.to(device=device, dtype=torch.float32).contiguous()
         self.rope_sin = rope_sin.to(device=device, dtype=torch.float32).contiguous()
@@ -227,7 +242,9 @@ class Cache:
             self.codes.data_ptr(), self.code_stride, self.scales.data_ptr(), self.scale_stride,
             self.idx_k.data_ptr(), self.idxk_stride,
             self.page_table.data_ptr() if self.page_table is not None else None,
-            self.seq_len.data_ptr(), self.rope_cos.data_ptr(), self.rope_sin.data_ptr())
+            self.seq_len.data_ptr(), self.rope_cos.data_ptr(), self.rope_sin.data_ptr(),
+            idx_format, self.idx_scales.data_ptr() if self.idx_scales is not None else None,
+            self.idx_scale_stride)
 
     def physical_row(self, b, t):
         """Host mirror of the row mapping (for reading rows back in tests)."""

@@ -31,7 +31,19 @@ bool cache_ok(const csa2_cache* c) {
   if (c->code_stride < c->dim / 2 || !mult16(c->code_stride)) return false;
   const int64_t scb = ((c->dim / 16) + 15) / 16 * 16;
   if (c->scale_stride < scb || !mult16(c->scale_stride)) return false;
-  if (c->idxk_stride < c->idx_dim || !mult16(c->idxk_stride)) return false;
+  if (c->idx_format == CSA2_IDX_E4M3) {
+    if (c->idxk_stride < c->idx_dim || !mult16(c->idxk_stride)) return false;
+  } else if (c->idx_format == CSA2_IDX_MXFP4) {
+    // the packed-E2M1 tensor map wants 32-byte aligned rows of 128 channels;
+    // a tile's scale rows are copied in 16-byte aligned runs
+    if (c->idx_dim != 128 || c->idxk_stride < 64 || c->idxk_stride % 32 != 0) return false;
+    if ((reinterpret_cast<uintptr_t>(c->idx_k) & 31) != 0) return false;
+    if (!c->idx_scales || c->idx_scale_stride != 4) return false;
+    if ((reinterpret_cast<uintptr_t>(c->idx_scales) & 15) != 0) return false;
+    if (c->page_size == 0 && c->max_len % 4 != 0) return false;
+  } else {
+    return false;
+  }
   if (c->rope_dim > 0 && (!c->rope_cos || !c->rope_sin)) return false;
   return true;
 }

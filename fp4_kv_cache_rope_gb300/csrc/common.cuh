@@ -238,6 +238,20 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
+// D[tmem] (+)= (A * 2^(sa-127)) (B * 2^(sb-127))^T, block-scaled with one E8M0
+// scale per 32 K-elements (kind::mxf8f6f4, scale_vec::1X).  Scale of A row m:
+// tensor-memory lane m, column sfa + m/32, byte "A scale id" of idesc; scale
+// of B column n: lane 32*(m/32) + n%32 (every lane quadrant holds a copy),
+// column sfb + n/32, byte "B scale id".
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %6, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
+}
 // Arrives on `bar` once all previously issued MMAs of this thread completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -266,6 +280,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[15])
       : "memory");
 }
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t v0, uint32_t v1) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(v0),
+               "r"(v1)
+               : "memory");
+}
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -293,6 +315,17 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 
 // Instruction descriptor: fp32 accumulator, operand formats a/b, majorness,
 // M and N.  kind::f16: 0 = f16, 1 = bf16.  kind::f8f6f4: 0 = E4M3.
+// Instruction descriptor of kind::mxf8f6f4 with E8M0 scales (both operands
+// K-major): A/B formats (E4M3 0, E2M1 5), N/8 at bit 17, the E8M0 scale type
+// at bit 23, M/16 at bit 24; the B and A scale ids (bits 4 and 29) are OR-ed
+// in per K step.
+__host__ __device__ constexpr uint32_t instr_desc_mx(uint32_t afmt, uint32_t bfmt, int m, int n) {
+  return (afmt << 7) | (bfmt << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(m >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t mx_scale_ids(uint32_t a_id, uint32_t b_id) {
+  return (a_id << 29) | (b_id << 4);
+}
 __host__ __device__ constexpr uint32_t instr_desc(uint32_t afmt, uint32_t bfmt, bool a_mn,
                                                   bool b_mn, int m, int n) {
   return (1u << 4) | (afmt << 7) | (bfmt << 10) | ((a_mn ? 1u : 0u) << 15) |

@@ -40,6 +40,8 @@ struct IndexerParams {
   const float* w;
   RowMap map;
   int32_t rows_per_load;  // Full mode box height (128 or the page size)
+  const uint8_t* idx_scales;  // MXFP4 keys: E8M0 bytes, 4 per physical row
+  int64_t phys_rows;          // physical key rows (bounds of the scale copies)
   int32_t* row_len;
   int32_t* tile_prefix;
   float* scores;
@@ -130,7 +132,12 @@ constexpr int kInlinePlanRows = 1024;
 // one CTA per SM with an 8-stage ring, the same bytes in flight).
 constexpr int kIdxCtasPerSm = 2;
 
-template <int HP, int DI>
+// MX: MXFP4 keys (E2M1 codes + an E8M0 scale per 32 channels, di = 128).  The
+// packed codes are expanded by the tensor map (CU_TENSOR_MAP_DATA_TYPE_16U4_
+// ALIGN16B: 16 codes in 8 bytes, then an 8-byte gap) into the same 128-byte
+// shared-memory rows the E4M3 keys use, and the MMA is the block-scaled
+// kind::mxf8f6f4 with the query's scales fixed at 1.
+template <int HP, int DI, bool MX = false>
 struct IdxCfg {
   static constexpr int kTile = 128;
   static constexpr int kStageBytes = kTile * DI;
@@ -139,12 +146,20 @@ struct IdxCfg {
   static constexpr int kSwizzle = DI == 128 ? 2 : (DI == 64 ? 4 : 6);
   static constexpr uint32_t kSbo = 8 * DI;
   static constexpr int kKSteps = DI / 32;
+  static constexpr uint32_t kKRowBytes = MX ? DI / 2 : DI;   // global key bytes per row
+  static constexpr int kSfTileBytes = MX ? kTile * 4 : 0;    // E8M0 bytes of one tile
   static constexpr int kAccCols = 2 * HP < 32 ? 32 : 2 * HP;
-  static constexpr int kTmemCols = kAccCols <= 32 ? 32 : (kAccCols <= 64 ? 64 : (kAccCols <= 128 ? 128 : 256));
-  static constexpr int kBarOff = kStages * kStageBytes + 2 * kQBytes;
-  // mbarriers: full/empty per stage, qfull/qempty/tfull/tempty x2, drain;
-  // then the abort flag and the TMEM address slot (one word each)
-  static constexpr int kNumBars = 2 * kStages + 8 + 1;
+  // MX tensor-memory columns: A scales of accumulator a at kSfaCol + 32a (4
+  // columns: row m reads column m/32), B scales at kSfbCol (2 columns, N <= 64)
+  static constexpr int kSfaCol = kAccCols;
+  static constexpr int kSfbCol = kAccCols + 64;
+  static constexpr int kUsedCols = MX ? kSfbCol + 2 : kAccCols;
+  static constexpr int kTmemCols = kUsedCols <= 32 ? 32 : (kUsedCols <= 64 ? 64 : (kUsedCols <= 128 ? 128 : 256));
+  static constexpr int kSfOff = kStages * kStageBytes + 2 * kQBytes;
+  static constexpr int kBarOff = kSfOff + kStages * kSfTileBytes;
+  // mbarriers: full/empty per stage, qfull/qempty/tfull/tempty x2, (MX) sfull
+  // x2, drain; then the abort flag and the TMEM address slot (one word each)
+  static constexpr int kNumBars = 2 * kStages + 8 + (MX ? 2 : 0) + 1;
   static constexpr int kBarBytes = (kNumBars * 8 + 8 + 127) / 128 * 128;
   static constexpr int kPlanOff = kBarOff + kBarBytes;  // row lengths, tile prefix
   static constexpr int kSmem = kPlanOff + 4 * (2 * kInlinePlanRows + 4);
@@ -200,14 +215,15 @@ struct RowCursor {
   }
 };
 
-template <int HP, int DI>
+template <int HP, int DI, bool MX>
 __global__ void __launch_bounds__(192, kIdxCtasPerSm)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                    IndexerParams p) {
-  using C = IdxCfg<HP, DI>;
+  using C = IdxCfg<HP, DI, MX>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   uint8_t* qbuf = smem + C::kStages * C::kStageBytes;
+  uint8_t* sfbuf = smem + C::kSfOff;           // MX: [kStages][128 rows][4 B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* full = bars;                       // [kStages]
   uint64_t* empty = bars + C::kStages;         // [kStages]
@@ -215,7 +231,8 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
   uint64_t* qempty = qfull + 2;                // [2]
   uint64_t* tfull = qempty + 2;                // [2]
   uint64_t* tempty = tfull + 2;                // [2]
-  uint64_t* drain = tempty + 2;                // [1]
+  uint64_t* sfull = tempty + 2;                // [2] (MX) A scales in tensor memory
+  uint64_t* drain = sfull + (MX ? 2 : 0);      // [1]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(drain + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1) + 1;
 
@@ -274,6 +291,7 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
       mbar_init(qempty + s, 1);
       mbar_init(tfull + s, 1);
       mbar_init(tempty + s, 4);
+      if (MX) mbar_init(sfull + s, 4);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -318,9 +336,17 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
         if (p.mode == 0) {
           const int64_t t0 = (int64_t)j * 128;
           if (p.map.page_size == 0) {
-            bytes = 128 * DI;
-            mbar_arrive_expect_tx(full + stage, bytes);
-            tma_load_2d(dst, &tm_k, 0, (int)((int64_t)b * p.map.max_len + t0), full + stage);
+            const int64_t r0 = (int64_t)b * p.map.max_len + t0;
+            bytes = 128 * C::kKRowBytes;
+            uint32_t sf_bytes = 0;
+            if (MX) {  // the tile's scale rows, cut at the end of the sequence
+              const int64_t n = p.map.max_len - t0 < 128 ? p.map.max_len - t0 : 128;
+              sf_bytes = (uint32_t)(4 * n);
+            }
+            mbar_arrive_expect_tx(full + stage, bytes + sf_bytes);
+            tma_load_2d(dst, &tm_k, 0, (int)r0, full + stage);
+            if (MX) bulk_load(sfbuf + stage * C::kSfTileBytes, p.idx_scales + 4 * r0, sf_bytes,
+                              full + stage);
           } else {
             const int rpl = p.rows_per_load;
             int nload = 0;
@@ -334,11 +360,15 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
                 else { src_rows[u] = r; ++nload; }
               }
             }
-            bytes = (uint32_t)(nload * rpl * DI);
+            bytes = (uint32_t)(nload * rpl * (C::kKRowBytes + (MX ? 4 : 0)));
             mbar_arrive_expect_tx(full + stage, bytes);
             for (int u = 0; u < 128 / rpl; ++u)
-              if (src_rows[u] >= 0)
+              if (src_rows[u] >= 0) {
                 tma_load_2d(dst + u * rpl * DI, &tm_k, 0, (int)src_rows[u], full + stage);
+                if (MX)
+                  bulk_load(sfbuf + stage * C::kSfTileBytes + u * rpl * 4,
+                            p.idx_scales + 4 * src_rows[u], (uint32_t)(rpl * 4), full + stage);
+              }
           }
         } else {
           int pc = p.pool_cnt[(int64_t)b * p.tq + tq];
@@ -360,17 +390,35 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
               }
             }
           }
-          bytes = (uint32_t)(nload * kBlock * DI);
+          // scale rows of a block, cut at the last physical row (a block may
+          // run past the end of the sequence's rows; the key box is clipped
+          // by the tensor map, the scale copy here)
+          uint32_t sf_n[16];
+          uint32_t sf_total = 0;
+          for (int e = 0; e < 16; ++e) {
+            sf_n[e] = 0;
+            if (MX && src_rows[e] >= 0) {
+              const int64_t n = p.phys_rows - src_rows[e];
+              sf_n[e] = (uint32_t)(n < kBlock ? n : kBlock);
+              sf_total += 4 * sf_n[e];
+            }
+          }
+          bytes = (uint32_t)(nload * kBlock * C::kKRowBytes) + sf_total;
           mbar_arrive_expect_tx(full + stage, bytes);
           for (int e = 0; e < 16; ++e)
-            if (src_rows[e] >= 0)
+            if (src_rows[e] >= 0) {
               tma_load_2d(dst + e * kBlock * DI, &tm_k, 0, (int)src_rows[e], full + stage);
+              if (MX)
+                bulk_load(sfbuf + stage * C::kSfTileBytes + e * kBlock * 4,
+                          p.idx_scales + 4 * src_rows[e], 4 * sf_n[e], full + stage);
+            }
         }
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
     } else if (warp == 1 && lane == 0) {
       // --------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = instr_desc(0, 0, false, false, 128, HP);
+      constexpr uint32_t idesc = MX ? instr_desc_mx(5, 0, 128, HP)
+                                    : instr_desc(0, 0, false, false, 128, HP);
       RowCursor rc;
       rc.init(pre, lens, p.n_rows, t_begin);
       int qn = 0, stage = 0, acc = 0;
@@ -386,13 +434,19 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
         const int qs = (qn - 1) & 1;
         if (!mbar_wait(full + stage, phase, abort_flag)) break;
         if (!mbar_wait(tempty + acc, aphase ^ 1, abort_flag)) break;
+        if (MX && !mbar_wait(sfull + acc, aphase, abort_flag)) break;
         tc_fence_after();
         const uint32_t a0 = st_base + stage * C::kStageBytes;
         const uint32_t b0 = q_base + qs * C::kQBytes;
 #pragma unroll
         for (int kk = 0; kk < C::kKSteps; ++kk) {
-          mma_f8(tmem + acc * HP, smem_desc(a0 + kk * 32, 16, C::kSbo, C::kSwizzle),
-                 smem_desc(b0 + kk * 32, 16, C::kSbo, C::kSwizzle), idesc, kk > 0 ? 1u : 0u);
+          const uint64_t ad = smem_desc(a0 + kk * 32, 16, C::kSbo, C::kSwizzle);
+          const uint64_t bd = smem_desc(b0 + kk * 32, 16, C::kSbo, C::kSwizzle);
+          if (MX)  // K step kk takes byte kk of each row's scale word
+            mma_mx(tmem + acc * HP, ad, bd, idesc | mx_scale_ids(kk, kk),
+                   tmem + C::kSfaCol + 32 * acc, tmem + C::kSfbCol, kk > 0 ? 1u : 0u);
+          else
+            mma_f8(tmem + acc * HP, ad, bd, idesc, kk > 0 ? 1u : 0u);
         }
         issued_mma = true;
         mma_commit(empty + stage);
@@ -403,6 +457,26 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
     } else if (warp >= 2) {
       // ----------------------------------------------------------- epilogue
       const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+      const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+      // MX: this warp's 32 rows of the A scales of local tile i go to the
+      // scale columns of accumulator i % 2 once the tile's copy has landed
+      auto stage_scales = [&](int i) -> bool {
+        if (!mbar_wait(full + i % C::kStages, (uint32_t)((i / C::kStages) & 1), abort_flag))
+          return false;
+        const uint32_t sf = *reinterpret_cast<const uint32_t*>(
+            sfbuf + (i % C::kStages) * C::kSfTileBytes + 4 * (32 * quad + lane));
+        tmem_st1(tmem + lane_base + C::kSfaCol + 32 * (i & 1) + quad, sf);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfull + (i & 1));
+        return true;
+      };
+      bool ok = true;
+      if (MX) {  // query scales: E8M0 1.0 in every byte; then the first two tiles
+        tmem_st2(tmem + lane_base + C::kSfbCol, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        for (int i = 0; i < 2 && ok && t_begin + i < t_end; ++i) ok = stage_scales(i);
+      }
       RowCursor rc;
       rc.init(pre, lens, p.n_rows, t_begin);
       int acc = 0;
@@ -410,7 +484,7 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
       float wv[HP];
       float* out_row = nullptr;
       float* bm_row = nullptr;
-      for (int t = t_begin; t < t_end; ++t) {
+      for (int t = t_begin; ok && t < t_end; ++t) {
         const bool fresh = rc.advance(p, t) || t == t_begin;
         if (fresh) {
           const int b = row_seq(p, rc.row);
@@ -436,6 +510,8 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty + acc);
+        // MMA(i) has read this accumulator's scale columns: stage tile i + 2's
+        if (MX && t + 2 < t_end && !stage_scales(t + 2 - t_begin)) break;
         // four independent partial sums over the heads (head h into s4[h % 4]),
         // two at a time with the packed fp32 FMA, then their sum.  The
         // epilogue's instruction count is on the kernel's critical path.
@@ -516,11 +592,29 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int width, 
   return r == CUDA_SUCCESS;
 }
 
-template <int HP, int DI>
+// Packed E2M1 rows of 128 channels (64 bytes) [rows, 128] with a row stride,
+// expanded on the way into shared memory to 128-byte rows (16 codes, then 8
+// bytes of gap), box [box_rows, 128 codes], 128-byte swizzle.  The mbarrier
+// transaction count of one box is its global bytes: 64 per row.
+static bool make_map_e2m1(CUtensorMap* m, const void* base, int64_t rows, int64_t stride,
+                          int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)stride};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int HP, int DI, bool MX>
 static cudaError_t run_indexer(const CUtensorMap& tk, const CUtensorMap& tq, const IndexerParams& p,
                                int num_sms, cudaStream_t s) {
-  using C = IdxCfg<HP, DI>;
-  auto kern = indexer_kernel<HP, DI>;
+  using C = IdxCfg<HP, DI, MX>;
+  auto kern = indexer_kernel<HP, DI, MX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e == cudaSuccess) e = prefer_max_shared(kern);
   if (e != cudaSuccess) return e;
@@ -569,8 +663,13 @@ cudaError_t launch_indexer(const csa2_cache& c, const RowSet& rows, int mode, co
   }
   p.rows_per_load = box_rows;
   phys_rows = c.page_size == 0 ? (int64_t)c.batch * c.max_len : (int64_t)c.num_pages * c.page_size;
+  p.phys_rows = phys_rows;
+  const bool mx = c.idx_format == CSA2_IDX_MXFP4;
+  p.idx_scales = mx ? c.idx_scales : nullptr;
   CUtensorMap tk, tq;
-  if (!make_map(&tk, c.idx_k, phys_rows, di, c.idxk_stride, box_rows)) return cudaErrorInvalidValue;
+  if (mx ? !make_map_e2m1(&tk, c.idx_k, phys_rows, c.idxk_stride, box_rows)
+         : !make_map(&tk, c.idx_k, phys_rows, di, c.idxk_stride, box_rows))
+    return cudaErrorInvalidValue;
   const int64_t q_rows = (int64_t)c.batch * rows.tq * hi;
   if (!make_map(&tq, q_idx, q_rows, di, di, hi)) return cudaErrorInvalidValue;
 
@@ -582,8 +681,14 @@ cudaError_t launch_indexer(const csa2_cache& c, const RowSet& rows, int mode, co
   }
 
   const int hp = hi <= 16 ? 16 : (hi <= 32 ? 32 : 64);
+  if (mx) {  // MXFP4 keys: di = 128 (checked with the cache description)
+    if (di != 128) return cudaErrorInvalidValue;
+    if (hp == 16) return run_indexer<16, 128, true>(tk, tq, p, num_sms, s);
+    if (hp == 32) return run_indexer<32, 128, true>(tk, tq, p, num_sms, s);
+    return run_indexer<64, 128, true>(tk, tq, p, num_sms, s);
+  }
 #define CSA2_IDX_CASE(HPV, DIV) \
-  if (hp == HPV && di == DIV) return run_indexer<HPV, DIV>(tk, tq, p, num_sms, s);
+  if (hp == HPV && di == DIV) return run_indexer<HPV, DIV, false>(tk, tq, p, num_sms, s);
   CSA2_IDX_CASE(16, 32) CSA2_IDX_CASE(16, 64) CSA2_IDX_CASE(16, 128)
   CSA2_IDX_CASE(32, 32) CSA2_IDX_CASE(32, 64) CSA2_IDX_CASE(32, 128)
   CSA2_IDX_CASE(64, 32) CSA2_IDX_CASE(64, 64) CSA2_IDX_CASE(64, 128)

@@ -1,5 +1,7 @@
 // Step 1 of the path: RoPE + FP4 (E2M1 x E4M3-per-16) quantisation + append,
-// and the plain FP8 (E4M3) cast used for the SWA window and indexer operands.
+// the indexer key (E4M3 per channel, or MXFP4: E2M1 with an E8M0 scale per 32
+// channels), and the plain FP8 (E4M3) cast used for the SWA window and the
+// indexer queries.
 //
 // "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression" knowledge
 // note, section "FP4 main KV: trade precision for bytes, not for a new GEMM":
@@ -30,6 +32,8 @@ struct QuantParams {
   uint8_t* codes;
   uint8_t* scales;
   uint8_t* idx_k;
+  uint8_t* idx_scales;  // MXFP4 keys: 4 E8M0 bytes per row
+  int32_t idx_mx;       // 1: MXFP4 indexer keys, 0: E4M3
   int64_t code_stride, scale_stride, idxk_stride;
   int32_t* seq_len;
   const float* rope_cos;
@@ -40,6 +44,50 @@ struct QuantParams {
   uint32_t* status;
 };
 
+// MXFP4 indexer key, one 32-channel block per thread: the E8M0 scale code is
+// the OCP Microscaling shared exponent floor(log2 amax) - 2 (E2M1's top
+// binade is 2^2), read off the fp32 exponent field of amax and clamped at
+// code 0; codes = E2M1(x * 2^(127 - code)), an exact power-of-two scaling.
+__device__ __noinline__ void quant_idx_mx(const QuantParams& p, int64_t row, int b, int i,
+                                          int gi) {
+  float y[32];
+  const float4* src = reinterpret_cast<const float4*>(p.idx_in + row * p.di + 32 * gi);
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const float4 f = __ldg(src + v);
+    y[4 * v + 0] = f.x;
+    y[4 * v + 1] = f.y;
+    y[4 * v + 2] = f.z;
+    y[4 * v + 3] = f.w;
+  }
+  const int64_t pos = (int64_t)p.seq_len[b] + i;
+  if (pos >= p.map.max_len || pos < 0) {
+    set_status(p.status, CSA2_DEV_OVERFLOW);
+    return;
+  }
+  const int64_t r = p.map.row(b, pos);
+  if (r < 0) {
+    set_status(p.status, CSA2_DEV_BAD_PAGE);
+    return;
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(y[e]));
+  const int bexp = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+  const uint32_t code = bexp > 2 ? (uint32_t)(bexp - 2) : 0u;
+  const float inv = __uint_as_float((254u - code) << 23);  // 2^(127 - code), a normal float
+  uint32_t w[4];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    uint32_t x = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x |= e2m1_encode(__fmul_rn(y[8 * v + e], inv)) << (4 * e);
+    w[v] = x;
+  }
+  *reinterpret_cast<uint4*>(p.idx_k + r * p.idxk_stride + 16 * gi) = make_uint4(w[0], w[1], w[2], w[3]);
+  p.idx_scales[r * 4 + gi] = (uint8_t)code;
+}
+
 // Quantises group gid (row gid / groups_total, group gid % groups_total).
 __device__ __forceinline__ void quant_group(const QuantParams& p, int64_t gid) {
   const int64_t row = gid / p.groups_total;
@@ -47,6 +95,10 @@ __device__ __forceinline__ void quant_group(const QuantParams& p, int64_t gid) {
   const int b = (int)(row / p.T);
   const int i = (int)(row - (int64_t)b * p.T);
   const bool is_idx = g >= p.groups_main;
+  if (is_idx && p.idx_mx) {
+    quant_idx_mx(p, row, b, i, g - p.groups_main);
+    return;
+  }
   // the input rows do not depend on the position: request them first
   float y[16];
   {
@@ -179,6 +231,8 @@ cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const floa
   p.codes = c.kv_codes;
   p.scales = c.kv_scales;
   p.idx_k = c.idx_k;
+  p.idx_scales = c.idx_scales;
+  p.idx_mx = c.idx_format == CSA2_IDX_MXFP4 ? 1 : 0;
   p.code_stride = c.code_stride;
   p.scale_stride = c.scale_stride;
   p.idxk_stride = c.idxk_stride;
@@ -192,7 +246,7 @@ cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const floa
   p.R = c.rope_dim;
   p.di = c.idx_dim;
   p.groups_main = c.dim / kGroup;
-  p.groups_total = p.groups_main + (idx_in ? c.idx_dim / 16 : 0);
+  p.groups_total = p.groups_main + (idx_in ? c.idx_dim / (p.idx_mx ? 32 : 16) : 0);
   p.status = status;
   const int64_t total = (int64_t)c.batch * T * p.groups_total;
   if (total <= kSmallAppendGroups) {

@@ -83,7 +83,16 @@ typedef enum csa2_status {
  *                                  low nibble of byte j (D/2 bytes used)
  *   kv_scales [rows, scale_stride] one E4M3 scale byte per 16 channels, in
  *                                  channel order (D/16 bytes used)
- *   idx_k     [rows, idxk_stride]  indexer key, one E4M3 byte per channel
+ *   idx_k     [rows, idxk_stride]  indexer key in one of two formats (idx_format):
+ *     CSA2_IDX_E4M3  one E4M3 byte per channel (di bytes used)
+ *     CSA2_IDX_MXFP4 E2M1 codes, two per byte, channel 2j in the low nibble
+ *                    of byte j (di/2 bytes used), with
+ *   idx_scales [rows, idx_scale_stride] one E8M0 byte 2^(code-127) per 32
+ *                    channels, in channel order (MXFP4 only: di/32 bytes).
+ *     The MXFP4 form is the released implementation's indexer key: 128 x 4/8
+ *     + 128/32 = 68 bytes per entry ("Inside DeepSeek V4.1 Flash: CED, CSA2
+ *     and the 890-Byte KV Cache", sections "Reconstructing the 890-byte cache
+ *     budget" and "How the derived numbers were built").
  * The physical row of position t of sequence b is
  *   page_size == 0 : b * max_len + t
  *   page_size  > 0 : page_table[b * max_pages_per_seq + t / page_size]
@@ -109,7 +118,17 @@ typedef struct csa2_cache {
   int32_t *seq_len;           /* [B] visible positions; advanced by csa2_quant_append */
   const float *rope_cos;      /* [max_len, R/2] fp32: cos(p * theta^(-2i/R)) */
   const float *rope_sin;      /* [max_len, R/2] fp32: sin(p * theta^(-2i/R)) */
+  /* Indexer-key format.  Zero-initialised descriptions get CSA2_IDX_E4M3.
+   * CSA2_IDX_MXFP4 requires di = 128, idx_k 32-byte aligned with
+   * idxk_stride >= 64 and a multiple of 32, idx_scales 16-byte aligned with
+   * idx_scale_stride == 4, and max_len a multiple of 4 when page_size == 0. */
+  int32_t idx_format;
+  uint8_t *idx_scales;        /* MXFP4 only; NULL for E4M3 */
+  int64_t idx_scale_stride;   /* MXFP4 only: 4 */
 } csa2_cache;
+
+#define CSA2_IDX_E4M3 0
+#define CSA2_IDX_MXFP4 1
 
 /*
  * Workspace bytes for calls on `cache` that process at most `max_rows` query
@@ -135,8 +154,12 @@ csa2_status csa2_fp8_quant(const float *x, int64_t n, uint8_t *out, void *stream
 /*
  * Step 1: RoPE + FP4 quantisation + append.
  * kv:       device fp32 [B, T, D], rows BEFORE rotation.
- * idx_k_in: device fp32 [B, T, di] or NULL; when given it is cast to E4M3 as
- *           csa2_fp8_quant does and written to the same rows' idx_k.
+ * idx_k_in: device fp32 [B, T, di] or NULL; when given it is written to the
+ *           same rows' indexer key: E4M3 as csa2_fp8_quant casts, or MXFP4:
+ *           per 32 channels the E8M0 scale code is max(E - 2, 0) where E is
+ *           the biased exponent field of the block's fp32 amax (the OCP
+ *           Microscaling rule 2^(floor(log2 amax) - 2)), and each code is
+ *           E2M1(x / scale) (RNE, saturating at 6, sign copied).
  * Row i of sequence b lands at position p = seq_len[b] + i: channels D-R+2j
  * and D-R+2j+1 are rotated by (c, s) = (rope_cos, rope_sin)[p][j] as
  * y0 = x0*c - x1*s, y1 = x0*s + x1*c in fp32 with one rounding per operation;
@@ -159,7 +182,9 @@ csa2_status csa2_quant_append(const csa2_cache *cache, const float *kv, const fl
  * batch_ids, n_batch: device int32 subset of sequences to process, or NULL
  *           with n_batch = B.
  * k:        1..CSA2_MAX_TOPK.
- * Score of position t: s_t = sum_h w_h * max(0, q_h . k_t) (fp32 accumulate).
+ * Score of position t: s_t = sum_h w_h * max(0, q_h . k_t) (fp32 accumulate);
+ * with MXFP4 keys k_t is the E2M1 code times its block's E8M0 scale (the
+ * tensor cores apply the scale per 32 channels).
  * Outputs (only rows of the processed sequences are written):
  *   out_idx     [B, Tq, k]  int32 positions of the top min(k, visible) scores
  *                           ranked by (score desc, position asc), written in

@@ -12,6 +12,7 @@ from synth.device import host_layer_inputs, host_rows_normal
 from synth.workloads import Workload
 
 from . import csa2 as O
+from . import formats as F
 
 
 class SeqRef:
@@ -26,6 +27,7 @@ class SeqRef:
             cos, sin = synth.rope_table(wl.max_len, wl.rope_dim, wl.theta)
         self.cos, self.sin = cos, sin
         self._idxk = None
+        self._idxk_n = 0
         self._inputs = {}
 
     # ---- cache contents ----------------------------------------------------
@@ -34,15 +36,32 @@ class SeqRef:
         x = host_rows_normal(self.wl.seed, synth.T_KV, self.b, positions, self.wl.dim, self.mult)
         return O.quant_append_rows(x, np.asarray(positions), self.cos, self.sin, self.wl.rope_dim)
 
+    @property
+    def mx_keys(self):
+        return getattr(self.wl, "idx_format", "e4m3") == "mxfp4"
+
     def idxk_rows(self, positions):
+        """Stored indexer-key bytes at ``positions``: E4M3 codes, or for MXFP4
+        keys the pair (E2M1 codes, E8M0 scales)."""
         x = host_rows_normal(self.wl.seed, synth.T_IDXK, self.b, positions, self.wl.idx_dim)
-        return O.fp8_cast(x)
+        return O.quantize_mxfp4(x) if self.mx_keys else O.fp8_cast(x)
 
     def idxk_all(self, n=None):
         n = self.n if n is None else n
-        if self._idxk is None or len(self._idxk) < n:
+        if self._idxk is None or self._idxk_n < n:
             self._idxk = self.idxk_rows(np.arange(n))
+            self._idxk_n = n
+        if self.mx_keys:
+            return self._idxk[0][:n], self._idxk[1][:n]
         return self._idxk[:n]
+
+    def _scores_of(self, inp, tq, keys):
+        """Scores of query ``tq`` against stored keys (either format)."""
+        if self.mx_keys:
+            q = F.e4m3_decode(inp["q_idx"][tq]).reshape(self.wl.idx_heads, -1)
+            return O.indexer_scores_values(
+                q, inp["w"][tq], O.dequantize_mxfp4(keys[0], keys[1], self.wl.idx_dim))
+        return O.indexer_scores(inp["q_idx"][tq], inp["w"][tq], keys)
 
     def dequant_rows(self, positions):
         codes, scales = self.cache_rows(positions)
@@ -60,7 +79,7 @@ class SeqRef:
     def scores(self, layer, n=None, tq=0, tq_total=1):
         inp = self.inputs(layer, tq_total)
         n = self.n if n is None else n
-        return O.indexer_scores(inp["q_idx"][tq], inp["w"][tq], self.idxk_all(n)[:n])
+        return self._scores_of(inp, tq, self.idxk_all(n))
 
     def full(self, layer, k, n=None, tq=0, tq_total=1):
         s = self.scores(layer, n, tq, tq_total)
@@ -73,11 +92,12 @@ class SeqRef:
         inp = self.inputs(layer, tq_total)
         n = self.n if n is None else n
         pos = O.pool_positions(pool, n)
-        if self._idxk is not None and len(self._idxk) >= n:
-            kp = self._idxk[pos]
+        if self._idxk is not None and self._idxk_n >= n:
+            kp = ((self._idxk[0][pos], self._idxk[1][pos]) if self.mx_keys
+                  else self._idxk[pos])
         else:
             kp = self.idxk_rows(pos)
-        s = O.indexer_scores(inp["q_idx"][tq], inp["w"][tq], kp)
+        s = self._scores_of(inp, tq, kp)
         return s, pos, O.topk(s, k, ids=pos)
 
     def attention(self, layer, idx, swa_count=None, tq=0, tq_total=1, scale=None):

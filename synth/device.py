@@ -137,17 +137,19 @@ class DeviceWorkload:
         self.mult = outlier_multipliers(wl.seed, wl.dim, wl.outlier_frac) if wl.outlier_frac else None
         cos, sin = rope_table(wl.max_len, wl.rope_dim, wl.theta)
         self.rope_cos, self.rope_sin = cos, sin
+        idx_format = K.IDX_MXFP4 if wl.idx_format == "mxfp4" else K.IDX_E4M3
         if wl.page_size:
             pt, npages = page_table_for(wl)
             self.page_table_np = pt
             self.cache = K.Cache(wl.batch, wl.dim, wl.rope_dim, wl.idx_dim, wl.max_len,
                                  torch.from_numpy(cos), torch.from_numpy(sin),
                                  page_size=wl.page_size, page_table=torch.from_numpy(pt),
-                                 num_pages=npages, device=device)
+                                 num_pages=npages, device=device, idx_format=idx_format)
         else:
             self.page_table_np = None
             self.cache = K.Cache(wl.batch, wl.dim, wl.rope_dim, wl.idx_dim, wl.max_len,
-                                 torch.from_numpy(cos), torch.from_numpy(sin), device=device)
+                                 torch.from_numpy(cos), torch.from_numpy(sin), device=device,
+                                 idx_format=idx_format)
         rows = max(wl.batch * max(1, wl.prefill_tokens), wl.batch)
         self.ws = self.cache.workspace(rows, wl.heads)
         if build_cache:
@@ -166,6 +168,8 @@ class DeviceWorkload:
             s.kv_codes = c.codes.data_ptr() + b * c.max_len * c.code_stride
             s.kv_scales = c.scales.data_ptr() + b * c.max_len * c.scale_stride
             s.idx_k = c.idx_k.data_ptr() + b * c.max_len * c.idxk_stride
+            if c.idx_scales is not None:
+                s.idx_scales = c.idx_scales.data_ptr() + b * c.max_len * c.idx_scale_stride
         s.seq_len = c.seq_len.data_ptr() + 4 * b
         view = type("View", (), {})()
         view.struct = s

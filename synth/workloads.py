@@ -35,13 +35,23 @@ class Workload:
     prefill_tokens: int = 0  # T new tokens appended and queried (prefill chunk)
     pool_blocks: int = 2048  # pool capacity in 8-position blocks
     extra_capacity: int = 0  # positions reserved for tokens appended by decode steps
+    idx_format: str = "e4m3"  # indexer-key storage: "e4m3" (1 B/channel) or "mxfp4"
 
     @property
     def max_len(self) -> int:
-        return int(max(self.lengths)) + max(self.prefill_tokens, 0) + 64 + self.extra_capacity
+        m = int(max(self.lengths)) + max(self.prefill_tokens, 0) + 64 + self.extra_capacity
+        if self.idx_format == "mxfp4":   # whole 16-byte runs of 4-byte scale rows
+            m = (m + 7) // 8 * 8
+        return m
 
     def entry_bytes(self) -> int:
         return self.dim // 2 + self.dim // 16
+
+    def idx_entry_bytes(self) -> int:
+        """Algorithmic indexer-key bytes per position."""
+        if self.idx_format == "mxfp4":
+            return self.idx_dim // 2 + self.idx_dim // 32
+        return self.idx_dim
 
 
 def _ragged_lengths(seed: int, batch: int, lo: int, hi: int) -> list:
@@ -58,7 +68,7 @@ def _modes(seed: int, batch: int) -> list:
 
 
 def get_workload(i: int) -> Workload:
-    """Workload number i (1..7)."""
+    """Workload number i (1..8)."""
     if i == 1:
         return Workload("tiny-full-decode-b1-n2048-d128", 1, [2048], 128, 32, 4, 32,
                         16, 64, 128, seed=0)
@@ -88,6 +98,11 @@ def get_workload(i: int) -> Workload:
         return Workload("pool-prefill-t256-after-n65536-d576", 2, [65536] * 2, 576, 64, 64, 128,
                         64, 2048, 128, seed=6, outlier_frac=0.01, prefill_tokens=256,
                         layers=[FULL, REINDEX])
+    if i == 8:
+        # the 128K decode step with the indexer keys stored as MXFP4 (68 bytes
+        # per position instead of 128)
+        return Workload("full-decode-b32-n131072-d576-mxfp4-keys", 32, [131072] * 32, 576, 64, 64,
+                        128, 64, 2048, 128, seed=1, outlier_frac=0.01, idx_format="mxfp4")
     raise ValueError(f"no workload {i}")
 
 

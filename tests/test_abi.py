@@ -59,3 +59,42 @@ def test_host_validation_without_gpu(lib):
     assert r == K.CSA2_ERR_INVALID
     assert K.entry_bytes(512) == 288 and K.entry_bytes(576) == 324
     assert K.status_string(K.CSA2_ERR_INVALID) == "invalid argument"
+
+
+def test_cache_struct_layout_matches_header(tmp_path):
+    """The ctypes description and the C struct agree field by field (gcc)."""
+    import shutil
+    import subprocess
+    import fp4_kv_cache_rope_gb300 as K
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    names = [f[0] for f in K.Csa2Cache._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "csa2.h"\nint main(void){\n'
+                   + "".join(f'printf("%zu\\n", offsetof(csa2_cache, {n}));\n' for n in names)
+                   + 'printf("%zu\\n", sizeof(csa2_cache));\nreturn 0;}\n')
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    want = [getattr(K.Csa2Cache, n).offset for n in names] + [ctypes.sizeof(K.Csa2Cache)]
+    assert got == want
+
+
+def test_mxfp4_key_description_checks(lib):
+    import fp4_kv_cache_rope_gb300 as K
+    base = K.Csa2Cache(2, 576, 64, 128, 0, 0, 1024, 0, 256, 288, 512, 48, 1024, 64, None, 64,
+                       80, 96, K.IDX_MXFP4, 2048, 4)
+    assert K.workspace_size(base, 2, 64) > 0
+    for field, value in [("idx_dim", 64),            # MXFP4 keys are 128 channels
+                         ("idxk_stride", 48),        # not a multiple of 32
+                         ("idx_k", 1024 + 16),       # not 32-byte aligned
+                         ("idx_scales", None),
+                         ("idx_scales", 2048 + 4),   # not 16-byte aligned
+                         ("idx_scale_stride", 8),
+                         ("max_len", 1022),          # contiguous rows need max_len % 4 == 0
+                         ("idx_format", 2)]:
+        bad = K.Csa2Cache.from_buffer_copy(base)
+        setattr(bad, field, value)
+        assert K.workspace_size(bad, 2, 64) == 0, field
