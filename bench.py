@@ -46,8 +46,9 @@ EVENT_EVERY = 25  # timed steps per sampled pair of kernel events
 # the indexer summary under profiles/).  Scaled to a launch by its visible
 # positions; must be re-measured whenever the kernel changes.
 INDEXER_TRAFFIC_B_PER_POS = 139.241216e6 / 1048592
-# The same figure for the MXFP4-key indexer, once an ncu capture gives it.
-MX_INDEXER_TRAFFIC_B_PER_POS = None
+# The same figure for the MXFP4-key indexer (71.51 MB read + 1.23 MB written for
+# the same 1,048,592 positions; profiles/indexer_kernel_mxfp4-decode-b8-n131072.md).
+MX_INDEXER_TRAFFIC_B_PER_POS = 72.741888e6 / 1048592
 
 
 def peaks():
