@@ -252,6 +252,14 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_
       "[%4], [%5], p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
 }
+// Copies a 32-row x 16-byte shared-memory matrix (descriptor `src`) into
+// tensor-memory columns taddr .. taddr+3 of every lane quadrant: lane 32q + r,
+// column taddr + j receives bytes 4j..4j+3 of row r.  Asynchronous, ordered
+// before later tcgen05.mma of the same thread.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t src) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src)
+               : "memory");
+}
 // Arrives on `bar` once all previously issued MMAs of this thread completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(

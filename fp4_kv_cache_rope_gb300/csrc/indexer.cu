@@ -20,6 +20,8 @@
 //   warp 1   MMA issuer: D[128 positions x Hp heads] = K_tile x Q^T with
 //            tcgen05.mma kind::f8f6f4 (M = 128, N = Hp, K = 32 per
 //            instruction), accumulators double-buffered in tensor memory;
+//            (MXFP4 keys: the warp also lays out each tile's E8M0 scales for
+//            tcgen05.cp into tensor memory, ahead of block-scaled MMAs);
 //   warps 2-5  epilogue: one thread per position reads its Hp accumulators
 //            (tcgen05.ld 32x32b), applies ReLU and the head weights, writes
 //            the fp32 score and, for Full layers, the block maximum.
@@ -150,16 +152,20 @@ struct IdxCfg {
   static constexpr int kSfTileBytes = MX ? kTile * 4 : 0;    // E8M0 bytes of one tile
   static constexpr int kAccCols = 2 * HP < 32 ? 32 : 2 * HP;
   // MX tensor-memory columns: A scales of accumulator a at kSfaCol + 32a (4
-  // columns: row m reads column m/32), B scales at kSfbCol (2 columns, N <= 64)
+  // columns: row m reads column m/32), B scales at kSfbCol (N <= 64 reads 2)
   static constexpr int kSfaCol = kAccCols;
   static constexpr int kSfbCol = kAccCols + 64;
-  static constexpr int kUsedCols = MX ? kSfbCol + 2 : kAccCols;
+  static constexpr int kUsedCols = MX ? kSfbCol + 4 : kAccCols;
   static constexpr int kTmemCols = kUsedCols <= 32 ? 32 : (kUsedCols <= 64 ? 64 : (kUsedCols <= 128 ? 128 : 256));
   static constexpr int kSfOff = kStages * kStageBytes + 2 * kQBytes;
-  static constexpr int kBarOff = kSfOff + kStages * kSfTileBytes;
-  // mbarriers: full/empty per stage, qfull/qempty/tfull/tempty x2, (MX) sfull
-  // x2, drain; then the abort flag and the TMEM address slot (one word each)
-  static constexpr int kNumBars = 2 * kStages + 8 + (MX ? 2 : 0) + 1;
+  // MX: the scale tiles of the two accumulators rearranged for tcgen05.cp
+  // (row r holds the words of rows r, r+32, r+64, r+96), then 512 bytes of
+  // E8M0 1.0 for the query scales
+  static constexpr int kSfTOff = kSfOff + kStages * kSfTileBytes;
+  static constexpr int kBarOff = kSfTOff + (MX ? 3 * 512 : 0);
+  // mbarriers: full/empty per stage, qfull/qempty/tfull/tempty x2, drain;
+  // then the abort flag and the TMEM address slot (one word each)
+  static constexpr int kNumBars = 2 * kStages + 8 + 1;
   static constexpr int kBarBytes = (kNumBars * 8 + 8 + 127) / 128 * 128;
   static constexpr int kPlanOff = kBarOff + kBarBytes;  // row lengths, tile prefix
   static constexpr int kSmem = kPlanOff + 4 * (2 * kInlinePlanRows + 4);
@@ -224,6 +230,7 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
   uint8_t* stages = smem;
   uint8_t* qbuf = smem + C::kStages * C::kStageBytes;
   uint8_t* sfbuf = smem + C::kSfOff;           // MX: [kStages][128 rows][4 B]
+  uint8_t* sft = smem + C::kSfTOff;            // MX: [2][32][16 B], then [32][16 B] of 1.0
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* full = bars;                       // [kStages]
   uint64_t* empty = bars + C::kStages;         // [kStages]
@@ -231,8 +238,7 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
   uint64_t* qempty = qfull + 2;                // [2]
   uint64_t* tfull = qempty + 2;                // [2]
   uint64_t* tempty = tfull + 2;                // [2]
-  uint64_t* sfull = tempty + 2;                // [2] (MX) A scales in tensor memory
-  uint64_t* drain = sfull + (MX ? 2 : 0);      // [1]
+  uint64_t* drain = tempty + 2;                // [1]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(drain + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1) + 1;
 
@@ -291,7 +297,6 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
       mbar_init(qempty + s, 1);
       mbar_init(tfull + s, 1);
       mbar_init(tempty + s, 4);
-      if (MX) mbar_init(sfull + s, 4);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -300,6 +305,10 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
   // Zero both query buffers: rows hi..HP-1 stay zero (padded heads).
   for (int i = threadIdx.x; i < 2 * C::kQBytes / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
+  if (MX)  // the query's E8M0 scales: 1.0 in every byte
+    for (int i = threadIdx.x; i < 32; i += blockDim.x)
+      reinterpret_cast<uint4*>(sft + 2 * 512)[i] =
+          make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
   fence_async_smem();
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
@@ -415,42 +424,66 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
         }
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && (MX || lane == 0)) {
       // --------------------------------------------------------- MMA issuer
+      // Lane 0 issues.  With MXFP4 keys the whole warp runs the loop: it
+      // rearranges each tile's scale words for tcgen05.cp (row r of the copy
+      // holds the words of tile rows r, r+32, r+64, r+96, so lane 32q + r,
+      // column q receives row 32q + r's scales: where the block-scaled MMA
+      // reads them), and lane 0 copies them into the accumulator's scale
+      // columns ahead of its MMAs.  Waits are made warp-uniform.
       constexpr uint32_t idesc = MX ? instr_desc_mx(5, 0, 128, HP)
                                     : instr_desc(0, 0, false, false, 128, HP);
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+        bool w = mbar_wait(bar, parity, abort_flag);
+        if constexpr (MX) w = __all_sync(0xffffffffu, w);
+        return w;
+      };
       RowCursor rc;
       rc.init(pre, lens, p.n_rows, t_begin);
       int qn = 0, stage = 0, acc = 0;
       uint32_t phase = 0, aphase = 0;
       const uint32_t st_base = smem_u32(stages), q_base = smem_u32(qbuf);
+      if (MX && lane == 0)  // query scales (no swizzle, 16-byte rows, 8-row groups 128 B apart)
+        tmem_cp_32x128b_x4(tmem + C::kSfbCol, smem_desc(smem_u32(sft + 2 * 512), 16, 128, 0));
       for (int t = t_begin; t < t_end; ++t) {
         const bool fresh = rc.advance(p, t) || t == t_begin;
         if (fresh) {
-          if (qn > 0) mma_commit(qempty + ((qn - 1) & 1));
-          if (!mbar_wait(qfull + (qn & 1), (qn >> 1) & 1, abort_flag)) break;
+          if (qn > 0 && lane == 0) mma_commit(qempty + ((qn - 1) & 1));
+          if (!wait_all(qfull + (qn & 1), (qn >> 1) & 1)) break;
           ++qn;
         }
         const int qs = (qn - 1) & 1;
-        if (!mbar_wait(full + stage, phase, abort_flag)) break;
-        if (!mbar_wait(tempty + acc, aphase ^ 1, abort_flag)) break;
-        if (MX && !mbar_wait(sfull + acc, aphase, abort_flag)) break;
-        tc_fence_after();
-        const uint32_t a0 = st_base + stage * C::kStageBytes;
-        const uint32_t b0 = q_base + qs * C::kQBytes;
-#pragma unroll
-        for (int kk = 0; kk < C::kKSteps; ++kk) {
-          const uint64_t ad = smem_desc(a0 + kk * 32, 16, C::kSbo, C::kSwizzle);
-          const uint64_t bd = smem_desc(b0 + kk * 32, 16, C::kSbo, C::kSwizzle);
-          if (MX)  // K step kk takes byte kk of each row's scale word
-            mma_mx(tmem + acc * HP, ad, bd, idesc | mx_scale_ids(kk, kk),
-                   tmem + C::kSfaCol + 32 * acc, tmem + C::kSfbCol, kk > 0 ? 1u : 0u);
-          else
-            mma_f8(tmem + acc * HP, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        if (!wait_all(full + stage, phase)) break;
+        if (!wait_all(tempty + acc, aphase ^ 1)) break;
+        if (MX) {  // MMA(i-2) has finished with this accumulator's scale copy
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(sfbuf + stage * C::kSfTileBytes);
+          reinterpret_cast<uint4*>(sft + acc * 512)[lane] =
+              make_uint4(src[lane], src[32 + lane], src[64 + lane], src[96 + lane]);
+          fence_async_smem();
+          __syncwarp();
         }
-        issued_mma = true;
-        mma_commit(empty + stage);
-        mma_commit(tfull + acc);
+        if (lane == 0) {
+          tc_fence_after();
+          if (MX)
+            tmem_cp_32x128b_x4(tmem + C::kSfaCol + 32 * acc,
+                               smem_desc(smem_u32(sft + acc * 512), 16, 128, 0));
+          const uint32_t a0 = st_base + stage * C::kStageBytes;
+          const uint32_t b0 = q_base + qs * C::kQBytes;
+#pragma unroll
+          for (int kk = 0; kk < C::kKSteps; ++kk) {
+            const uint64_t ad = smem_desc(a0 + kk * 32, 16, C::kSbo, C::kSwizzle);
+            const uint64_t bd = smem_desc(b0 + kk * 32, 16, C::kSbo, C::kSwizzle);
+            if (MX)  // K step kk takes byte kk of each row's scale word
+              mma_mx(tmem + acc * HP, ad, bd, idesc | mx_scale_ids(kk, kk),
+                     tmem + C::kSfaCol + 32 * acc, tmem + C::kSfbCol, kk > 0 ? 1u : 0u);
+            else
+              mma_f8(tmem + acc * HP, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          }
+          issued_mma = true;
+          mma_commit(empty + stage);
+          mma_commit(tfull + acc);
+        }
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
         if (++acc == 2) { acc = 0; aphase ^= 1; }
       }
@@ -458,25 +491,7 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
       // ----------------------------------------------------------- epilogue
       const int quad = warp & 3;  // TMEM lane quadrant this warp may access
       const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-      // MX: this warp's 32 rows of the A scales of local tile i go to the
-      // scale columns of accumulator i % 2 once the tile's copy has landed
-      auto stage_scales = [&](int i) -> bool {
-        if (!mbar_wait(full + i % C::kStages, (uint32_t)((i / C::kStages) & 1), abort_flag))
-          return false;
-        const uint32_t sf = *reinterpret_cast<const uint32_t*>(
-            sfbuf + (i % C::kStages) * C::kSfTileBytes + 4 * (32 * quad + lane));
-        tmem_st1(tmem + lane_base + C::kSfaCol + 32 * (i & 1) + quad, sf);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sfull + (i & 1));
-        return true;
-      };
       bool ok = true;
-      if (MX) {  // query scales: E8M0 1.0 in every byte; then the first two tiles
-        tmem_st2(tmem + lane_base + C::kSfbCol, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-        for (int i = 0; i < 2 && ok && t_begin + i < t_end; ++i) ok = stage_scales(i);
-      }
       RowCursor rc;
       rc.init(pre, lens, p.n_rows, t_begin);
       int acc = 0;
@@ -502,7 +517,7 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
 #pragma unroll
         for (int c = 0; c < HP; c += 16) {
           uint32_t (&rr)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[c]);
-          tmem_ld16(tmem + acc * HP + c + ((uint32_t)(32 * quad) << 16), rr);
+          tmem_ld16(tmem + lane_base + acc * HP + c, rr);
         }
         tmem_ld_wait();
 #pragma unroll
@@ -510,8 +525,6 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty + acc);
-        // MMA(i) has read this accumulator's scale columns: stage tile i + 2's
-        if (MX && t + 2 < t_end && !stage_scales(t + 2 - t_begin)) break;
         // four independent partial sums over the heads (head h into s4[h % 4]),
         // two at a time with the packed fp32 FMA, then their sum.  The
         // epilogue's instruction count is on the kernel's critical path.
