@@ -129,6 +129,74 @@ def quant_append_rows(kv, pos, cos_tab, sin_tab, rope_dim):
     return quantize_fp4(rope_rotate(kv, pos, cos_tab, sin_tab, rope_dim))
 
 
+# ------------------------------------------ step 1b: m = 2 pair compression
+# The exponential of the pair weights, written out so that every operation is
+# one fp32 rounding (Cody-Waite range reduction, then the Taylor series of
+# e^r to degree 7): the kernels evaluate the same sequence, so the compressed
+# rows -- and the FP4 codes they decide -- agree bit for bit.
+INV_LN2 = np.float32(1.0 / math.log(2.0))
+LN2_HI = np.float32(2839.0 / 4096.0)                 # 12 significant bits: k * LN2_HI is exact
+LN2_LO = np.float32(math.log(2.0) - 2839.0 / 4096.0)
+EXP_TAYLOR = [np.float32(1.0 / math.factorial(i)) for i in range(8)]
+EXP_MIN = np.float32(-80.0)                          # below: e^x is taken as 0
+
+
+def exp_neg_f32(x):
+    """e^x for fp32 x <= 0, one fp32 rounding per operation; 0 below -80.
+
+    k = rint(x / ln 2); r = (x - k ln2_hi) - k ln2_lo; e^r by Horner on the
+    degree-7 Taylor polynomial; times 2^k (exact: k >= -116 keeps it normal).
+    Pinned: within 4 ulp of e^x across [-80, 0], exactly 1 at 0.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    k = np.rint(x * INV_LN2).astype(np.float32)
+    r = (x - k * LN2_HI) - k * LN2_LO
+    p = EXP_TAYLOR[7]
+    for c in EXP_TAYLOR[6::-1]:
+        p = p * r + c
+    t = np.ldexp(p, k.astype(np.int32)).astype(np.float32)
+    return np.where(x < EXP_MIN, np.float32(0.0), t).astype(np.float32)
+
+
+def pair_weights(z0, z1):
+    """Per-channel softmax of the two compression logits of a pair (fp32).
+
+    [KN] "Causal Encoder-Decoder" and the symbol table: Z_l is the weight used
+    when forming a compressed global KV entry; [ID] "CSA2: reuse memory and
+    reuse selection independently": CSA2 groups non-overlapping source
+    positions and drops the compressor's positional embedding.  The pages do
+    not print the combination; the reading is a softmax of Z over the group's
+    positions, channel by channel.  With d = z1 - z0 and t = e^-|d|:
+    the larger logit gets 1 / (1 + t), the other t / (1 + t).
+    Pinned: equal logits give exactly (1/2, 1/2); the weights sum to 1 within
+    1 ulp; swapping the pair swaps them; far-apart logits select one row.
+    """
+    z0 = np.asarray(z0, dtype=np.float32)
+    z1 = np.asarray(z1, dtype=np.float32)
+    d = z1 - z0
+    t = exp_neg_f32(-np.abs(d))
+    s = np.float32(1.0) + t
+    big = np.float32(1.0) / s
+    small = t / s
+    w1 = np.where(d >= 0, big, small).astype(np.float32)
+    w0 = np.where(d >= 0, small, big).astype(np.float32)
+    return w0, w1
+
+
+def compress_pairs(kv, z):
+    """Source rows [2T, D] and their logits [2T, D] -> T compressed rows (fp32).
+
+    Entry j combines source positions 2j and 2j+1 (m = 2, the encoder's
+    ratio, [KN] symbol table): c = w0 * x0 + w1 * x1 per channel, two fp32
+    products and one fp32 sum.  The entry is then rotated at its compressed
+    position j and quantised like any main-KV row.
+    """
+    kv = np.asarray(kv, dtype=np.float32)
+    z = np.asarray(z, dtype=np.float32)
+    w0, w1 = pair_weights(z[0::2], z[1::2])
+    return (w0 * kv[0::2] + w1 * kv[1::2]).astype(np.float32)
+
+
 def fp8_cast(x):
     """fp32 -> E4M3 codes (SWA rows, indexer keys and queries)."""
     return e4m3_encode(x)
