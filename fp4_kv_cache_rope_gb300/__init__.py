@@ -61,6 +61,7 @@ _workspace_size = _sig("csa2_workspace_size", [_CP, _i32, _i32], ctypes.c_size_t
 _entry_bytes = _sig("csa2_entry_bytes", [_i32], _i64)
 _fp8_quant = _sig("csa2_fp8_quant", [_p, _i64, _p, _p])
 _quant_append = _sig("csa2_quant_append", [_CP, _p, _p, _i32, _p, _p])
+_quant_append_pairs = _sig("csa2_quant_append_pairs", [_CP, _p, _p, _p, _i32, _p, _p])
 _index_full = _sig("csa2_index_full", [_CP, _p, _p, _i32, _i32, _p, _p, _i32, _i32,
                                        _p, _p, _p, _p, _p, _p])
 _index_full_noalloc = _sig("csa2_index_full_noalloc", [_CP, _p, _p, _i32, _i32, _p, _p, _i32,
@@ -81,7 +82,7 @@ KERNEL_QUANT, KERNEL_INDEXER, KERNEL_SELECT, KERNEL_ATTENTION = 0, 1, 2, 3
 EXPORTED = ["csa2_workspace_size", "csa2_entry_bytes", "csa2_fp8_quant", "csa2_quant_append",
             "csa2_index_full", "csa2_index_reindex", "csa2_attn_decode", "csa2_attn_prefill",
             "csa2_get_status", "csa2_reset_status", "csa2_status_string",
-            "csa2_set_launch_events", "csa2_index_full_noalloc"]
+            "csa2_set_launch_events", "csa2_index_full_noalloc", "csa2_quant_append_pairs"]
 
 
 class Csa2Error(RuntimeError):
@@ -132,6 +133,12 @@ def fp8_quant(x, out, stream=None):
 def quant_append(cache, kv, idx_k_in, T, ws, stream=None):
     _check(_quant_append(ctypes.byref(cache.struct), _ptr(kv), _ptr(idx_k_in), T, _ptr(ws),
                          _stream(stream)), "csa2_quant_append")
+
+
+def quant_append_pairs(cache, kv, z, idx_k_in, T, ws, stream=None):
+    """Append T entries per sequence, each compressed from 2 source rows (m = 2)."""
+    _check(_quant_append_pairs(ctypes.byref(cache.struct), _ptr(kv), _ptr(z), _ptr(idx_k_in), T,
+                               _ptr(ws), _stream(stream)), "csa2_quant_append_pairs")
 
 
 def index_full(cache, q_idx, w, hi, tq, q_pos, batch_ids, n_batch, k, out_idx, out_cnt,

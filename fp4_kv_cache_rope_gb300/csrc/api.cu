@@ -120,7 +120,22 @@ csa2_status csa2_quant_append(const csa2_cache* cache, const float* kv, const fl
   if (T > cache->max_len) return CSA2_ERR_INVALID;
   uint8_t* w = static_cast<uint8_t*>(ws);
   const WsLayout L = layout_for(cache, 1);
-  return from_cuda(launch_quant_append(*cache, kv, idx_k_in, T,
+  return from_cuda(launch_quant_append(*cache, kv, nullptr, idx_k_in, T,
+                                       reinterpret_cast<uint32_t*>(w + L.status),
+                                       (cudaStream_t)stream));
+}
+
+csa2_status csa2_quant_append_pairs(const csa2_cache* cache, const float* kv, const float* z,
+                                    const float* idx_k_in, int32_t T, void* ws, void* stream) {
+  if (!cache_ok(cache) || !kv || !z || !ws || T < 0 || !aligned16(kv) || !aligned16(z) ||
+      !aligned16(ws))
+    return CSA2_ERR_INVALID;
+  if (idx_k_in && !aligned16(idx_k_in)) return CSA2_ERR_INVALID;
+  if (T == 0) return CSA2_OK;
+  if (T > cache->max_len) return CSA2_ERR_INVALID;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const WsLayout L = layout_for(cache, 1);
+  return from_cuda(launch_quant_append(*cache, kv, z, idx_k_in, T,
                                        reinterpret_cast<uint32_t*>(w + L.status),
                                        (cudaStream_t)stream));
 }

@@ -50,8 +50,9 @@ void record_launch_end(int family, cudaStream_t s);
 
 // quant.cu
 cudaError_t launch_fp8_quant(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
-cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const float* idx_in,
-                                int32_t T, uint32_t* status, cudaStream_t s);
+cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const float* z,
+                                const float* idx_in, int32_t T, uint32_t* status,
+                                cudaStream_t s);
 
 // Description of the query rows of one indexer call.
 struct RowSet {

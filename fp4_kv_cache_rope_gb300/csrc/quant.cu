@@ -28,6 +28,7 @@ constexpr int64_t kSmallAppendGroups = 8 * 512;
 
 struct QuantParams {
   const float* kv;
+  const float* z;       // pair compression: logits [B, 2T, D], else null
   const float* idx_in;
   uint8_t* codes;
   uint8_t* scales;
@@ -43,6 +44,47 @@ struct QuantParams {
   int32_t groups_main, groups_total;  // per row
   uint32_t* status;
 };
+
+// ------------------------------------------------------ m = 2 compression
+// An encoder entry combines two source positions with per-channel weights:
+// the softmax of the two compression logits ("DeepSeek-V4.1-Flash" knowledge
+// note, symbol table and "Causal Encoder-Decoder": Z_l is the weight used when
+// forming a compressed global KV entry; "Inside DeepSeek V4.1 Flash", "CSA2:
+// reuse memory and reuse selection independently": non-overlapping groups, no
+// positional embedding).  Every step is one fp32 rounding, written out (no
+// library exponential, no contraction), so the rows -- and the FP4 codes they
+// decide -- are reproducible exactly: e^x for x <= 0 by Cody-Waite reduction
+// with ln 2 split as 2839/4096 + remainder, then the degree-7 Taylor series.
+constexpr float kInvLn2 = (float)(1.0 / 0.6931471805599453);
+constexpr float kLn2Hi = (float)(2839.0 / 4096.0);
+constexpr float kLn2Lo = (float)(0.6931471805599453 - 2839.0 / 4096.0);
+
+__device__ __forceinline__ float exp_nonpos(float x) {
+  if (x < -80.0f) return 0.0f;
+  const float k = rintf(__fmul_rn(x, kInvLn2));
+  const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(k, kLn2Hi)), __fmul_rn(k, kLn2Lo));
+  float p = (float)(1.0 / 5040.0);
+  p = __fadd_rn(__fmul_rn(p, r), (float)(1.0 / 720.0));
+  p = __fadd_rn(__fmul_rn(p, r), (float)(1.0 / 120.0));
+  p = __fadd_rn(__fmul_rn(p, r), (float)(1.0 / 24.0));
+  p = __fadd_rn(__fmul_rn(p, r), (float)(1.0 / 6.0));
+  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  // times 2^k, exact: k >= -116 here, so the result stays a normal float
+  return __fmul_rn(p, __int_as_float((127 + (int)k) << 23));
+}
+
+// c = w0 x0 + w1 x1 with (w0, w1) the softmax of (z0, z1).
+__device__ __forceinline__ float combine_pair(float x0, float x1, float z0, float z1) {
+  const float d = __fsub_rn(z1, z0);
+  const float t = exp_nonpos(-fabsf(d));
+  const float s = __fadd_rn(1.0f, t);
+  const float big = __fdiv_rn(1.0f, s), small = __fdiv_rn(t, s);
+  const float w0 = d >= 0.0f ? small : big;
+  const float w1 = d >= 0.0f ? big : small;
+  return __fadd_rn(__fmul_rn(w0, x0), __fmul_rn(w1, x1));
+}
 
 // MXFP4 indexer key, one 32-channel block per thread: the E8M0 scale code is
 // the OCP Microscaling shared exponent floor(log2 amax) - 2 (E2M1's top
@@ -102,16 +144,39 @@ __device__ __forceinline__ void quant_group(const QuantParams& p, int64_t gid) {
   // the input rows do not depend on the position: request them first
   float y[16];
   {
-    const float4* src =
-        is_idx ? reinterpret_cast<const float4*>(p.idx_in + row * p.di + 16 * (g - p.groups_main))
-               : reinterpret_cast<const float4*>(p.kv + row * p.D + 16 * g);
+    if (p.z && !is_idx) {  // entry i of sequence b from source rows 2i, 2i+1
+      const int64_t r0 = ((int64_t)b * p.T + i) * 2 * p.D + 16 * g;
+      const float4* x0 = reinterpret_cast<const float4*>(p.kv + r0);
+      const float4* x1 = reinterpret_cast<const float4*>(p.kv + r0 + p.D);
+      const float4* z0 = reinterpret_cast<const float4*>(p.z + r0);
+      const float4* z1 = reinterpret_cast<const float4*>(p.z + r0 + p.D);
+      float4 a[4], c[4], u[4], v4[4];
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const float4 f = __ldg(src + v);
-      y[4 * v + 0] = f.x;
-      y[4 * v + 1] = f.y;
-      y[4 * v + 2] = f.z;
-      y[4 * v + 3] = f.w;
+      for (int v = 0; v < 4; ++v) {
+        a[v] = __ldg(x0 + v);
+        c[v] = __ldg(x1 + v);
+        u[v] = __ldg(z0 + v);
+        v4[v] = __ldg(z1 + v);
+      }
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        y[4 * v + 0] = combine_pair(a[v].x, c[v].x, u[v].x, v4[v].x);
+        y[4 * v + 1] = combine_pair(a[v].y, c[v].y, u[v].y, v4[v].y);
+        y[4 * v + 2] = combine_pair(a[v].z, c[v].z, u[v].z, v4[v].z);
+        y[4 * v + 3] = combine_pair(a[v].w, c[v].w, u[v].w, v4[v].w);
+      }
+    } else {
+      const float4* src =
+          is_idx ? reinterpret_cast<const float4*>(p.idx_in + row * p.di + 16 * (g - p.groups_main))
+                 : reinterpret_cast<const float4*>(p.kv + row * p.D + 16 * g);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const float4 f = __ldg(src + v);
+        y[4 * v + 0] = f.x;
+        y[4 * v + 1] = f.y;
+        y[4 * v + 2] = f.z;
+        y[4 * v + 3] = f.w;
+      }
     }
   }
   const int64_t pos = (int64_t)p.seq_len[b] + i;
@@ -223,10 +288,12 @@ cudaError_t launch_fp8_quant(const float* x, int64_t n, uint8_t* out, cudaStream
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const float* idx_in,
-                                int32_t T, uint32_t* status, cudaStream_t s) {
+cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const float* z,
+                                const float* idx_in, int32_t T, uint32_t* status,
+                                cudaStream_t s) {
   QuantParams p;
   p.kv = kv;
+  p.z = z;
   p.idx_in = idx_in;
   p.codes = c.kv_codes;
   p.scales = c.kv_scales;

@@ -173,6 +173,30 @@ csa2_status csa2_quant_append(const csa2_cache *cache, const float *kv, const fl
                               int32_t T, void *ws, void *stream);
 
 /*
+ * Step 1 for an encoder cache (compression ratio m = 2): entry i of sequence
+ * b combines source rows 2i and 2i+1 and is appended at entry position
+ * p = seq_len[b] + i ("DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache
+ * Compression" knowledge note, symbol table (m = 2 in the encoder; Z_l the
+ * weight used when forming a compressed entry) and "Causal Encoder-Decoder";
+ * "Inside DeepSeek V4.1 Flash: CED, CSA2 and the 890-Byte KV Cache", "CSA2:
+ * reuse memory and reuse selection independently": non-overlapping groups,
+ * no positional embedding).  The pages do not print the combination; this
+ * library takes a per-channel softmax of the two logits:
+ *   d = z1 - z0, t = e^-|d| (0 when |d| > 80), s = 1 + t,
+ *   the larger logit's row gets 1/s, the other t/s, c = w0 x0 + w1 x1,
+ * every operation one fp32 rounding (e^x by Cody-Waite reduction with ln 2 =
+ * 2839/4096 + (ln 2 - 2839/4096), then Horner on the degree-7 Taylor
+ * polynomial, times 2^k).  The entry is then rotated at p and quantised
+ * exactly as csa2_quant_append does.
+ * kv, z:    device fp32 [B, 2T, D] source rows before rotation and their
+ *           compression logits, 16-byte aligned.
+ * idx_k_in: device fp32 [B, T, di] (one indexer key per entry) or NULL.
+ * Afterwards seq_len[b] += T (entries).  Errors as csa2_quant_append.
+ */
+csa2_status csa2_quant_append_pairs(const csa2_cache *cache, const float *kv, const float *z,
+                                    const float *idx_k_in, int32_t T, void *ws, void *stream);
+
+/*
  * Steps 2-3, Full layer: score every visible position and select.
  * q_idx:    device E4M3 [B, Tq, Hi, di] indexer queries.
  * w:        device fp32 [B, Tq, Hi] head weights.

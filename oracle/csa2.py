@@ -149,8 +149,9 @@ def exp_neg_f32(x):
     Pinned: within 4 ulp of e^x across [-80, 0], exactly 1 at 0.
     """
     x = np.asarray(x, dtype=np.float32)
-    k = np.rint(x * INV_LN2).astype(np.float32)
-    r = (x - k * LN2_HI) - k * LN2_LO
+    xc = np.maximum(x, EXP_MIN)          # below the cut the result is 0 anyway
+    k = np.rint(xc * INV_LN2).astype(np.float32)
+    r = (xc - k * LN2_HI) - k * LN2_LO
     p = EXP_TAYLOR[7]
     for c in EXP_TAYLOR[6::-1]:
         p = p * r + c

@@ -32,9 +32,17 @@ class SeqRef:
 
     # ---- cache contents ----------------------------------------------------
     def cache_rows(self, positions):
-        """(codes, scales) the cache must hold at ``positions``."""
-        x = host_rows_normal(self.wl.seed, synth.T_KV, self.b, positions, self.wl.dim, self.mult)
-        return O.quant_append_rows(x, np.asarray(positions), self.cos, self.sin, self.wl.rope_dim)
+        """(codes, scales) the cache must hold at ``positions`` (entries; for an
+        m = 2 cache each entry compresses source rows 2j and 2j+1)."""
+        positions = np.asarray(positions, dtype=np.int64)
+        if getattr(self.wl, "compress", 1) == 2:
+            src = np.stack([2 * positions, 2 * positions + 1], axis=1).reshape(-1)
+            x = host_rows_normal(self.wl.seed, synth.T_KV, self.b, src, self.wl.dim, self.mult)
+            z = host_rows_normal(self.wl.seed, synth.T_Z, self.b, src, self.wl.dim) * np.float32(2.0)
+            x = O.compress_pairs(x, z)
+        else:
+            x = host_rows_normal(self.wl.seed, synth.T_KV, self.b, positions, self.wl.dim, self.mult)
+        return O.quant_append_rows(x, positions, self.cos, self.sin, self.wl.rope_dim)
 
     @property
     def mx_keys(self):

@@ -41,6 +41,7 @@ T_POOL = 11       # supplied pools for Reindex sequences
 T_PRIOR = 12      # supplied prior indices for Reuse sequences
 T_NEWKV = 13      # the new token's main-KV row appended each decode step
 T_NEWIDXK = 14    # the new token's indexer key appended each decode step
+T_Z = 15          # compression logits of encoder source rows (m = 2), N(0,1) x 2, fp32
 LAYER_STRIDE = 100  # tensor id offset between layers of one CSA2 group
 
 

@@ -19,7 +19,7 @@ import subprocess
 
 import numpy as np
 
-from . import (LAYER_STRIDE, NORMAL_TABLE, T_IDXK, T_KV, T_PAGE, T_POOL, T_PRIOR, T_Q, T_QIDX,
+from . import (LAYER_STRIDE, NORMAL_TABLE, T_IDXK, T_KV, T_Z, T_PAGE, T_POOL, T_PRIOR, T_Q, T_QIDX,
                T_SWA, T_W, outlier_multipliers, permutation, rope_table, sample_distinct,
                stream_key)
 from .workloads import FULL, REINDEX, REUSE, Workload
@@ -176,17 +176,29 @@ class DeviceWorkload:
         return view
 
     def fill_cache(self, chunk_rows=1 << 16):
-        """Append positions 0..N_b-1 of every sequence through quant_append."""
+        """Append entries 0..N_b-1 of every sequence through quant_append (or,
+        for an m = 2 cache, quant_append_pairs over source rows 0..2N_b-1)."""
         wl = self.wl
         for b, n in enumerate(wl.lengths):
             v = self.seq_view(b)
             for t0 in range(0, n, chunk_rows):
                 m = min(chunk_rows, n - t0)
-                kv = gen_rows_normal(wl.seed, T_KV, b, t0, m, wl.dim, self.mult, self.device)
                 ik = gen_rows_normal(wl.seed, T_IDXK, b, t0, m, wl.idx_dim, None, self.device)
-                self.K.quant_append(v, kv, ik, m, self.ws)
+                if wl.compress == 2:
+                    kv, z = self.pair_sources(b, t0, m)
+                    self.K.quant_append_pairs(v, kv, z, ik, m, self.ws)
+                else:
+                    kv = gen_rows_normal(wl.seed, T_KV, b, t0, m, wl.dim, self.mult, self.device)
+                    self.K.quant_append(v, kv, ik, m, self.ws)
         import torch
         torch.cuda.synchronize()
+
+    def pair_sources(self, b, e0, m):
+        """Source rows 2e0..2(e0+m)-1 of sequence b and their compression logits."""
+        wl = self.wl
+        kv = gen_rows_normal(wl.seed, T_KV, b, 2 * e0, 2 * m, wl.dim, self.mult, self.device)
+        z = gen_rows_normal(wl.seed, T_Z, b, 2 * e0, 2 * m, wl.dim, None, self.device) * 2.0
+        return kv, z
 
     def new_token_inputs(self, step_positions):
         """fp32 main-KV and indexer-key rows of the next token of every sequence."""

@@ -36,6 +36,8 @@ class Workload:
     pool_blocks: int = 2048  # pool capacity in 8-position blocks
     extra_capacity: int = 0  # positions reserved for tokens appended by decode steps
     idx_format: str = "e4m3"  # indexer-key storage: "e4m3" (1 B/channel) or "mxfp4"
+    compress: int = 1        # m: source positions per main-KV entry (2 for encoder caches);
+                             # lengths count entries
 
     @property
     def max_len(self) -> int:
