@@ -1,0 +1,87 @@
+"""GPU parity of the whole-model CSA2 decode schedule: two decode tokens (the
+second completes a pair, so every encoder cache gains an m = 2 entry) through
+the 38 CSA2 layers, every layer checked against the oracle:
+
+* Full layers (2, 8, 14 on the encoder caches, 20 on the decoder cache):
+  top-k sets and, for layer 20, the pool;
+* Reindex layers (24, 28, 32, 36) over layer 20's pool;
+* every layer's attention output (Full, Reindex and the 30 Reuse layers, each
+  with its own query and window over its group's selection), where the GPU's
+  selection equals the oracle's.
+"""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import fp4_kv_cache_rope_gb300 as K  # noqa: E402
+from checks import check_attention, check_select  # noqa: E402
+from fp4_kv_cache_rope_gb300.schedule import FULL, REINDEX, DecodeSchedule  # noqa: E402
+from oracle import csa2 as O  # noqa: E402
+from oracle.workload import SeqRef  # noqa: E402
+from synth.model import ModelInputs  # noqa: E402
+from synth.workloads import Workload  # noqa: E402
+
+
+def test_two_decode_tokens_through_all_layers():
+    base = Workload("model-mini", 2, [3000, 520], 128, 32, 8, 64, 16, 64, 16, seed=61,
+                    outlier_frac=0.02, extra_capacity=8)
+    m = ModelInputs(base)
+    sch = DecodeSchedule(m.caches, m.workspaces, base.heads, base.idx_heads, base.topk,
+                         base.window)
+    n = list(base.lengths)
+    for step in range(2):                      # tokens n (even), then n + 1 (odd)
+        pos = [x + step for x in n]
+        dec_in, enc_in = m.token_inputs(pos)
+        assert (enc_in is not None) == (step == 1)
+        sch.append(dec_in[0], dec_in[1], enc_in)
+        sch.layers(m.inputs, m.out)
+    torch.cuda.synchronize()
+    for dw in m.dws:
+        assert K.get_status(dw.ws) == 0
+    k = base.topk
+    idx = {h: t.cpu().numpy() for h, t in sch.idx.items()}
+    cnt = {h: t.cpu().numpy() for h, t in sch.cnt.items()}
+    pool, pcnt = sch.pool.cpu().numpy(), sch.pool_cnt.cpu().numpy()
+    compared = total = 0
+    for b in range(base.batch):
+        entries = [(n[b] + 2) // 2] * 3 + [n[b] + 2]
+        refs = [SeqRef(wl, b, n=entries[c]) for c, wl in enumerate(m.wls)]
+        for c in range(3):
+            assert int(m.caches[c].seq_len[b]) == entries[c]
+        assert int(m.caches[3].seq_len[b]) == entries[3]
+        sel = {}
+        rpool = None
+        for p in sch.plan:
+            ref = refs[p.cache]
+            nvis = entries[p.cache]
+            if p.mode == FULL:
+                s, ridx, rp = ref.full(p.layer, k, n=nvis)
+                gi = idx[p.layer][b, : cnt[p.layer][b]]
+                check_select(gi, s, np.arange(nvis), k, f"layer {p.layer} b={b}")
+                if p.cache == 3:
+                    gp = pool[b, 0, : pcnt[b, 0]]
+                    check_select(gp, O.block_maxima(s), np.arange(-(-nvis // 8)), K.POOL_BLOCKS,
+                                 f"pool b={b}")
+                    rpool = rp if set(gp.tolist()) == set(rp.tolist()) else None
+                sel[p.layer] = (gi, ridx)
+            elif p.mode == REINDEX:
+                gi = idx[p.layer][b, : cnt[p.layer][b]]
+                if rpool is None:
+                    sel[p.layer] = (gi, None)
+                    continue
+                s2, pos2, ridx = ref.reindex(p.layer, rpool, k, n=nvis)
+                check_select(gi, s2, pos2, k, f"layer {p.layer} b={b}")
+                sel[p.layer] = (gi, ridx)
+            gi, ridx = sel[p.selection]
+            total += 1
+            if ridx is not None and set(gi.tolist()) == set(ridx.tolist()):
+                check_attention(m.out[p.layer][b].cpu().numpy(), ref.attention(p.layer, ridx),
+                                f"attention layer {p.layer} b={b}")
+                compared += 1
+    assert total == 38 * base.batch
+    assert compared >= 0.75 * total
