@@ -439,6 +439,311 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------- whole-model decode step
+def model_oracle_sample(base, b, positions_n):
+    """One sequence of one model decode token on the oracle: the 38 CSA2
+    layers (4 Full scans, 4 Reindex scans, 38 attentions) over caches holding
+    positions_n tokens.  Inputs are prepared untimed; returns the timed work."""
+    import numpy as np
+    from oracle import csa2 as O
+    from oracle.formats import bf16_bits_to_f64
+    from oracle.workload import SeqRef
+    from fp4_kv_cache_rope_gb300.schedule import FULL, REINDEX, layer_plan
+    from synth.model import model_workloads
+    wls = model_workloads(base)
+    entries = [positions_n // 2] * 3 + [positions_n]
+    refs = [SeqRef(wl, b, n=entries[c]) for c, wl in enumerate(wls)]
+    plan = layer_plan()
+    for p in plan:
+        refs[p.cache].inputs(p.layer)
+    for r in refs:
+        r.idxk_all()
+
+    def run():
+        sel, pool = {}, None
+        for p in plan:
+            ref = refs[p.cache]
+            if p.mode == FULL:
+                s, idx, pl = ref.full(p.layer, base.topk)
+                sel[p.layer] = idx
+                if p.cache == 3:
+                    pool = pl
+            elif p.mode == REINDEX:
+                sel[p.layer] = ref.reindex(p.layer, pool, base.topk)[2]
+            ref.attention(p.layer, sel[p.selection])
+    return run
+
+
+def model_bench(args):
+    """bench.py --workload 9: one decode token per sequence through the
+    model's 38 CSA2 layers per step (fp4_kv_cache_rope_gb300.schedule)."""
+    import torch
+    import fp4_kv_cache_rope_gb300 as K
+    from fp4_kv_cache_rope_gb300.schedule import REUSE, DecodeSchedule
+    from synth.model import ModelInputs
+    from synth.workloads import get_workload
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    base = get_workload(9)
+    if args.batch:
+        base.batch = args.batch
+        base.lengths = base.lengths[: args.batch]
+        base.name += "-first" + str(args.batch)
+    base.extra_capacity = args.steps + args.warmup + 16
+    m = ModelInputs(base)
+    sch = DecodeSchedule(m.caches, m.workspaces, base.heads, base.idx_heads, base.topk,
+                         base.window)
+    B, n0 = base.batch, list(base.lengths)
+    tok = [m.token_inputs([n + par for n in n0]) for par in (0, 1)]   # even / odd token rows
+    starts = [c.seq_len.clone() for c in m.caches]
+    layers_per = len(sch.plan)
+
+    def reset():
+        for c, s0 in zip(m.caches, starts):
+            c.seq_len.copy_(s0)
+        for w in m.workspaces:
+            K.reset_status(w)
+        torch.cuda.synchronize()
+
+    every = max(1, min(EVENT_EVERY, args.steps))
+    sampled = lambda i: i % every == every // 2
+    watch = {(20, "index"): K.KERNEL_INDEXER, (2, "index"): K.KERNEL_INDEXER,
+             (24, "index"): K.KERNEL_INDEXER, (21, "attention"): K.KERNEL_ATTENTION}
+    n_ev = sum(1 for i in range(args.steps) if sampled(i))
+    evs = {key: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(max(n_ev, 1))] for key in watch}
+    for lst in evs.values():
+        for a, b in lst:
+            a.record()
+            b.record()
+    torch.cuda.synchronize()
+
+    def one_step(i, inputs=None, out=None, token=None, take=False, j=0):
+        dec, enc = token if token is not None else tok[i % 2]
+        sch.append(dec[0], dec[1], enc)
+
+        def hook(p, phase, before):
+            key = (p.layer, phase)
+            if take and key in watch:
+                if before:
+                    K.set_launch_events(watch[key], *evs[key][j])
+                else:
+                    K.set_launch_events(watch[key])
+        sch.layers(inputs or m.inputs, out or m.out, hook if take else None)
+        return sch.launches(enc is not None)
+
+    def run_steps(n, with_events=False):
+        cnt = 0
+        for i in range(n):
+            take = with_events and sampled(i)
+            cnt += one_step(i, take=take, j=i // every)
+        return cnt
+
+    reset()
+    run_steps(args.warmup)
+    reset()
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            launches = run_steps(args.steps, True)
+        reset()
+        graph.replay()
+        torch.cuda.synchronize()
+        reset()
+    clocks = ClockSampler(local)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0.record()
+    if graph is not None:
+        graph.replay()
+    else:
+        launches = run_steps(args.steps, True)
+    t1.record()
+    torch.cuda.synchronize()
+    time.sleep(0.1)
+    clk = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    status = [K.get_status(w) for w in m.workspaces]
+    us = {f"{l}:{ph}": statistics.mean(a.elapsed_time(b) for a, b in evs[(l, ph)][:n_ev]) * 1e3
+          for (l, ph) in watch}
+    value = job_throughput(layers_per * args.steps, world, ms)
+    # the dominant kernel: 38 attention launches per step against 8 indexer
+    # launches; attention flops per launch = 4 H (k + W) D per sequence
+    attn_flops = 4.0 * base.heads * (base.topk + base.window) * base.dim * B
+    attn_us = us["21:attention"]
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tf_peak, tf_kind = float(json.load(f)["bf16_tflops_sustained"]), "measured (sustained)"
+    except Exception:
+        tf_peak, tf_kind = 1700.0, "fallback (sustained)"
+    ach = attn_flops / (attn_us * 1e-6) / 1e12
+    idx_total = us["20:index"] + 3 * us["2:index"] + 4 * us["24:index"]
+    roofline = {"bound": "tensor", "kernel": "attention_kernel", "achieved": ach, "peak": tf_peak,
+                "unit": "TFLOP/s", "frac": ach / tf_peak, "traffic": None, "peak_source": tf_kind,
+                "flops_per_launch": attn_flops, "launch_us": attn_us,
+                "share_of_step": 38 * attn_us / (ms / args.steps * 1e3),
+                "timed_launches": n_ev,
+                "sampling": f"CUDA events on every {every}th timed step (layer 21's attention)"}
+    del graph
+
+    # ---- e2e through the API: per step the appended rows and every layer's
+    # query-side inputs are copied from pinned host memory, and the last
+    # layer's output is read back; copies on two streams, double buffered.
+    modes = {p.layer: p.mode for p in sch.plan}
+    need = lambda L: ("q", "swa") if modes[L] == REUSE else ("q", "swa", "q_idx", "w")
+    host = {}
+    for L, inp in m.inputs.items():
+        for name in need(L):
+            host[(L, name)] = inp[name].cpu().pin_memory()
+    for par in (0, 1):
+        dec, enc = tok[par]
+        host[("dec", par, 0)], host[("dec", par, 1)] = dec[0].cpu().pin_memory(), dec[1].cpu().pin_memory()
+        if enc is not None:
+            for g in range(3):
+                for r in range(3):
+                    host[("enc", g, r)] = enc[g][r].cpu().pin_memory()
+    bufs = []
+    for _ in range(2):
+        dev_inputs = {L: {n: torch.empty_like(inp[n]) for n in need(L)}
+                      for L, inp in m.inputs.items()}
+        dev_dec = [torch.empty_like(t) for t in tok[0][0]]
+        dev_enc = [tuple(torch.empty_like(t) for t in tok[1][1][g]) for g in range(3)]
+        out = {L: (torch.empty_like(o) if L == 39 else o) for L, o in m.out.items()}
+        bufs.append((dev_inputs, dev_dec, dev_enc, out, torch.empty(m.out[39].shape).pin_memory()))
+    h2d_even = sum(t.numel() * t.element_size() for k_, t in host.items()
+                   if k_[0] not in ("dec", "enc") or (k_[0] == "dec" and k_[1] == 0))
+    h2d_odd = sum(t.numel() * t.element_size() for k_, t in host.items()
+                  if k_[0] not in ("dec", "enc") or (k_[0] == "dec" and k_[1] == 1) or k_[0] == "enc")
+    d2h = m.out[39].numel() * 4
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    e_steps = max(args.steps // 4, 10)
+    pool = [torch.cuda.Event() for _ in range(3 * e_steps + 6)]
+    for e in pool:
+        e.record()
+    torch.cuda.synchronize()
+
+    def e2e_steps(n):
+        comp = torch.cuda.current_stream()
+        s_in.wait_stream(comp)
+        s_out.wait_stream(comp)
+        in_ready, comp_done, out_done = pool[0:n], pool[n:2 * n], pool[2 * n:3 * n]
+
+        def issue_h2d(i):
+            di, dd, de, _, _ = bufs[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(comp_done[i - 2])
+                for L, inp in di.items():
+                    for name, t in inp.items():
+                        t.copy_(host[(L, name)], non_blocking=True)
+                par = i % 2
+                dd[0].copy_(host[("dec", par, 0)], non_blocking=True)
+                dd[1].copy_(host[("dec", par, 1)], non_blocking=True)
+                if par:
+                    for g in range(3):
+                        for r in range(3):
+                            de[g][r].copy_(host[("enc", g, r)], non_blocking=True)
+                in_ready[i].record(s_in)
+
+        issue_h2d(0)
+        for i in range(n):
+            if i + 1 < n:
+                issue_h2d(i + 1)
+            di, dd, de, out, pinned = bufs[i % 2]
+            comp.wait_event(in_ready[i])
+            if i >= 2:
+                comp.wait_event(out_done[i - 2])
+            one_step(i, inputs=di, out=out, token=((dd[0], dd[1]), de if i % 2 else None))
+            comp_done[i].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[i])
+                pinned.copy_(out[39], non_blocking=True)
+                out_done[i].record(s_out)
+        comp.wait_stream(s_in)
+        comp.wait_stream(s_out)
+
+    def timed(fn):
+        reset()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return job_throughput(layers_per * e_steps, world, max_over_ranks(e0.elapsed_time(e1), world))
+
+    reset()
+    e2e_steps(2)
+    e2e_eager = timed(lambda: e2e_steps(e_steps))
+    e2e_graph, e2e_note = None, None
+    if not args.eager:
+        try:
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g2, capture_error_mode="thread_local"):
+                e2e_steps(e_steps)
+            reset()
+            g2.replay()
+            e2e_graph = timed(g2.replay)
+            del g2
+        except Exception as exc:
+            e2e_note = f"graph capture of the copies failed: {type(exc).__name__}: {exc}"[:200]
+            torch.cuda.synchronize()
+    e2e_value = e2e_graph if e2e_graph is not None else e2e_eager
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        run = model_oracle_sample(base, 0, n0[0])
+        t = time.perf_counter()
+        run()
+        dt = time.perf_counter() - t
+        cpu = {"value": layers_per / (dt * B), "unit": "layer-steps/s", "cores": os.cpu_count(),
+               "kind": "oracle",
+               "sample": f"sequence 0 of {B}: its 38 CSA2 layers of one decode token (4 Full and "
+                         f"4 Reindex scans, selections, 38 attentions) in numpy fp64, scaled to "
+                         f"the batch", "seconds_per_sequence": dt}
+    if rank == 0:
+        line = {
+            "metric": "CSA2 decode layer-steps/s, whole-model schedule (38 CSA2 layers per token)",
+            "value": value, "unit": "layer-steps/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3/e2m1 storage; fp8 and f16 tensor-core MMA, f32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": base.name, "batch": B, "ctx_tokens": max(n0),
+                       "encoder_entries": max(n0) // 2, "topk": base.topk, "window": base.window,
+                       "layers_per_step": layers_per,
+                       "model_steps_per_s": value / layers_per,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "launch": "eager" if args.eager else "cuda_graph",
+                       "l2": "inputs exceed L2 (four caches of 1-2 GB)"},
+            "roofline": roofline,
+            "kernels_us": {"decoder_full_indexer": us["20:index"],
+                           "encoder_full_indexer": us["2:index"],
+                           "reindex_indexer": us["24:index"], "attention": attn_us,
+                           "indexers_per_step": idx_total, "attention_per_step": 38 * attn_us},
+            "e2e": {"value": e2e_value, "unit": "layer-steps/s",
+                    "h2d_bytes_per_step": (h2d_even + h2d_odd) / 2, "d2h_bytes_per_step": d2h,
+                    "steps": e_steps, "cuda_graph": e2e_graph is not None, "eager_value": e2e_eager,
+                    "copies": "per step: appended rows and every layer's query-side inputs in, "
+                              "the last layer's output back, on two copy streams",
+                    **({"note": e2e_note} if e2e_note else {})},
+            "gpu_launches": launches,
+            "clocks": clk,
+            "device_status": status,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 # -------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -456,6 +761,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return reference_arm(args)
+    if args.workload == 9:
+        return model_bench(args)
 
     import numpy as np
     import torch

@@ -70,7 +70,7 @@ def _modes(seed: int, batch: int) -> list:
 
 
 def get_workload(i: int) -> Workload:
-    """Workload number i (1..8)."""
+    """Workload number i (1..9)."""
     if i == 1:
         return Workload("tiny-full-decode-b1-n2048-d128", 1, [2048], 128, 32, 4, 32,
                         16, 64, 128, seed=0)
@@ -105,6 +105,12 @@ def get_workload(i: int) -> Workload:
         # per position instead of 128)
         return Workload("full-decode-b32-n131072-d576-mxfp4-keys", 32, [131072] * 32, 576, 64, 64,
                         128, 64, 2048, 128, seed=1, outlier_frac=0.01, idx_format="mxfp4")
+    if i == 9:
+        # one decode token through the whole model's 38 CSA2 layers (synth.model:
+        # three encoder caches of m = 2 entries, one decoder cache); lengths
+        # count tokens
+        return Workload("model-decode-38-layers-b32-n131072-d576", 32, [131072] * 32, 576, 64, 64,
+                        128, 64, 2048, 128, seed=7, outlier_frac=0.01)
     raise ValueError(f"no workload {i}")
 
 
