@@ -358,15 +358,29 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
                               full + stage);
           } else {
             const int rpl = p.rows_per_load;
+            const int nu = 128 / rpl;
             int nload = 0;
             int64_t src_rows[16];
-            for (int u = 0; u < 128 / rpl; ++u) {
+            // the units' page-table entries, all requested before any is used
+            const int32_t* pt = p.map.page_table + (int64_t)b * p.map.max_pages_per_seq;
+            int32_t phys[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const int64_t pg = (t0 + (int64_t)u * rpl) / p.map.page_size;
+              phys[u] = u < nu ? __ldg(pt + (pg < p.map.max_pages_per_seq ? pg : p.map.max_pages_per_seq - 1))
+                               : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
               const int64_t pos = t0 + (int64_t)u * rpl;
               src_rows[u] = -1;
-              if (pos < len) {
-                const int64_t r = p.map.row(b, pos);
-                if (r < 0) set_status(p.status, CSA2_DEV_BAD_PAGE);
-                else { src_rows[u] = r; ++nload; }
+              if (u < nu && pos < len) {
+                if (phys[u] < 0 || phys[u] >= p.map.num_pages) {
+                  set_status(p.status, CSA2_DEV_BAD_PAGE);
+                } else {
+                  src_rows[u] = (int64_t)phys[u] * p.map.page_size + pos % p.map.page_size;
+                  ++nload;
+                }
               }
             }
             bytes = (uint32_t)(nload * rpl * (C::kKRowBytes + (MX ? 4 : 0)));
@@ -383,19 +397,42 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
           int pc = p.pool_cnt[(int64_t)b * p.tq + tq];
           pc = pc < 0 ? 0 : (pc > kPoolBlocks ? kPoolBlocks : pc);
           const int32_t* pool = p.pool_blocks + ((int64_t)b * p.tq + tq) * kPoolBlocks;
-          int64_t src_rows[16];
-          int nload = 0;
+          // the tile's 16 block ids, then (paged caches) their page-table
+          // entries, each as 16 loads in flight at once: loads issued one
+          // after another behind their checks would cost one L2 round trip
+          // each (clamped indices keep every load inside its array)
+          int blk[16];
+#pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int pi = j * 16 + e;
+            blk[e] = __ldg(pool + (pi < kPoolBlocks ? pi : kPoolBlocks - 1));
+          }
+          int32_t phys[16];
+          if (p.map.page_size != 0) {
+            const int32_t* pt = p.map.page_table + (int64_t)b * p.map.max_pages_per_seq;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int64_t pg = (int64_t)(blk[e] > 0 ? blk[e] : 0) * kBlock / p.map.page_size;
+              phys[e] = __ldg(pt + (pg < p.map.max_pages_per_seq ? pg : p.map.max_pages_per_seq - 1));
+            }
+          }
+          int64_t src_rows[16];
+          int nload = 0;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
             src_rows[e] = -1;
-            if (pi < pc) {
-              const int blk = pool[pi];
-              if (blk < 0 || (int64_t)blk * kBlock >= len) {
+            if (j * 16 + e < pc) {
+              const int64_t t0b = (int64_t)blk[e] * kBlock;
+              if (blk[e] < 0 || t0b >= len) {
                 set_status(p.status, CSA2_DEV_BAD_POOL);
+              } else if (p.map.page_size == 0) {
+                src_rows[e] = (int64_t)b * p.map.max_len + t0b;
+                ++nload;
+              } else if (phys[e] < 0 || phys[e] >= p.map.num_pages) {
+                set_status(p.status, CSA2_DEV_BAD_PAGE);
               } else {
-                const int64_t r = p.map.row(b, (int64_t)blk * kBlock);
-                if (r < 0) set_status(p.status, CSA2_DEV_BAD_PAGE);
-                else { src_rows[e] = r; ++nload; }
+                src_rows[e] = (int64_t)phys[e] * p.map.page_size + t0b % p.map.page_size;
+                ++nload;
               }
             }
           }

@@ -115,7 +115,8 @@ def page_table_for(wl: Workload):
     """Seeded random physical page ids: [B, max_pages] int32, -1 where unused."""
     ps = wl.page_size
     max_pages = -(-wl.max_len // ps)
-    need = [-(-min(wl.max_len, n + 64 + max(wl.prefill_tokens, 0)) // ps) for n in wl.lengths]
+    need = [-(-min(wl.max_len, n + 64 + max(wl.prefill_tokens, 0) + wl.extra_capacity) // ps)
+            for n in wl.lengths]
     need = [min(max_pages, x) for x in need]
     total = int(sum(need))
     perm = permutation(wl.seed, T_PAGE, total)
