@@ -135,6 +135,49 @@ __device__ __forceinline__ bool named_sync_or(int id, int n, bool pred) {
   return r != 0;
 }
 
+// f16 copy of the query rows [heads x D] (bf16, at qs) into the swizzled Q
+// slabs, by all 288 threads of the CTA (thread t of n), assuming no head needs
+// scaling; returns, over the CTA, whether some |q| >= 2^14 (then the data
+// warps redo the copy with a power-of-two scale per head).  Rows past `heads`
+// are zero.
+template <int NSLAB>
+__device__ __forceinline__ bool convert_query(const uint8_t* qs, uint8_t* sq, int t, bool ok,
+                                              int heads) {
+  constexpr int D = NSLAB * 64;
+  constexpr int kChunks = D / 8;     // 16-byte chunks per head row
+  constexpr int kAll = 64 * kChunks;
+  constexpr int kSlab = 64 * 128;
+  constexpr int n = 288;
+  bool big = false;
+  for (int i0 = t; i0 < kAll; i0 += 4 * n) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + n * u;
+      v[u] = (ok && i < kAll && i / kChunks < heads) ? *reinterpret_cast<const uint4*>(qs + i * 16)
+                                                     : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + n * u;
+      if (i >= kAll) break;
+      const int h = i / kChunks, c = i - h * kChunks;
+      const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t r[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        big |= ((w4[q] & 0x7F80u) >= (141u << 7)) | (((w4[q] >> 16) & 0x7F80u) >= (141u << 7));
+        __half2 h2 = __floats2half2_rn(__uint_as_float(w4[q] << 16),
+                                       __uint_as_float(w4[q] & 0xFFFF0000u));
+        r[q] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      *reinterpret_cast<uint4*>(sq + (c >> 3) * kSlab + h * 128 + (((c & 7) ^ (h & 7)) << 4)) =
+          make_uint4(r[0], r[1], r[2], r[3]);
+    }
+  }
+  return named_sync_or(4, 288, big);
+}
+
 // 2^x with the hardware approximation (relative error about 2^-22; the
 // weights are rounded to f16 afterwards).
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -427,47 +470,15 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
     load_raw(src_next, raw);
     KeySrc src_n1 = resolve_src(1, resolve_pos(1));
     int pos3 = resolve_pos(2);
-    // ---- query: f16 copy of the bf16 rows.  When some |q| >= 2^14 the head
-    // is scaled by a power of two so that its f16 copy stays exact.
+    // ---- query: f16 copy of the bf16 rows, by all nine warps.  When some
+    // |q| >= 2^14 the data warps redo it with each head scaled by a power of
+    // two so that its f16 copy stays exact.
     bool ok = mbar_wait(q_full, 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     {
       const uint8_t* qs = sx + C::kXBytes;
       constexpr int kChunks = D / 8;  // 16-byte chunks per head row
-      bool big = false;
-      for (int i = dt; i < p.heads * kChunks && ok; i += 128) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qs + i * 16);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          big |= ((w4[u] & 0x7F80u) >= (141u << 7)) | (((w4[u] >> 16) & 0x7F80u) >= (141u << 7));
-      }
-      if (!named_sync_or(4, 128, big)) {
-        constexpr int kAll = 64 * kChunks;  // multiple of 4 * 128
-        static_assert(kAll % 512 == 0, "query chunks");
-        for (int i0 = dt; i0 < kAll; i0 += 512) {
-          uint4 v[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = i0 + 128 * u;
-            v[u] = (ok && i / kChunks < p.heads) ? *reinterpret_cast<const uint4*>(qs + i * 16)
-                                                 : make_uint4(0, 0, 0, 0);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = i0 + 128 * u;
-            const int h = i / kChunks, c = i - h * kChunks;
-            const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-            uint32_t r[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              __half2 h2 = __floats2half2_rn(__uint_as_float(w4[q] << 16),
-                                             __uint_as_float(w4[q] & 0xFFFF0000u));
-              r[q] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            st_swz(sq + (c >> 3) * C::kSlab, h, c & 7, make_uint4(r[0], r[1], r[2], r[3]));
-          }
-        }
+      if (!convert_query<NSLAB>(qs, sq, tid, ok, p.heads)) {
         if (dt < 64) qmul[dt] = p.scale_log2;
       } else {
         constexpr int kPer = (kChunks + 31) / 32;
@@ -653,6 +664,10 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
     // over the four threads; the sums stay per thread until the end.
     const int hA = 16 * warp + (lane >> 2), hB = hA + 8;
     const int cq = 2 * (lane & 3);  // this thread's first key in each group of 8
+    {  // a share of the query conversion
+      const bool okq = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag));
+      convert_query<NSLAB>(sx + C::kXBytes, sq, tid, okq, p.heads);
+    }
     named_sync(1, 288);  // Q slabs written
     float mA = -INFINITY, mB = -INFINITY, lA = 0.0f, lB = 0.0f;
     const float qmA = qmul[hA], qmB = qmul[hB];
@@ -757,6 +772,10 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
     named_sync(2, 288);
   } else {
     // ================================================================ MMA warp
+    {  // a share of the query conversion
+      const bool okq = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag));
+      convert_query<NSLAB>(sx + C::kXBytes, sq, tid, okq, p.heads);
+    }
     named_sync(1, 288);  // Q slabs written
     if (lane == 0 && nloc > 0) {
       constexpr uint32_t idesc_qk = instr_desc(0, 0, false, false, 64, 64);

@@ -272,3 +272,27 @@ def test_invalid_arguments_rejected():
         K.attn_decode(dw.cache, inp["q"].view(torch.int16), 65, oi.view(wl.batch, -1),
                       oc.view(-1), 64, inp["swa"], None, wl.window, 0.0,
                       torch.empty(1, device="cuda"), dw.ws)  # more than 64 heads
+
+
+def test_attention_with_large_queries(tiny):
+    """Heads whose |q| reach 2^14 and beyond take the scaled f16 copy; the
+    output must still match the oracle (which uses the bf16 values exactly)."""
+    wl, dw = tiny
+    inp = dw.layer_inputs(0)
+    q = inp["q"].clone()                                   # bf16 [1, 1, H, D]
+    scale = torch.ones(wl.heads, dtype=torch.float32, device="cuda")
+    scale[0], scale[3], scale[7] = 2.0 ** 15, 2.0 ** 20, 2.0 ** -20
+    q = (q.float() * scale.view(1, 1, -1, 1)).to(torch.bfloat16)
+    n = wl.lengths[0]
+    idx = torch.arange(0, n, n // wl.topk, dtype=torch.int32, device="cuda")[: wl.topk].view(1, -1)
+    cnt = torch.tensor([wl.topk], dtype=torch.int32, device="cuda")
+    out = torch.empty((1, wl.heads, wl.dim), dtype=torch.float32, device="cuda")
+    K.attn_decode(dw.cache, q.view(torch.int16), wl.heads, idx, cnt, wl.topk, inp["swa"], None,
+                  wl.window, 0.0, out, dw.ws)
+    assert K.get_status(dw.ws) == 0
+    ref = SeqRef(wl, 0)
+    qb = q.view(torch.int16).cpu().numpy().view(np.uint16).reshape(wl.heads, wl.dim)
+    rows = np.concatenate([ref.dequant_rows(idx.cpu().numpy()[0]),
+                           O.swa_rows_decode(ref.inputs(0)["swa"][: wl.window])])
+    expect = O.sparse_attention(F.bf16_bits_to_f64(qb), rows)
+    check_attention(out[0].cpu().numpy(), expect, "large queries")
