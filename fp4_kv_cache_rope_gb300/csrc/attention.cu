@@ -382,13 +382,6 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
     return;
   }
   const int row = blockIdx.y, split = blockIdx.x;
-  const RowKeys rk = row_keys(p, row, D);
-  const int nk = rk.n_global + rk.n_swa;
-  const int nchunk = (nk + C::kKeys - 1) / C::kKeys;
-  const int c0 = (int)((int64_t)nchunk * split / p.splits);
-  const int c1 = (int)((int64_t)nchunk * (split + 1) / p.splits);
-  const int nloc = c1 - c0;
-  const bool direct = p.splits == 1;
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -403,16 +396,29 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
     mbar_init(p_full, 4);
     *abort_flag = 0;
     fence_barrier_init();
+  }
+  if (warp == 8) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // everything read from here on may come from the previous kernels (the
+  // selection, seq_len, and whatever wrote the query)
+  griddep_wait();
+  griddep_launch_dependents();
+  if (tid == 0) {
     // the query rows [H, D] bf16 are contiguous: one bulk copy into X tile 1,
     // which holds no slab before the second chunk
     const uint32_t qbytes = (uint32_t)(p.heads * D * 2);
     mbar_arrive_expect_tx(q_full, qbytes);
     bulk_load(sx + C::kXBytes, p.q + (int64_t)row * p.heads * D, qbytes, q_full);
   }
-  if (warp == 8) tmem_alloc(tmem_slot, C::kTmemCols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  const RowKeys rk = row_keys(p, row, D);
+  const int nk = rk.n_global + rk.n_swa;
+  const int nchunk = (nk + C::kKeys - 1) / C::kKeys;
+  const int c0 = (int)((int64_t)nchunk * split / p.splits);
+  const int c1 = (int)((int64_t)nchunk * (split + 1) / p.splits);
+  const int nloc = c1 - c0;
+  const bool direct = p.splits == 1;
   const uint32_t tmem = *tmem_slot;
   const uint32_t tO = tmem + C::kSCols;
 
@@ -875,13 +881,14 @@ static cudaError_t run_attention(AttnParams p, cudaStream_t s) {
   cfg.blockDim = dim3(288, 1, 1);
   cfg.dynamicSmemBytes = (size_t)C::kSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;  // the split CTAs of a row
   attr[0].val.clusterDim.x = (unsigned)p.splits;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   record_launch_begin(CSA2_KERNEL_ATTENTION, s);
   e = cudaLaunchKernelEx(&cfg, kern, p);
   record_launch_end(CSA2_KERNEL_ATTENTION, s);

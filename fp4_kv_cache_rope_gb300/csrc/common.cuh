@@ -171,6 +171,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ---------------------------------------------- programmatic dependent launch
+// The step's kernels are launched with programmatic stream serialisation, so a
+// kernel's CTAs may start while the previous kernel of the stream finishes.
+// Before touching anything that kernel writes (or reads and this one
+// overwrites) a kernel waits here: the wait returns once the previous grid has
+// completed and its memory operations are visible.  Without the launch
+// attribute it returns at once.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel of the stream start launching; its CTAs still wait in
+// griddep_wait until this grid has completed.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ async copies
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar) {

@@ -243,6 +243,7 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1) + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_wait();  // seq_len (the append) and, for many rows, the row plan
   if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled layouts need 1 KB alignment
     if (threadIdx.x == 0) set_status(p.status, CSA2_DEV_BAD_ALIGN);
     return;
@@ -314,6 +315,7 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch_dependents();
   const uint32_t tmem = *tmem_slot;
   bool issued_mma = false;
 
@@ -668,9 +670,18 @@ static cudaError_t run_indexer(const CUtensorMap& tk, const CUtensorMap& tq, con
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e == cudaSuccess) e = prefer_max_shared(kern);
   if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(kIdxCtasPerSm * num_sms), 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   record_launch_begin(CSA2_KERNEL_INDEXER, s);
-  kern<<<kIdxCtasPerSm * num_sms, 192, C::kSmem, s>>>(tk, tq, p);
+  e = cudaLaunchKernelEx(&cfg, kern, tk, tq, p);
   record_launch_end(CSA2_KERNEL_INDEXER, s);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

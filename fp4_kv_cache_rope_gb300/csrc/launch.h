@@ -14,6 +14,15 @@ namespace csa2 {
 // Every kernel of the path asks for the largest shared-memory carveout, so
 // that consecutive kernels of a step never make an SM change its L1/shared
 // split between launches.
+// Launch attribute that lets a kernel overlap the tail of the previous kernel
+// of its stream (it must call griddep_wait() before using that kernel's work).
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 template <typename Kernel>
 inline cudaError_t prefer_max_shared(Kernel kern) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,

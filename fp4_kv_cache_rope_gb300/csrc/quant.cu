@@ -246,6 +246,8 @@ __global__ void __launch_bounds__(256) quant_append_kernel(QuantParams p) {
 // group; after a cluster barrier (every read of seq_len precedes it) CTA 0
 // advances seq_len, so no second launch is needed.
 __global__ void __launch_bounds__(512) quant_append_cluster_kernel(QuantParams p) {
+  griddep_wait();  // the previous kernel reads seq_len, which this one advances
+  griddep_launch_dependents();
   const int64_t total = (int64_t)p.B * p.T * p.groups_total;
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (gid < total) quant_group(p, gid);
@@ -322,13 +324,14 @@ cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const floa
     cfg.gridDim = dim3((unsigned)ctas, 1, 1);
     cfg.blockDim = dim3(512, 1, 1);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)ctas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = prefer_max_shared(quant_append_cluster_kernel);
     if (e != cudaSuccess) return e;
     record_launch_begin(CSA2_KERNEL_QUANT, s);

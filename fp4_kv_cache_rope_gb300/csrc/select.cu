@@ -526,6 +526,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelectParams p) 
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
   constexpr int S = E * kSelThreads;
+  griddep_wait();  // the indexer's scores, block maxima and row plan
+  griddep_launch_dependents();
   const int C = cluster_size(), rank = cluster_rank();
   const int row = blockIdx.x / C, t = threadIdx.x;
   const int base = rank * S;
@@ -614,13 +616,14 @@ static cudaError_t launch_select_e(const SelectParams& p, int C, cudaStream_t s)
   cfg.blockDim = dim3(kSelThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, select_kernel<E>, p);
 }
 
