@@ -607,6 +607,317 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
   if (threadIdx.x == 0 && *abort_flag) set_status(p.status, CSA2_DEV_TIMEOUT);
 }
 
+// ------------------------------------------------ multi-query Full indexer
+// Full layers with Tq > 1 query rows per sequence (prefill chunks, multi-token
+// verify): one work unit is (sequence, group of up to 128/HP consecutive query
+// rows, 128-position key tile).  The MMA computes D[128 positions x
+// (group x HP heads)] = K_tile x Q_group^T, so a sequence's keys are read once
+// per group instead of once per query row (the per-row form re-reads them
+// from L2 for every query, which bounds it on long chunks) and the tensor core
+// runs N = 128.  Two accumulators of 128 columns per CTA, two CTAs per SM as
+// in the per-row kernel; the four epilogue warps take the group's queries in
+// turn: query g's HP accumulator columns, its head weights from shared
+// memory, its own causal limit, its own score row and block maxima.
+template <int HP, int DI>
+struct MqCfg {
+  static constexpr int kGroup = 128 / HP;           // query rows per group
+  static constexpr int kN = kGroup * HP;             // 128
+  static constexpr int kStageBytes = 128 * DI;
+  static constexpr int kStages = 4;
+  static constexpr int kQBytes = kN * DI;            // one group's query block
+  static constexpr int kWBytes = kN * 4;             // one group's head weights
+  static constexpr int kSwizzle = IdxCfg<HP, DI>::kSwizzle;
+  static constexpr uint32_t kSbo = 8 * DI;
+  static constexpr int kKSteps = DI / 32;
+  static constexpr int kTmemCols = 256;
+  static constexpr int kQOff = kStages * kStageBytes;
+  static constexpr int kWOff = kQOff + 2 * kQBytes;
+  static constexpr int kBarOff = kWOff + 2 * kWBytes;
+  static constexpr int kNumBars = 2 * kStages + 9;
+  static constexpr int kBarBytes = (kNumBars * 8 + 8 + 127) / 128 * 128;
+  static constexpr int kPlanOff = kBarOff + kBarBytes;  // group tile prefix
+  static constexpr int kSmem = kPlanOff + 4 * (kInlinePlanRows + 4);
+  static_assert(kSmem <= 113 * 1024, "multi-query indexer: two CTAs per SM");
+};
+
+// Group gi: batch entry bi (sequence b), first query t0, gsz queries.
+struct MqGroup {
+  int bi, b, t0, gsz;
+};
+__device__ __forceinline__ MqGroup mq_group(const IndexerParams& p, int gi, int G) {
+  const int gpb = (p.tq + G - 1) / G;
+  MqGroup g;
+  g.bi = gi / gpb;
+  g.t0 = (gi - g.bi * gpb) * G;
+  g.gsz = min(G, p.tq - g.t0);
+  g.b = p.batch_ids ? p.batch_ids[g.bi] : g.bi;
+  return g;
+}
+
+constexpr int kMqThreads = 192;  // producer, MMA issuer, 4 epilogue warps
+
+template <int HP, int DI>
+__global__ void __launch_bounds__(kMqThreads, kIdxCtasPerSm)
+    indexer_mq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                      IndexerParams p, int n_groups) {
+  using C = MqCfg<HP, DI>;
+  constexpr int G = C::kGroup;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* stages = smem;
+  uint8_t* qbuf = smem + C::kQOff;
+  float* wbuf = reinterpret_cast<float*>(smem + C::kWOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::kStages;
+  uint64_t* qfull = bars + 2 * C::kStages;
+  uint64_t* qempty = qfull + 2;
+  uint64_t* tfull = qempty + 2;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(drain + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1) + 1;
+  int32_t* s_pre = reinterpret_cast<int32_t*>(smem + C::kPlanOff);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_wait();  // seq_len (the append)
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) set_status(p.status, CSA2_DEV_BAD_ALIGN);
+    return;
+  }
+  // ---- plan: visible length of every query row (published by CTA 0 for the
+  // selection kernel) and the tile prefix over groups
+  if (blockIdx.x == 0) {
+    for (int row = threadIdx.x; row < p.n_rows; row += blockDim.x) {
+      int len;
+      row_tiles(p, row, len);
+      p.row_len[row] = len;
+    }
+  }
+  for (int gi = threadIdx.x; gi < n_groups; gi += blockDim.x) {
+    const MqGroup g = mq_group(p, gi, G);
+    int vmax = 0;
+    for (int q = 0; q < g.gsz; ++q) {
+      int len;
+      row_tiles(p, g.bi * p.tq + g.t0 + q, len);
+      vmax = max(vmax, len);
+    }
+    s_pre[gi + 1] = (vmax + 127) / 128;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < n_groups; base += 32) {
+      const int i = base + lane;
+      int v = i < n_groups ? s_pre[i + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      if (i < n_groups) s_pre[i + 1] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) s_pre[0] = 0;
+  }
+  __syncthreads();
+  const int total = s_pre[n_groups];
+  const int t_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
+  const int t_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < C::kStages; ++st) {
+      mbar_init(full + st, 1);
+      mbar_init(empty + st, 1);
+    }
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(qfull + st, 1);
+      mbar_init(qempty + st, 1);
+      mbar_init(tfull + st, 1);
+      mbar_init(tempty + st, 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  // zero both query blocks and weights: padded heads and queries stay zero
+  for (int i = threadIdx.x; i < 2 * C::kQBytes / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = threadIdx.x; i < 2 * C::kN; i += blockDim.x) wbuf[i] = 0.0f;
+  fence_async_smem();
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  griddep_launch_dependents();
+  const uint32_t tmem = *tmem_slot;
+  bool issued_mma = false;
+
+  if (t_begin < t_end) {
+    // the group of tile t and the group's first tile, walked in order
+    int gcur = find_row(s_pre, n_groups, t_begin);
+    auto advance = [&](int t) -> bool {  // true when tile t starts a new group
+      if (t < s_pre[gcur + 1]) return false;
+      while (t >= s_pre[gcur + 1]) ++gcur;
+      return true;
+    };
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      int qn = 0, stage = 0;
+      uint32_t phase = 0;
+      MqGroup g = mq_group(p, gcur, G);
+      int vmax = 0;
+      for (int t = t_begin; t < t_end; ++t) {
+        const bool fresh = advance(t) || t == t_begin;
+        if (fresh) {
+          g = mq_group(p, gcur, G);
+          vmax = 0;
+          for (int q = 0; q < g.gsz; ++q) {
+            int len;
+            row_tiles(p, g.bi * p.tq + g.t0 + q, len);
+            vmax = max(vmax, len);
+          }
+          const int qs = qn & 1;
+          if (!mbar_wait(qempty + qs, ((qn >> 1) & 1) ^ 1, abort_flag)) break;
+          const uint32_t wbytes = (uint32_t)(g.gsz * p.hi * 4);
+          mbar_arrive_expect_tx(qfull + qs, (uint32_t)(g.gsz * p.hi * DI) + wbytes);
+          const int64_t row0 = (int64_t)g.b * p.tq + g.t0;
+          for (int q = 0; q < g.gsz; ++q)
+            tma_load_2d(qbuf + qs * C::kQBytes + q * HP * DI, &tm_q, 0, (int)((row0 + q) * p.hi),
+                        qfull + qs);
+          bulk_load(wbuf + qs * C::kN, p.w + row0 * p.hi, wbytes, qfull + qs);
+          ++qn;
+        }
+        if (!mbar_wait(empty + stage, phase ^ 1, abort_flag)) break;
+        const int64_t t0 = (int64_t)(t - s_pre[gcur]) * 128;
+        uint8_t* dst = stages + stage * C::kStageBytes;
+        if (p.map.page_size == 0) {
+          mbar_arrive_expect_tx(full + stage, 128 * DI);
+          tma_load_2d(dst, &tm_k, 0, (int)((int64_t)g.b * p.map.max_len + t0), full + stage);
+        } else {
+          const int rpl = p.rows_per_load;
+          int nload = 0;
+          int64_t src_rows[16];
+          for (int u = 0; u < 128 / rpl; ++u) {
+            const int64_t pos = t0 + (int64_t)u * rpl;
+            src_rows[u] = -1;
+            if (pos < vmax) {
+              const int64_t r = p.map.row(g.b, pos);
+              if (r < 0) set_status(p.status, CSA2_DEV_BAD_PAGE);
+              else { src_rows[u] = r; ++nload; }
+            }
+          }
+          mbar_arrive_expect_tx(full + stage, (uint32_t)(nload * rpl * DI));
+          for (int u = 0; u < 128 / rpl; ++u)
+            if (src_rows[u] >= 0)
+              tma_load_2d(dst + u * rpl * DI, &tm_k, 0, (int)src_rows[u], full + stage);
+        }
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // --------------------------------------------------------- MMA issuer
+      int qn = 0, stage = 0, acc = 0;
+      uint32_t phase = 0, aphase = 0;
+      const uint32_t st_base = smem_u32(stages), q_base = smem_u32(qbuf);
+      uint32_t idesc = 0;
+      for (int t = t_begin; t < t_end; ++t) {
+        const bool fresh = advance(t) || t == t_begin;
+        if (fresh) {
+          if (qn > 0) mma_commit(qempty + ((qn - 1) & 1));
+          if (!mbar_wait(qfull + (qn & 1), (qn >> 1) & 1, abort_flag)) break;
+          ++qn;
+          idesc = instr_desc(0, 0, false, false, 128, mq_group(p, gcur, G).gsz * HP);
+        }
+        const int qs = (qn - 1) & 1;
+        if (!mbar_wait(full + stage, phase, abort_flag)) break;
+        if (!mbar_wait(tempty + acc, aphase ^ 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t a0 = st_base + stage * C::kStageBytes;
+        const uint32_t b0 = q_base + qs * C::kQBytes;
+#pragma unroll
+        for (int kk = 0; kk < C::kKSteps; ++kk)
+          mma_f8(tmem + acc * C::kN, smem_desc(a0 + kk * 32, 16, C::kSbo, C::kSwizzle),
+                 smem_desc(b0 + kk * 32, 16, C::kSbo, C::kSwizzle), idesc, kk > 0 ? 1u : 0u);
+        issued_mma = true;
+        mma_commit(empty + stage);
+        mma_commit(tfull + acc);
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        if (++acc == 2) { acc = 0; aphase ^= 1; }
+      }
+    } else if (warp >= 2) {
+      // ----------------------------------------------------------- epilogue
+      const int quad = warp & 3;          // tensor-memory lane quadrant
+      int acc = 0, qn = 0;
+      uint32_t aphase = 0;
+      MqGroup g = mq_group(p, gcur, G);
+      int vis[G];
+      for (int t = t_begin; t < t_end; ++t) {
+        const bool fresh = advance(t) || t == t_begin;
+        if (fresh) {
+          g = mq_group(p, gcur, G);
+#pragma unroll
+          for (int q = 0; q < G; ++q) {
+            vis[q] = 0;
+            if (q < g.gsz) row_tiles(p, g.bi * p.tq + g.t0 + q, vis[q]);
+          }
+          ++qn;
+        }
+        const float* wq = wbuf + ((qn - 1) & 1) * C::kN;
+        if (!mbar_wait(tfull + acc, aphase, abort_flag)) break;
+        tc_fence_after();
+        const int j = t - s_pre[gcur];
+        const int local = 32 * quad + lane;
+        const int pos = j * 128 + local;
+        for (int q = 0; q < g.gsz; ++q) {
+          uint32_t r[HP];
+#pragma unroll
+          for (int c = 0; c < HP; c += 16) {
+            uint32_t (&rr)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[c]);
+            tmem_ld16(tmem + acc * C::kN + q * HP + c + ((uint32_t)(32 * quad) << 16), rr);
+          }
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < HP; c += 16) reg_fence(*reinterpret_cast<uint32_t(*)[16]>(&r[c]));
+          float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+          for (int h = 0; h < HP; h += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(wq + q * p.hi + h);
+            fma2_relu(s4[0], s4[1], w4.x, w4.y, __uint_as_float(r[h]), __uint_as_float(r[h + 1]));
+            fma2_relu(s4[2], s4[3], w4.z, w4.w, __uint_as_float(r[h + 2]),
+                      __uint_as_float(r[h + 3]));
+          }
+          const float sc = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          const int64_t orow = (int64_t)g.bi * p.tq + g.t0 + q;
+          const bool valid = pos < vis[q];
+          if (valid) p.scores[orow * p.score_stride + pos] = sc;
+          float m = valid ? sc : -INFINITY;
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          if ((lane & 7) == 0 && valid) p.blockmax[orow * p.bm_stride + pos / kBlock] = m;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty + acc);
+        if (++acc == 2) { acc = 0; aphase ^= 1; }
+      }
+    }
+  }
+  __syncwarp();
+  if (warp == 1) {
+    if (lane == 0 && issued_mma) {
+      mma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never);
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+  if (threadIdx.x == 0 && *abort_flag) set_status(p.status, CSA2_DEV_TIMEOUT);
+}
+
 // Host side ---------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -685,6 +996,30 @@ static cudaError_t run_indexer(const CUtensorMap& tk, const CUtensorMap& tq, con
   return cudaGetLastError();
 }
 
+template <int HP, int DI>
+static cudaError_t run_indexer_mq(const CUtensorMap& tk, const CUtensorMap& tq,
+                                  const IndexerParams& p, int n_groups, int num_sms,
+                                  cudaStream_t s) {
+  using C = MqCfg<HP, DI>;
+  auto kern = indexer_mq_kernel<HP, DI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e == cudaSuccess) e = prefer_max_shared(kern);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(kIdxCtasPerSm * num_sms), 1, 1);
+  cfg.blockDim = dim3(kMqThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  record_launch_begin(CSA2_KERNEL_INDEXER, s);
+  e = cudaLaunchKernelEx(&cfg, kern, tk, tq, p, n_groups);
+  record_launch_end(CSA2_KERNEL_INDEXER, s);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_indexer(const csa2_cache& c, const RowSet& rows, int mode, const uint8_t* q_idx,
                            const float* w, int32_t hi, const int32_t* pool_blocks,
                            const int32_t* pool_cnt, const WsLayout& L, uint8_t* ws, int num_sms,
@@ -747,6 +1082,20 @@ cudaError_t launch_indexer(const csa2_cache& c, const RowSet& rows, int mode, co
     if (hp == 16) return run_indexer<16, 128, true>(tk, tq, p, num_sms, s);
     if (hp == 32) return run_indexer<32, 128, true>(tk, tq, p, num_sms, s);
     return run_indexer<64, 128, true>(tk, tq, p, num_sms, s);
+  }
+  // several query rows per sequence in a Full layer: the multi-query kernel
+  // (keys read once per group of 128/HP query rows), when its plan fits
+  if (mode == 0 && rows.tq > 1 && hi % 4 == 0 && (reinterpret_cast<uintptr_t>(w) & 15) == 0) {
+    const int G = 128 / hp;
+    const int64_t n_groups = (int64_t)(rows.n_rows / rows.tq) * ((rows.tq + G - 1) / G);
+    if (n_groups <= kInlinePlanRows) {
+#define CSA2_MQ_CASE(HPV, DIV) \
+  if (hp == HPV && di == DIV) return run_indexer_mq<HPV, DIV>(tk, tq, p, (int)n_groups, num_sms, s);
+      CSA2_MQ_CASE(16, 32) CSA2_MQ_CASE(16, 64) CSA2_MQ_CASE(16, 128)
+      CSA2_MQ_CASE(32, 32) CSA2_MQ_CASE(32, 64) CSA2_MQ_CASE(32, 128)
+      CSA2_MQ_CASE(64, 32) CSA2_MQ_CASE(64, 64) CSA2_MQ_CASE(64, 128)
+#undef CSA2_MQ_CASE
+    }
   }
 #define CSA2_IDX_CASE(HPV, DIV) \
   if (hp == HPV && di == DIV) return run_indexer<HPV, DIV, false>(tk, tq, p, num_sms, s);
