@@ -24,17 +24,17 @@ from fp4_kv_cache_rope_gb300.schedule import FULL, REINDEX, DecodeSchedule  # no
 from oracle import csa2 as O  # noqa: E402
 from oracle.workload import SeqRef  # noqa: E402
 from synth.model import ModelInputs  # noqa: E402
-from synth.workloads import Workload  # noqa: E402
+from synth.workloads import Workload, get_workload  # noqa: E402
 
 
-def test_two_decode_tokens_through_all_layers():
-    base = Workload("model-mini", 2, [3000, 520], 128, 32, 8, 64, 16, 64, 16, seed=61,
-                    outlier_frac=0.02, extra_capacity=8)
+def run_two_tokens(base):
+    """Two decode tokens (n even, then n + 1 completing a pair) through the 38
+    CSA2 layers; returns the model inputs and the schedule after the second."""
     m = ModelInputs(base)
     sch = DecodeSchedule(m.caches, m.workspaces, base.heads, base.idx_heads, base.topk,
                          base.window)
     n = list(base.lengths)
-    for step in range(2):                      # tokens n (even), then n + 1 (odd)
+    for step in range(2):
         pos = [x + step for x in n]
         dec_in, enc_in = m.token_inputs(pos)
         assert (enc_in is not None) == (step == 1)
@@ -43,17 +43,24 @@ def test_two_decode_tokens_through_all_layers():
     torch.cuda.synchronize()
     for dw in m.dws:
         assert K.get_status(dw.ws) == 0
+    return m, sch
+
+
+def check_layers(base, m, sch, seqs):
+    """Every layer of the second token for sequences `seqs`: selections and
+    pools against the oracle's scores, attention where the selection agrees.
+    Returns (compared, total)."""
     k = base.topk
+    n = list(base.lengths)
     idx = {h: t.cpu().numpy() for h, t in sch.idx.items()}
     cnt = {h: t.cpu().numpy() for h, t in sch.cnt.items()}
     pool, pcnt = sch.pool.cpu().numpy(), sch.pool_cnt.cpu().numpy()
     compared = total = 0
-    for b in range(base.batch):
+    for b in seqs:
         entries = [(n[b] + 2) // 2] * 3 + [n[b] + 2]
         refs = [SeqRef(wl, b, n=entries[c]) for c, wl in enumerate(m.wls)]
-        for c in range(3):
+        for c in range(4):
             assert int(m.caches[c].seq_len[b]) == entries[c]
-        assert int(m.caches[3].seq_len[b]) == entries[3]
         sel = {}
         rpool = None
         for p in sch.plan:
@@ -83,5 +90,24 @@ def test_two_decode_tokens_through_all_layers():
                 check_attention(m.out[p.layer][b].cpu().numpy(), ref.attention(p.layer, ridx),
                                 f"attention layer {p.layer} b={b}")
                 compared += 1
+    return compared, total
+
+
+def test_two_decode_tokens_through_all_layers():
+    base = Workload("model-mini", 2, [3000, 520], 128, 32, 8, 64, 16, 64, 16, seed=61,
+                    outlier_frac=0.02, extra_capacity=8)
+    m, sch = run_two_tokens(base)
+    compared, total = check_layers(base, m, sch, range(base.batch))
     assert total == 38 * base.batch
+    assert compared >= 0.75 * total
+
+
+def test_whole_model_at_full_size():
+    """The bench's whole-model workload (B = 32 sequences of 131,072 tokens):
+    two decode tokens through all 38 layers, sequences 0 and 31 checked."""
+    base = get_workload(9)
+    base.extra_capacity = 8
+    m, sch = run_two_tokens(base)
+    compared, total = check_layers(base, m, sch, (0, base.batch - 1))
+    assert total == 38 * 2
     assert compared >= 0.75 * total

@@ -5,6 +5,9 @@ configuration bench.py times:
   and 1% of the other rows bit-exact; top-k and pool of all 32 sequences;
   attention of all 32 sequences (on the oracle's own selection, where the
   GPU's selection equals it);
+* the same decode with MXFP4 indexer keys: key codes and block scales of
+  sequences 0 and 31 and 1% of the other rows bit-exact; top-k, pool and
+  attention of sequences 0, 9, 22, 31;
 * 1M-context Full -> Reindex -> Reuse group (B = 16): sequences 0, 7, 15;
 * ragged paged mixed-mode decode (B = 64): 8 sequences covering the modes;
 * prefill chunk of 4,096 tokens after 262,144: 8 sampled query rows and
@@ -109,6 +112,36 @@ def test_w2_full_layer_all_sequences(w2):
     wl, dw = w2
     t = Tally()
     full_layer_checks(wl, dw, range(wl.batch), tally=t)
+    t.done()
+
+
+@pytest.fixture(scope="module")
+def w8():
+    wl = get_workload(8)
+    return wl, DeviceWorkload(wl)
+
+
+def test_w8_mxfp4_key_bytes(w8):
+    """MXFP4 indexer keys of the 128K decode (B = 32): E2M1 codes and E8M0
+    block scales of sequences 0 and 31 in full, 1% of the other rows."""
+    wl, dw = w8
+    rng = np.random.default_rng(8)
+    c = dw.cache
+    for b in range(wl.batch):
+        n = wl.lengths[b]
+        pos = np.arange(n) if b in (0, wl.batch - 1) else np.sort(rng.choice(n, n // 100, replace=False))
+        ix = torch.tensor([c.physical_row(b, int(t)) for t in pos], dtype=torch.long, device="cuda")
+        codes = c.idx_k.index_select(0, ix).cpu().numpy()
+        scales = c.idx_scales.index_select(0, ix).cpu().numpy()
+        rc, rs = SeqRef(wl, b).idxk_rows(pos)
+        assert np.array_equal(codes[:, : wl.idx_dim // 2], rc), b
+        assert np.array_equal(scales[:, : wl.idx_dim // O.MX_BLOCK], rs), b
+
+
+def test_w8_mxfp4_full_layer_sampled_sequences(w8):
+    wl, dw = w8
+    t = Tally()
+    full_layer_checks(wl, dw, (0, 9, 22, wl.batch - 1), tally=t)
     t.done()
 
 
