@@ -93,6 +93,8 @@ struct SelSmem {
   int peer_base[kMaxCluster], peer_cnt[kMaxCluster];
   int taken[kMaxCluster];                // refine: taken boundary keys per CTA of the cluster
   int digit, above, nbd, nloc, nb_local, n_above;
+  uint32_t floor_key;                    // every key the last selection took is >= it
+  uint32_t range_hi;                     // the last selection's upper key bound
 };
 
 // Publishes m, synchronises the cluster and gathers every CTA's Mail into
@@ -147,51 +149,73 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scan, int* total) {
 // global ids [base, base + E*512); keys past its candidates are 0).  On
 // return sm.sel holds this CTA's selected global ids in ascending order
 // (sm.nloc of them), sm.peer_base / sm.peer_cnt give every CTA's share, and
-// the cluster-wide number selected is returned.  Control flow is uniform
-// over the cluster.  The loops over a thread's E keys are unrolled so that
-// their shared-memory loads are all in flight together.
+// the cluster-wide number selected is returned; sm.floor_key is a key that
+// every selected key reaches and sm.range_hi the largest key of the range the
+// search started from.  Control flow is uniform over the cluster.  The loops over a thread's E keys are unrolled twice only: with
+// 16 warps per SM the shared-memory latency is hidden across warps, and the
+// smaller code keeps the function in the instruction cache.
+//
+// floor_key != 0 states that at least k present keys of the cluster lie in
+// [floor_key, ceil_key]; the cluster-wide range exchange is then skipped and
+// the search starts from that range.  Should the counts contradict it (fewer
+// than k keys in range, or keys above ceil_key taken besides k), the
+// selection starts again with the exchange; the counts it tests are the
+// cluster's, so every CTA restarts together.
 template <int E>
-__device__ __noinline__ int block_select(SelSmem& sm, int base, int k, int C, int rank, int& par) {
+__device__ __noinline__ int block_select(SelSmem& sm, int base, int k, int C, int rank, int& par,
+                                         uint32_t floor_key, uint32_t ceil_key) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, t = threadIdx.x;
   const uint32_t* my = sm.keys + t * (E + 1);
+  if (ceil_key < floor_key) floor_key = 0u;
+restart:
   // ---- 1. range and number of the present keys over the cluster
   uint32_t mx = 0u, mn = 0xFFFFFFFFu;
   int present = 0;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const uint32_t v = my[e];
-    mx = max(mx, v);
-    mn = min(mn, v ? v : 0xFFFFFFFFu);
-    present += v != 0u;
-  }
-  mx = __reduce_max_sync(0xffffffffu, mx);
-  mn = __reduce_min_sync(0xffffffffu, mn);
-  present = __reduce_add_sync(0xffffffffu, present);
-  if (lane == 0) {
-    sm.ured[0][warp] = mx;
-    sm.ured[1][warp] = mn;
-    sm.red[warp] = present;
-  }
-  __syncthreads();
-  Mail m{};
-  if (warp == 0) {
-    m.a = __reduce_max_sync(0xffffffffu, lane < kSelWarps ? sm.ured[0][lane] : 0u);
-    m.b = __reduce_min_sync(0xffffffffu, lane < kSelWarps ? sm.ured[1][lane] : 0xFFFFFFFFu);
-    m.c = __reduce_add_sync(0xffffffffu, lane < kSelWarps ? sm.red[lane] : 0);
-  }
-  exchange(sm, m, C, par);
-  mx = 0u;
-  mn = 0xFFFFFFFFu;
-  present = 0;
-  for (int r = 0; r < C; ++r) {
-    mx = max(mx, sm.pm[r].a);
-    mn = min(mn, sm.pm[r].b);
-    present += sm.pm[r].c;
+  if (floor_key != 0u) {
+    mx = ceil_key;
+    mn = floor_key;
+    present = k;
+  } else {
+#pragma unroll 2
+    for (int e = 0; e < E; ++e) {
+      const uint32_t v = my[e];
+      mx = max(mx, v);
+      mn = min(mn, v ? v : 0xFFFFFFFFu);
+      present += v != 0u;
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    present = __reduce_add_sync(0xffffffffu, present);
+    if (lane == 0) {
+      sm.ured[0][warp] = mx;
+      sm.ured[1][warp] = mn;
+      sm.red[warp] = present;
+    }
+    __syncthreads();
+    Mail m{};
+    if (warp == 0) {
+      m.a = __reduce_max_sync(0xffffffffu, lane < kSelWarps ? sm.ured[0][lane] : 0u);
+      m.b = __reduce_min_sync(0xffffffffu, lane < kSelWarps ? sm.ured[1][lane] : 0xFFFFFFFFu);
+      m.c = __reduce_add_sync(0xffffffffu, lane < kSelWarps ? sm.red[lane] : 0);
+    }
+    exchange(sm, m, C, par);
+    mx = 0u;
+    mn = 0xFFFFFFFFu;
+    present = 0;
+    for (int r = 0; r < C; ++r) {
+      mx = max(mx, sm.pm[r].a);
+      mn = min(mn, sm.pm[r].b);
+      present += sm.pm[r].c;
+    }
   }
   k = min(k, present);
   if (k <= 0) {
     if (t < C) sm.peer_base[t] = sm.peer_cnt[t] = 0;
-    if (t == 0) sm.nloc = 0;
+    if (t == 0) {
+      sm.nloc = 0;
+      sm.floor_key = 0u;
+      sm.range_hi = 0u;
+    }
     __syncthreads();
     return 0;
   }
@@ -214,7 +238,7 @@ __device__ __noinline__ int block_select(SelSmem& sm, int base, int k, int C, in
       uint32_t* wh = sm.whist[warp];
       for (int i = lane; i < nquad * 4; i += 32) wh[i] = 0u;
       __syncwarp();
-#pragma unroll
+#pragma unroll 2
       for (int e = 0; e < E; ++e) {
         const uint32_t v = my[e];
         if (v && (v & mask) == prefix) {
@@ -265,6 +289,13 @@ __device__ __noinline__ int block_select(SelSmem& sm, int base, int k, int C, in
       for (int u = 0; u < 8; ++u) mine += c[u];
       int total;
       const int before = block_excl_scan(mine, sm.scan, &total);
+      if (floor_key != 0u && total < remaining) {
+        // only with a floor key whose promise does not hold (a NaN score
+        // missing from its block maximum): redo with the range exchange.
+        // total is the cluster's sum, so every CTA takes this branch.
+        floor_key = 0u;
+        goto restart;
+      }
       int cum = total - before - mine;  // keys in higher bins
 #pragma unroll
       for (int u = 7; u >= 0; --u) {
@@ -290,7 +321,7 @@ __device__ __noinline__ int block_select(SelSmem& sm, int base, int k, int C, in
         if (t < kMaxCluster) sm.taken[t] = 0;
         __syncthreads();
         int n_above = 0;
-#pragma unroll
+#pragma unroll 2
         for (int e = 0; e < E; ++e) {
           const uint32_t v = my[e];
           if (v == 0u) continue;
@@ -347,7 +378,7 @@ __device__ __noinline__ int block_select(SelSmem& sm, int base, int k, int C, in
   // ---- 3. ordered compaction.  Per thread: keys above the boundary (low
   // half) and boundary keys (high half: all of them, or the marked ones).
   int packed = 0;
-#pragma unroll
+#pragma unroll 2
   for (int e = 0; e < E; ++e) {
     const uint32_t v = my[e];
     const uint32_t km = v & mask;
@@ -367,23 +398,34 @@ __device__ __noinline__ int block_select(SelSmem& sm, int base, int k, int C, in
   }
   // Boundary keys of lower-ranked CTAs come first in id order; the cluster
   // takes the first `remaining` of them (refine: exactly the marked ones).
-  int on_base = 0, out_base = 0, nloc = 0;
+  // Every CTA computes every CTA's share from the same exchanged counts, so
+  // peer_base, peer_cnt and out_base agree across the cluster.
+  int on_acc = 0, on_base = 0, out_base = 0, nloc = 0;
   for (int r = 0; r < C; ++r) {
     const int a = refine ? sm.pm[r].d : sm.pm[r].c;
     const int o = refine ? sm.taken[r] : sm.pm[r].d;
-    const int taken_on = refine ? o : min(o, max(0, remaining - on_base));
+    const int taken_on = refine ? o : min(o, max(0, remaining - on_acc));
     if (r == t) {
       sm.peer_base[r] = out_base;
       sm.peer_cnt[r] = a + taken_on;
     }
-    if (r == rank) nloc = a + taken_on;
+    if (r == rank) {
+      nloc = a + taken_on;
+      on_base = on_acc;
+    }
     out_base += a + taken_on;
-    if (r < rank) on_base += o;
+    on_acc += o;
+  }
+  if (floor_key != 0u && out_base != k) {
+    // keys above ceil_key were taken besides the k (NaN scores missing from
+    // their block maxima): redo with the range exchange
+    floor_key = 0u;
+    goto restart;
   }
   const int room = refine ? 0x7FFFFFFF : max(0, remaining - on_base);  // boundary keys taken here
   int on_before = pbefore >> 16;
   int pos = (pbefore & 0xFFFF) + min(on_before, room);
-#pragma unroll
+#pragma unroll 2
   for (int e = 0; e < E; ++e) {
     const uint32_t v = my[e];
     const uint32_t km = v & mask;
@@ -394,7 +436,11 @@ __device__ __noinline__ int block_select(SelSmem& sm, int base, int k, int C, in
     }
     if (take) sm.sel[pos++] = base + t * E + e;
   }
-  if (t == 0) sm.nloc = nloc;
+  if (t == 0) {
+    sm.nloc = nloc;
+    sm.floor_key = prefix;  // selected keys have (key & mask) >= prefix, low bits of prefix 0
+    sm.range_hi = mx;
+  }
   __syncthreads();
   return k;
 }
@@ -555,7 +601,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelectParams p) 
     else
       fill_groups<E>(sm, bm, nb, span, [&](int i) { return base + i < ng ? base + i : -1; });
     // (fewer than P only if some keys are absent, i.e. NaN block maxima)
-    P = block_select<E>(sm, base, P, C, rank, par);
+    P = block_select<E>(sm, base, P, C, rank, par, 0u, 0u);
     cluster_sync();  // every CTA's selection is final before it is read
     for (; span > 1; span /= kBlock) {
       const int sub = span / kBlock;
@@ -566,7 +612,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelectParams p) 
         fill_groups<E>(sm, bm, nb, sub, [&](int i) {
           return base + i < P * kBlock ? sm.list[i / kBlock] * kBlock + i % kBlock : -1;
         });
-      P = block_select<E>(sm, base, P, C, rank, par);
+      P = block_select<E>(sm, base, P, C, rank, par, 0u, 0u);
       expand_selected(sm, base);
     }
     if (p.pool_out) {
@@ -574,10 +620,16 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelectParams p) 
       for (int i = t; i < sm.nloc; i += kSelThreads) po[i] = sm.sel[i];
     }
     if (p.pool_cnt_out && rank == 0 && t == 0) p.pool_cnt_out[orow] = P;
-    // ---- top-k over the pool's positions
+    // ---- top-k over the pool's positions.  Each of the P pool blocks holds
+    // a position whose score is its block maximum, every pool block maximum
+    // reaches the pool selection's floor key, and no score exceeds the
+    // largest block maximum: with P >= k, at least k candidates lie in that
+    // key range, which lets the selection skip its range exchange.
+    const uint32_t pool_floor = P >= p.k ? sm.floor_key : 0u;
+    const uint32_t pool_ceil = sm.range_hi;
     map_slots(sm, S, base, P, C, rank);
     fill_pool_positions<E>(sm, sc, P, len, false, base);
-    const int kk = block_select<E>(sm, base, p.k, C, rank, par);
+    const int kk = block_select<E>(sm, base, p.k, C, rank, par, pool_floor, pool_ceil);
     int32_t* oi = p.out_idx + orow * p.k + sm.peer_base[rank];
     for (int i = t; i < sm.nloc; i += kSelThreads) {
       const int c = sm.sel[i];
@@ -593,7 +645,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelectParams p) 
       sm.list[s] = pool[base / kBlock + s];
     __syncthreads();
     fill_pool_positions<E>(sm, cd, pc, len, true, base);
-    const int kk = block_select<E>(sm, base, p.k, C, rank, par);
+    const int kk = block_select<E>(sm, base, p.k, C, rank, par, 0u, 0u);
     int32_t* oi = p.out_idx + orow * p.k + sm.peer_base[rank];
     for (int i = t; i < sm.nloc; i += kSelThreads) {
       const int c = sm.sel[i];

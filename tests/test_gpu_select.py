@@ -1,5 +1,6 @@
 """GPU selection edge cases: massive exact ties in the indexer scores (few
-distinct key rows), all-equal scores, and a sequence long enough that the
+distinct key rows), all-equal scores, a tied pool boundary split over the
+CTAs of a cluster, and a sequence long enough that the
 pool is chosen through two levels of block groups.  The indexer-key bytes
 are written directly into the cache by the test (the same bytes feed the
 oracle), so ties are exact on both sides and the sets must match exactly:
@@ -70,6 +71,44 @@ def test_ties_and_equal_scores():
             assert np.array_equal(oi[b, 0, : oc[b, 0]], ridx), (b, k)
             assert pc[b, 0] == len(rpool)
             assert np.array_equal(pool[b, 0, : pc[b, 0]], rpool), (b, k)
+
+
+def test_tied_boundary_split_across_cluster():
+    """Equal block maxima on the pool boundary held by three CTAs of a row's
+    cluster and taken in part (the first `remaining` of them by position),
+    with the blocks above the boundary held by a fourth CTA.  Every CTA must
+    agree on every CTA's share: the pool slots of the first CTA are filled
+    from its peers' selections, and the top-k that follows (all its keys in
+    one tie as well) is split the same way."""
+    nb = 11164
+    wl = Workload("split-ties", 1, [nb * 8], 128, 32, 4, 32, 16, 2048, 16, seed=23)
+    dw = DeviceWorkload(wl)
+    rng = np.random.default_rng(23)
+    hi, di = wl.idx_heads, wl.idx_dim
+    q = F.e4m3_encode(rng.standard_normal((1, 1, hi, di)).astype(np.float32))
+    w = rng.random((1, 1, hi)).astype(np.float32)
+    cand = F.e4m3_encode(rng.standard_normal((16, di)).astype(np.float32))
+    sc = O.indexer_scores(q[0, 0], w[0, 0], cand)
+    order = np.argsort(-sc, kind="stable")
+    top, mid, low = cand[order[0]], cand[order[8]], cand[order[15]]
+    s_top, s_mid, s_low = sc[order[0]], sc[order[8]], sc[order[15]]
+    assert s_top > s_mid * 1.01 and s_mid > 0 and s_mid > s_low * 1.01 + 1e-6
+    blk = np.full(nb, 2)                 # below the boundary
+    blk[0:50] = 1                        # on the boundary: 50 + 50 + 3000 blocks,
+    blk[3072:3122] = 1                   # of which the first 100 are taken
+    blk[6144:9144] = 1
+    blk[9216:] = 0                       # above the boundary: 1948 blocks
+    rows = np.stack([top, mid, low])[np.repeat(blk, 8)]
+    write_idx_rows(dw, 0, rows)
+    torch.cuda.synchronize()
+    s = O.indexer_scores(q[0, 0], w[0, 0], rows)
+    for k in (1, 1024, 2048):
+        oi, oc, pool, pc = run_index(dw, q, w, k)
+        ridx, rpool = O.full_select(s, k)
+        assert pc[0, 0] == len(rpool) == K.POOL_BLOCKS
+        assert np.array_equal(pool[0, 0, : pc[0, 0]], rpool), k
+        assert oc[0, 0] == len(ridx)
+        assert np.array_equal(oi[0, 0, : oc[0, 0]], ridx), k
 
 
 def test_two_level_pool_long_sequence():
