@@ -57,7 +57,7 @@ typedef enum csa2_status {
   CSA2_OK = 0,
   CSA2_ERR_INVALID = 1,      /* argument rejected on the host; nothing launched */
   CSA2_ERR_CUDA = 2,         /* a CUDA runtime or driver call failed */
-  CSA2_ERR_UNSUPPORTED = 3,  /* valid request outside the shapes this build runs */
+  CSA2_ERR_UNSUPPORTED = 3,  /* valid request outside the shapes the library runs */
   CSA2_ERR_TIMEOUT = 4,      /* reserved for host-side waits */
   CSA2_ERR_DEVICE = 5        /* csa2_get_status found device status bits set */
 } csa2_status;

@@ -18,7 +18,7 @@ Pages followed (titles and sections):
       Optimizations": "FP4 main KV cache" (range after normalisation),
       "Hierarchical Sparse Indexer".
 
-Readings of points the pages leave open (each is also listed in the design doc):
+Readings of points the pages leave open:
 
 * RoPE rotates the last ``rope_dim`` channels in interleaved pairs
   (2i, 2i+1) with angle p * theta**(-2i/rope_dim); the cos/sin table is an
