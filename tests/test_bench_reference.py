@@ -1,0 +1,40 @@
+"""bench.py --impl reference: the oracle arm prints one JSON line with the
+GPU arm's metric, unit and config keys, times every piece of a sequence's
+layer-step, and stays within its time budget; workloads it does not cover
+print an `unavailable` line."""
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_ref(*args):
+    t0 = time.time()
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          *args], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [x for x in out.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    return json.loads(lines[0]), time.time() - t0
+
+
+def test_reference_arm_line_on_the_tiny_decode():
+    d, wall = run_ref("--workload", "1", "--steps", "40", "--warmup", "3")
+    assert d["impl"] == "reference"
+    assert d["metric"].startswith("CSA2 decode layer-steps/s")
+    assert d["unit"] == "layer-steps/s" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["e2e"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    for key in ("workload", "batch", "ctx", "topk", "window", "dim", "idx_heads", "heads"):
+        assert key in d["config"], key
+    assert d["steps"] == 40 and d["warmup"] == 3
+    assert wall < 300
+
+
+def test_reference_arm_unavailable_for_multi_query_workloads():
+    d, _ = run_ref("--workload", "6", "--steps", "2", "--warmup", "0")
+    assert d["impl"] == "reference" and "unavailable" in d
