@@ -364,7 +364,7 @@ def oracle_sample(wl, b, n, layer=0):
     from oracle import csa2 as O
     from oracle.formats import bf16_bits_to_f64
     from oracle.workload import SeqRef
-    from synth.device import host_rows_normal
+    from synth.host import host_rows_normal
     ref = SeqRef(wl, b, n=n)
     ik = ref.idxk_all(n)
     inp = ref.inputs(layer)
@@ -421,7 +421,7 @@ def oracle_pieces(wl, b, n, m, layer=0):
     from oracle import csa2 as O
     from oracle.formats import bf16_bits_to_f64
     from oracle.workload import SeqRef
-    from synth.device import host_rows_normal
+    from synth.host import host_rows_normal
     ref = SeqRef(wl, b, n=n)
     ik = ref.idxk_all(n)
     inp = ref.inputs(layer)

@@ -8,7 +8,7 @@ from __future__ import annotations
 import numpy as np
 
 import synth
-from synth.device import host_layer_inputs, host_rows_normal
+from synth.host import host_layer_inputs, host_rows_normal
 from synth.workloads import Workload
 
 from . import csa2 as O

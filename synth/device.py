@@ -22,11 +22,12 @@ import numpy as np
 from . import (LAYER_STRIDE, NORMAL_TABLE, T_IDXK, T_KV, T_Z, T_PAGE, T_POOL, T_PRIOR, T_Q, T_QIDX,
                T_SWA, T_W, outlier_multipliers, permutation, rope_table, sample_distinct,
                stream_key)
+from .host import (ROW_SHIFT, host_layer_inputs, host_rows_normal,  # noqa: F401
+                   supplied_pool, supplied_prior)
 from .workloads import FULL, REINDEX, REUSE, Workload
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB = os.path.join(HERE, "libsynth.so")
-ROW_SHIFT = 21
 
 
 def build():
@@ -101,14 +102,6 @@ def gen_rows_normal(seed, tensor_id, b, t0, n, width, chan_mult=None, device="cu
     """Rows t0..t0+n of sequence b of a [*, width] normal tensor."""
     start = ((b << ROW_SHIFT) + t0) * width
     return gen_normal((n, width), seed, tensor_id, start, chan_mult, device)
-
-
-# ------------------------------------------------------------------ host twins
-def host_rows_normal(seed, tensor_id, b, positions, width, chan_mult=None):
-    """Host copy of rows ``positions`` of sequence b (same bits as the device)."""
-    from . import normal_rows
-    rows = (np.int64(b) << ROW_SHIFT) + np.asarray(positions, dtype=np.int64)
-    return normal_rows(seed, tensor_id, rows, width, chan_mult)
 
 
 def page_table_for(wl: Workload):
@@ -231,30 +224,3 @@ class DeviceWorkload:
         swa = torch.empty(sf.shape, dtype=torch.uint8, device=self.device)
         self.K.fp8_quant(sf, swa)
         return dict(q_idx=q_idx, w=w, q=q, swa=swa, q_f32=qf, swa_f32=sf)
-
-
-def host_layer_inputs(wl: Workload, layer, b, tq=1):
-    """Host copy (fp32 / bf16 as float) of sequence b's query-side inputs."""
-    import torch
-    from . import normal_block, uniform_block
-    off = LAYER_STRIDE * layer
-    Hi, di, H, D, W = wl.idx_heads, wl.idx_dim, wl.heads, wl.dim, wl.window
-    mult = outlier_multipliers(wl.seed, wl.dim, wl.outlier_frac) if wl.outlier_frac else None
-    qf = normal_block(wl.seed, T_QIDX + off, (tq, Hi, di), start=b * tq * Hi * di)
-    w = uniform_block(wl.seed, T_W + off, (tq, Hi), start=b * tq * Hi)
-    q = normal_block(wl.seed, T_Q + off, (tq, H, D), start=b * tq * H * D)
-    qb = torch.from_numpy(q).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-    swa_rows = (tq + W - 1) if tq > 1 else W
-    sf = normal_block(wl.seed, T_SWA + off, (swa_rows, D), start=b * swa_rows * D, chan_mult=mult)
-    return dict(q_idx_f32=qf, w=w, q_bf16=qb, swa_f32=sf)
-
-
-def supplied_pool(wl: Workload, b, n):
-    """Pool given to a Reindex sequence of the ragged workload (sorted block ids)."""
-    nb = -(-n // 8)
-    return sample_distinct(wl.seed, T_POOL, b, nb, 2048)
-
-
-def supplied_prior(wl: Workload, b, n):
-    """Prior index set given to a Reuse sequence of the ragged workload."""
-    return sample_distinct(wl.seed, T_PRIOR, b, n, min(wl.topk, n))
