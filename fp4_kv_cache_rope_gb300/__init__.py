@@ -77,12 +77,14 @@ _get_status = _sig("csa2_get_status", [_p, ctypes.POINTER(ctypes.c_uint32), _p])
 _reset_status = _sig("csa2_reset_status", [_p, _p])
 _status_string = _sig("csa2_status_string", [_i32], ctypes.c_char_p)
 _set_launch_events = _sig("csa2_set_launch_events", [_i32, _p, _p])
+_set_wait_limit = _sig("csa2_set_wait_limit", [ctypes.c_uint64])
 KERNEL_QUANT, KERNEL_INDEXER, KERNEL_SELECT, KERNEL_ATTENTION = 0, 1, 2, 3
 
 EXPORTED = ["csa2_workspace_size", "csa2_entry_bytes", "csa2_fp8_quant", "csa2_quant_append",
             "csa2_index_full", "csa2_index_reindex", "csa2_attn_decode", "csa2_attn_prefill",
             "csa2_get_status", "csa2_reset_status", "csa2_status_string",
-            "csa2_set_launch_events", "csa2_index_full_noalloc", "csa2_quant_append_pairs"]
+            "csa2_set_launch_events", "csa2_index_full_noalloc", "csa2_quant_append_pairs",
+            "csa2_set_wait_limit"]
 
 
 class Csa2Error(RuntimeError):
@@ -187,6 +189,11 @@ def set_launch_events(family, begin=None, end=None):
     b = begin.cuda_event if begin is not None else None
     e = end.cuda_event if end is not None else None
     _check(_set_launch_events(family, b, e), "csa2_set_launch_events")
+
+
+def set_wait_limit(ns: int = 0):
+    """Limit of the kernels' bounded on-chip waits in ns (0 = the 2 s default)."""
+    _check(_set_wait_limit(int(ns)), "csa2_set_wait_limit")
 
 
 def get_status(ws, stream=None) -> int:

@@ -99,6 +99,14 @@ csa2_status csa2_set_launch_events(int32_t family, void* begin, void* end) {
   return CSA2_OK;
 }
 
+csa2_status csa2_set_wait_limit(uint64_t ns) {
+  const unsigned long long v = ns == 0 ? (unsigned long long)kWaitNs : (unsigned long long)ns;
+  cudaError_t e = set_wait_limit_indexer(v);
+  if (e == cudaSuccess) e = set_wait_limit_attention(v);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  return from_cuda(e);
+}
+
 size_t csa2_workspace_size(const csa2_cache* cache, int32_t max_rows, int32_t heads) {
   if (!cache_ok(cache) || max_rows <= 0 || heads <= 0 || heads > 64) return 0;
   return layout_for(cache, max_rows).total;

@@ -835,19 +835,19 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
           tc_fence_after();
           issue_qk(next_qk);
           ++next_qk;
-        } else if ((spin & 63) == 63 && (*abort_flag || globaltimer() - t0 > kWaitNs)) {
+        } else if ((spin & 63) == 63 && (*abort_flag || globaltimer() - t0 > g_wait_ns)) {
           *abort_flag = 1;
           ok = false;
         }
       }
       // let every issued MMA land before the tensor memory is freed
       mma_commit(drain);
-      volatile int never = 0;
-      mbar_wait(drain, 0, &never);
+      mbar_wait_drain(drain, 0);
     }
     __syncwarp();
     named_sync(2, 288);
   }
+  if (tid == 0) mbar_wait_drain(q_full, 0);  // the query copy, if a wait gave up early
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -855,6 +855,8 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
   if (tid == 0 && *abort_flag) set_status(p.status, CSA2_DEV_TIMEOUT);
   if (p.splits > 1) merge_splits<NSLAB>(p);
 }
+
+cudaError_t set_wait_limit_attention(unsigned long long ns) { return set_wait_limit_here(ns); }
 
 template <int NSLAB>
 static cudaError_t run_attention(AttnParams p, cudaStream_t s) {

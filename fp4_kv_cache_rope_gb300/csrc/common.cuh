@@ -18,7 +18,7 @@ constexpr int kPoolBlocks = CSA2_POOL_BLOCKS;
 constexpr int kMaxTopk = CSA2_MAX_TOPK;
 constexpr int kPoolPositions = kPoolBlocks * kBlock;   // 16,384 candidates
 constexpr int kMaxSplits = 8;               // attention split-K limit (one cluster per query row)
-constexpr uint64_t kWaitNs = 2000000000ull; // bounded on-chip waits give up after ~2 s
+constexpr uint64_t kWaitNs = 2000000000ull; // default limit of a bounded on-chip wait (~2 s)
 
 // ------------------------------------------------------------------ workspace
 // The workspace is carved into 256-byte aligned regions in this order.
@@ -153,22 +153,56 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Limit of the pipeline waits below, per translation unit (each kernel file
+// has its own copy); kWaitNs unless csa2_set_wait_limit changed it.
+static __device__ unsigned long long g_wait_ns = kWaitNs;
+
 // Waits for the phase with the given parity to complete.  Gives up after
-// kWaitNs or when *abort is set by another thread; returns false then and the
-// caller records CSA2_DEV_TIMEOUT and winds down.
+// g_wait_ns or when *abort is set by another thread; returns false then and
+// the caller records CSA2_DEV_TIMEOUT and winds down.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
+  const uint64_t lim = g_wait_ns;
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 0) {
+    if ((i & 7) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitNs) {
+      if (globaltimer() - t0 > lim) {
         *abort = 1;
         return false;
       }
     }
   }
+}
+
+// Wait used while winding down: for copies and MMAs this CTA issued, which
+// complete on their own.  It ignores the abort flag and the settable limit
+// (a CTA must not exit, or free tensor memory, while one is in flight) and
+// gives up only after the fixed kWaitNs.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0 && globaltimer() - t0 > kWaitNs) return false;
+  }
+}
+
+// Waits until every copy armed on a ring of n mbarriers has landed.  Arm i
+// (i = 0 .. armed-1) went to barrier i % n in phase i / n; phases of one
+// barrier complete in order, so waiting for the last armed phase of each
+// barrier covers all of them.
+__device__ __forceinline__ void drain_armed(uint64_t* bars, int n, int armed) {
+  for (int s = 0; s < n && s < armed; ++s) {
+    const int last = s + n * ((armed - 1 - s) / n);
+    mbar_wait_drain(bars + s, (uint32_t)((last / n) & 1));
+  }
+}
+
+// Sets this translation unit's wait limit (host side).
+static inline cudaError_t set_wait_limit_here(unsigned long long ns) {
+  return cudaMemcpyToSymbol(g_wait_ns, &ns, sizeof(ns));
 }
 
 // ---------------------------------------------- programmatic dependent launch

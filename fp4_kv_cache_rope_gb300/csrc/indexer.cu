@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
       // ------------------------------------------------------ TMA producer
       RowCursor rc;
       rc.init(pre, lens, p.n_rows, t_begin);
-      int qn = 0, stage = 0;
+      int qn = 0, stage = 0, armed = 0;
       uint32_t phase = 0;
       int b = row_seq(p, rc.row), tq = rc.row % p.tq;
       for (int t = t_begin; t < t_end; ++t) {
@@ -461,8 +461,13 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
                           p.idx_scales + 4 * src_rows[e], 4 * sf_n[e], full + stage);
             }
         }
+        ++armed;
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
+      // a CTA must not exit while a copy it started still writes its shared
+      // memory: after a timeout the consumers may have stopped reading the ring
+      drain_armed(full, C::kStages, armed);
+      drain_armed(qfull, 2, qn);
     } else if (warp == 1 && (MX || lane == 0)) {
       // --------------------------------------------------------- MMA issuer
       // Lane 0 issues.  With MXFP4 keys the whole warp runs the loop: it
@@ -595,8 +600,7 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
   if (warp == 1) {
     if (lane == 0 && issued_mma) {  // let every issued MMA land before freeing TMEM
       mma_commit(drain);
-      volatile int never = 0;
-      mbar_wait(drain, 0, &never);
+      mbar_wait_drain(drain, 0);
     }
     __syncwarp();
   }
@@ -762,7 +766,7 @@ __global__ void __launch_bounds__(kMqThreads, kIdxCtasPerSm)
     };
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------ TMA producer
-      int qn = 0, stage = 0;
+      int qn = 0, stage = 0, armed = 0;
       uint32_t phase = 0;
       MqGroup g = mq_group(p, gcur, G);
       int vmax = 0;
@@ -811,8 +815,11 @@ __global__ void __launch_bounds__(kMqThreads, kIdxCtasPerSm)
             if (src_rows[u] >= 0)
               tma_load_2d(dst + u * rpl * DI, &tm_k, 0, (int)src_rows[u], full + stage);
         }
+        ++armed;
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
+      drain_armed(full, C::kStages, armed);   // copies in flight, as above
+      drain_armed(qfull, 2, qn);
     } else if (warp == 1 && lane == 0) {
       // --------------------------------------------------------- MMA issuer
       int qn = 0, stage = 0, acc = 0;
@@ -906,8 +913,7 @@ __global__ void __launch_bounds__(kMqThreads, kIdxCtasPerSm)
   if (warp == 1) {
     if (lane == 0 && issued_mma) {
       mma_commit(drain);
-      volatile int never = 0;
-      mbar_wait(drain, 0, &never);
+      mbar_wait_drain(drain, 0);
     }
     __syncwarp();
   }
@@ -919,6 +925,8 @@ __global__ void __launch_bounds__(kMqThreads, kIdxCtasPerSm)
 }
 
 // Host side ---------------------------------------------------------------
+cudaError_t set_wait_limit_indexer(unsigned long long ns) { return set_wait_limit_here(ns); }
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,

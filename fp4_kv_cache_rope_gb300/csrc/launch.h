@@ -52,6 +52,10 @@ inline int max_active_clusters(Kernel kern, int cluster, int threads, int smem) 
   return n;
 }
 
+// Limit of the bounded on-chip waits of each kernel file (0 = the default).
+cudaError_t set_wait_limit_indexer(unsigned long long ns);
+cudaError_t set_wait_limit_attention(unsigned long long ns);
+
 // Benchmark instrumentation (api.cu): records the family's begin/end events
 // on stream s when they are set.
 void record_launch_begin(int family, cudaStream_t s);

@@ -331,6 +331,20 @@ csa2_status csa2_reset_status(void *ws, void *stream);
 #define CSA2_KERNEL_ATTENTION 3
 csa2_status csa2_set_launch_events(int32_t family, void *begin, void *end);
 
+/* Time after which a bounded on-chip wait of the kernels gives up, in
+ * nanoseconds (default 2e9: two seconds); 0 restores the default.
+ * The indexer and attention kernels keep their pipeline stages in step with
+ * mbarriers.  Each wait on one is bounded by the GPU's global timer.  When a
+ * wait runs out the kernel stops its pipeline, sets CSA2_DEV_TIMEOUT in the
+ * workspace status word, waits for the copies and MMAs it has already
+ * started, frees its tensor memory and returns.  No data computed by that
+ * launch may be used.  This call exists so that tests can make a wait run out
+ * on an ordinary launch.  It sets the limit for the current device and
+ * affects kernels launched after it returns.  It synchronises with the
+ * device, and it is not thread safe.  Errors: CSA2_ERR_CUDA when the device
+ * copy fails.  No counterpart on the pages (an implementation safety limit). */
+csa2_status csa2_set_wait_limit(uint64_t ns);
+
 /* Static string for a status code. */
 const char *csa2_status_string(csa2_status status);
 

@@ -357,3 +357,18 @@ def sparse_attention(q, rows, scale=None):
 def swa_rows_decode(swa_codes):
     """FP8 SWA rows -> float64 (plain per-element E4M3, no scale)."""
     return e4m3_decode(swa_codes)
+
+
+def swa_band_rows(p0, tq, window):
+    """Rows of a prefill chunk's SWA band that query ``tq`` attends.
+
+    [KN] "Putting It Together": every query also attends its local sliding
+    window of the most recent positions.  The chunk's queries sit at
+    positions p0 .. p0+T-1 and share one band of T+W-1 FP8 rows, row r
+    holding position p0-(W-1)+r.  Query tq at position p = p0+tq sees the
+    window positions max(0, p-W+1) .. p, i.e. band rows
+    max(tq, W-1-p0) .. tq+W-1 (rows of negative positions are skipped).
+    Pinned against a brute-force walk over the positions each query sees.
+    """
+    lo = max(tq, (window - 1) - p0)
+    return np.arange(lo, tq + window, dtype=np.int64)

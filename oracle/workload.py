@@ -118,11 +118,8 @@ class SeqRef:
             wc = wl.window if swa_count is None else swa_count
             rows.append(O.swa_rows_decode(inp["swa"][:wc]))
         else:
-            p0 = self.n_prior_positions
-            pos_q = p0 + tq
-            lo = max(tq, (wl.window - 1) - p0)
-            rows.append(O.swa_rows_decode(inp["swa"][lo:tq + wl.window]))
-            del pos_q
+            band = O.swa_band_rows(self.n_prior_positions, tq, wl.window)
+            rows.append(O.swa_rows_decode(inp["swa"][band]))
         return O.sparse_attention(q, np.concatenate(rows), scale)
 
     n_prior_positions = 0

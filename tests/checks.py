@@ -5,7 +5,12 @@
   set must contain every id whose oracle score is above the oracle's k-th
   score by more than ``RTOL_TIE`` (relative) and no id below it by more than
   that; it must have the right size, be ascending and hold valid ids only.
-* Attention rows: max_i |o_i - o*_i| / max(max_i |o*_i|, 1e-6) <= ATOL_ROW.
+* Attention rows: max_i |o_i - o*_i| / max(max_i |o*_i|, 1e-6) <= ATOL_ROW,
+  on every row.  Attention given a selection is unique; the selection itself
+  is unique only outside the tie band.  So a row is compared over the
+  oracle's own selection when the GPU chose the same set, and otherwise over
+  the GPU's set, once ``check_select`` has accepted it (it then differs from
+  the oracle's only among near-tied scores, and is a correct top-k).
   The bar (2e-3) is the one stated for the path; the kernel's own error budget
   (f16 softmax weights, fp32 accumulation) is about 1e-4.
 """
@@ -40,6 +45,16 @@ def check_select(gpu_ids, ref_scores, ref_ids, k, what="topk"):
     # number of ids decided by near-ties (informational)
     ref_set = set(ref_ids[order[:kk]].tolist())
     return len(ref_set ^ got) // 2
+
+
+def attended_set(gpu_ids, ref_ids):
+    """Index set an attention row is compared on (see the module docstring):
+    the oracle's selection if the GPU's equals it, else the GPU's accepted one."""
+    gpu_ids = np.asarray(gpu_ids, dtype=np.int64)
+    ref_ids = np.asarray(ref_ids, dtype=np.int64)
+    if set(gpu_ids.tolist()) == set(ref_ids.tolist()):
+        return ref_ids
+    return gpu_ids
 
 
 def row_error(o, ref):

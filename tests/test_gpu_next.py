@@ -10,8 +10,9 @@
   selection.
 
 Selections are compared as sets with the tie band of checks.check_select;
-attention is compared with the oracle only where the GPU's set equals the
-oracle's (the oracle never consumes a GPU output)."""
+every attention row is compared, over the oracle's selection or, where the
+GPU's differs from it only among near-ties, over the GPU's accepted one
+(checks.attended_set)."""
 import numpy as np
 import pytest
 
@@ -24,7 +25,7 @@ if not torch.cuda.is_available():
 import fp4_kv_cache_rope_gb300 as K  # noqa: E402
 import synth  # noqa: E402
 import synth.device  # noqa: E402
-from checks import check_attention, check_select  # noqa: E402
+from checks import attended_set, check_attention, check_select  # noqa: E402
 from oracle import csa2 as O  # noqa: E402
 from oracle.workload import SeqRef  # noqa: E402
 from synth.device import DeviceWorkload  # noqa: E402
@@ -60,7 +61,6 @@ def test_verify5_multi_query_decode():
                    inp["swa"], wl.window, 0.0, out, dw.ws)
     assert K.get_status(dw.ws) == 0
     o, oi_h, oc_h = out.cpu().numpy(), oi.cpu().numpy(), oc.cpu().numpy()
-    compared = 0
     for b in range(B):
         ref = SeqRef(wl, b, n=wl.lengths[b] + T)
         ref.n_prior_positions = wl.lengths[b]
@@ -71,11 +71,8 @@ def test_verify5_multi_query_decode():
             assert oc_h[b, t] == min(k, vis)
             check_select(gi, s, np.arange(vis), k, f"verify5 top-k b={b} t={t}")
             ridx = O.topk(s, k)
-            if set(gi.tolist()) == set(ridx.tolist()):
-                check_attention(o[b, t], ref.attention(0, ridx, tq=t, tq_total=T),
-                                f"verify5 attention b={b} t={t}")
-                compared += 1
-    assert compared >= 0.75 * B * T
+            check_attention(o[b, t], ref.attention(0, attended_set(gi, ridx), tq=t, tq_total=T),
+                            f"verify5 attention b={b} t={t}")
 
 
 def test_pool_aware_prefill_full_then_reindex():
@@ -104,7 +101,6 @@ def test_pool_aware_prefill_full_then_reindex():
     assert K.get_status(dw.ws) == 0
     h = {n: v.cpu().numpy() for n, v in dict(oi=oi, oc=oc, pool=pool, pcnt=pcnt, oi2=oi2,
                                                oc2=oc2, out=out).items()}
-    compared = 0
     rng = np.random.default_rng(6)
     for b in range(B):
         ref = SeqRef(wl, b, n=wl.lengths[b] + T)
@@ -121,8 +117,6 @@ def test_pool_aware_prefill_full_then_reindex():
             gi2 = h["oi2"][b, t, : h["oc2"][b, t]]
             assert h["oc2"][b, t] == min(k, len(pos))
             check_select(gi2, s2, pos, k, f"prefill reindex top-k b={b} t={t}")
-            if set(gi2.tolist()) == set(ridx2.tolist()):
-                check_attention(h["out"][b, t], ref.attention(1, ridx2, tq=t, tq_total=T),
-                                f"prefill reindex attention b={b} t={t}")
-                compared += 1
-    assert compared >= 1
+            check_attention(h["out"][b, t],
+                            ref.attention(1, attended_set(gi2, ridx2), tq=t, tq_total=T),
+                            f"prefill reindex attention b={b} t={t}")

@@ -12,7 +12,7 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("no CUDA device", allow_module_level=True)
 
-from checks import check_attention, check_select  # noqa: E402
+from checks import attended_set, check_attention, check_select  # noqa: E402
 from oracle import csa2 as O  # noqa: E402
 from oracle import formats as F  # noqa: E402
 
@@ -44,9 +44,9 @@ def test_readme_example_runs_and_matches_the_oracle():
         gi = env["idx"][b, 0, : int(env["cnt"][b, 0])].cpu().numpy()
         check_select(gi, s, rows, k, f"README top-k b={b}")
         ridx, _ = O.full_select(s, k)
-        if set(gi.tolist()) == set(ridx.tolist()):
-            sel = O.dequantize_fp4(codes[ridx], scales[ridx], D)
-            win = O.swa_rows_decode(env["swa"][b].cpu().numpy())
-            q = env["q"][b].float().cpu().numpy().astype(np.float64)
-            ref = O.sparse_attention(q, np.concatenate([sel, win]))
-            check_attention(env["out"][b].cpu().numpy(), ref, f"README attention b={b}")
+        use = attended_set(gi, ridx)
+        sel = O.dequantize_fp4(codes[use], scales[use], D)
+        win = O.swa_rows_decode(env["swa"][b].cpu().numpy())
+        q = env["q"][b].float().cpu().numpy().astype(np.float64)
+        ref = O.sparse_attention(q, np.concatenate([sel, win]))
+        check_attention(env["out"][b].cpu().numpy(), ref, f"README attention b={b}")

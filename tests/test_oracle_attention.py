@@ -100,3 +100,21 @@ def test_dequantize_matches_group_scaling():
         for c in range(32):
             nib = (codes[r, c // 2] >> (4 * (c % 2))) & 0xF
             assert x[r, c] == F.e2m1_decode(nib) * F.e4m3_decode(scales[r, c // 16])
+
+
+def test_prefill_swa_band_rows_brute_force():
+    """The SWA band of a prefill chunk: row r holds position p0-(W-1)+r, and
+    query tq (position p0+tq) must see exactly the positions q with
+    0 <= q <= p0+tq and p0+tq-q < W.  Checked by walking every position,
+    including chunks that start before W-1 (p0 < W-1: negative band rows)."""
+    for W in (1, 2, 5, 16):
+        for p0 in (0, 1, 3, W - 2, W - 1, W, 40):
+            if p0 < 0:
+                continue
+            T = 7
+            band_pos = [p0 - (W - 1) + r for r in range(T + W - 1)]
+            for tq in range(T):
+                p = p0 + tq
+                want = [q for q in range(0, p + 1) if p - q < W]
+                got = [band_pos[r] for r in O.swa_band_rows(p0, tq, W)]
+                assert got == want, (W, p0, tq, got, want)
