@@ -298,8 +298,12 @@ def step(st, ev=None, ev_attn=None, i=0):
             K.index_reindex(c, ins[1]["q_idx"], ins[1]["w"], wl.idx_heads, 1, None, st["pool"],
                             st["pool_cnt"], st["re_ids"], nr, k, st["idx"][0], st["cnt"][0], ws)
             launches += 2
+        if ev_attn is not None:
+            K.set_launch_events(K.KERNEL_ATTENTION, ev_attn[0], ev_attn[1])
         K.attn_decode(c, ins[2]["q"].view(st["q_dtype"]), wl.heads, st["idx"][0].view(B, k),
                       st["cnt"][0].view(B), k, ins[2]["swa"], None, wl.window, 0.0, st["out"][0], ws)
+        if ev_attn is not None:
+            K.set_launch_events(K.KERNEL_ATTENTION)
         launches += st["attn_launches"]
     return launches
 
@@ -409,102 +413,205 @@ def cpu_baseline(wl, samples=4, budget_s=20.0):
             "seconds_per_sequence": per_seq}
 
 
-def oracle_pieces(wl, b, n, m, layer=0):
-    """One sequence of a Full layer-step on the oracle, cut into m + 1 timed
-    pieces whose sum is the whole step: pieces 0..m-1 score a contiguous
-    slice of the n positions each (the indexer score of a position depends
-    on that position's key alone), piece m appends the new row, selects from
-    the full score row and attends.  Inputs, and the score row piece m
-    selects from, are prepared untimed."""
+def _score_fn(wl, inp, ik, tq=0):
+    """Oracle indexer scores of query row tq against key positions [lo, hi)."""
+    from oracle import csa2 as O
+
+    def score(lo, hi):
+        if wl.idx_format == "mxfp4":
+            q = O.e4m3_decode(inp["q_idx"][tq]).reshape(wl.idx_heads, -1)
+            return O.indexer_scores_values(q, inp["w"][tq], O.dequantize_mxfp4(
+                ik[0][lo:hi], ik[1][lo:hi], wl.idx_dim))
+        return O.indexer_scores(inp["q_idx"][tq], inp["w"][tq], ik[lo:hi])
+    return score
+
+
+def _slices(score, n, per_step_s):
+    """Cut the scoring of n positions into slices of about per_step_s each."""
+    probe_n = min(n, 8192)
+    t0 = time.perf_counter()
+    score(0, probe_n)
+    per_pos = (time.perf_counter() - t0) / max(1, probe_n)
+    m = max(1, min(256, math.ceil(per_pos * n / per_step_s)))
+    cuts = [n * j // m for j in range(m + 1)]
+    return [(lambda lo=cuts[j], hi=cuts[j + 1]: score(lo, hi)) for j in range(m)]
+
+
+def oracle_plan(wl, per_step_s):
+    """One layer-step of workload `wl` on the oracle, as bounded pieces.
+
+    Returns (pieces, layers, text): pieces is a list of (callable, weight),
+    and one step of the workload takes sum(weight * time of the piece).  A
+    Full scan is cut into slices of positions (a position's score depends
+    on its own key only), each about per_step_s of CPU time; the rest of a
+    sequence's work (append, selection, dequantisation, attention) is one
+    piece.  Sequences of one kind are represented by one of them, weighted
+    by their number (or, for Full scans of ragged lengths, by their summed
+    length).  Inputs are prepared outside the pieces."""
     import numpy as np
     import synth
     from oracle import csa2 as O
     from oracle.formats import bf16_bits_to_f64
     from oracle.workload import SeqRef
-    from synth.host import host_rows_normal
-    ref = SeqRef(wl, b, n=n)
-    ik = ref.idxk_all(n)
-    inp = ref.inputs(layer)
-    newrow = host_rows_normal(wl.seed, synth.T_KV, b, [n], wl.dim, ref.mult)
-    q64 = bf16_bits_to_f64(inp["q_bf16"][0])
-    swa = O.swa_rows_decode(inp["swa"][: wl.window])
-    cuts = [n * j // m for j in range(m + 1)]
+    from synth.host import host_rows_normal, supplied_pool, supplied_prior
+    from synth.workloads import FULL, REINDEX, REUSE
+    B, k = wl.batch, wl.topk
 
-    def score(lo, hi):
-        if wl.idx_format == "mxfp4":
-            q = O.e4m3_decode(inp["q_idx"][0]).reshape(wl.idx_heads, -1)
-            return O.indexer_scores_values(q, inp["w"][0], O.dequantize_mxfp4(
-                ik[0][lo:hi], ik[1][lo:hi], wl.idx_dim))
-        return O.indexer_scores(inp["q_idx"][0], inp["w"][0], ik[lo:hi])
+    if wl.name.startswith("model-"):
+        run = model_oracle_sample(wl, 0, wl.lengths[0])
+        return [(run, B)], 38, (f"sequence 0's 38 CSA2 layers of one decode token (4 Full and 4 "
+                                f"Reindex scans, selections, 38 attentions), weight {B}")
 
-    s_full = np.concatenate([score(cuts[j], cuts[j + 1]) for j in range(m)])
+    def decode_parts(b, n, layer):
+        ref = SeqRef(wl, b, n=n)
+        ik = ref.idxk_all(n)
+        inp = ref.inputs(layer)
+        score = _score_fn(wl, inp, ik)
+        s_full = score(0, n)
+        newrow = host_rows_normal(wl.seed, synth.T_KV, b, [n], wl.dim, ref.mult)
+        q64 = bf16_bits_to_f64(inp["q_bf16"][0])
+        swa = O.swa_rows_decode(inp["swa"][: wl.window])
 
-    def tail():
-        O.quant_append_rows(newrow, np.array([n]), ref.cos, ref.sin, wl.rope_dim)
-        idx, pool = O.full_select(s_full, wl.topk)
-        xh = ref.dequant_rows(idx)
-        return O.sparse_attention(q64, np.concatenate([xh, swa]))
+        def tail():
+            O.quant_append_rows(newrow, np.array([n]), ref.cos, ref.sin, wl.rope_dim)
+            idx, pool = O.full_select(s_full, k)
+            return O.sparse_attention(q64, np.concatenate([ref.dequant_rows(idx), swa]))
+        return ref, score, s_full, tail
 
-    return [(lambda j=j: score(cuts[j], cuts[j + 1])) for j in range(m)] + [tail]
+    def attend(ref, layer, idx, tq=0, tq_total=1):
+        return lambda: ref.attention(layer, idx, tq=tq, tq_total=tq_total)
+
+    if wl.prefill_tokens:
+        # one query row of the chunk stands for all T: its scan slices are
+        # weighted by the chunk's summed visible length over its own, its
+        # selection + attention by T; the chunk's append is one more piece
+        T = wl.prefill_tokens
+        n0 = wl.lengths[0]
+        tm = T // 2
+        ref = SeqRef(wl, 0, n=n0 + T)
+        ref.n_prior_positions = n0
+        ik = ref.idxk_all(n0 + T)
+        inp = ref.inputs(0, T)
+        vis = n0 + tm + 1
+        score = _score_fn(wl, inp, ik, tm)
+        s_full = score(0, vis)
+        rows = host_rows_normal(wl.seed, synth.T_KV, 0, np.arange(n0, n0 + T), wl.dim, ref.mult)
+        total_vis = sum(n * T + T * (T + 1) // 2 for n in wl.lengths)
+        pieces = [(f, total_vis / vis) for f in _slices(score, vis, per_step_s)]
+
+        def tail():
+            idx, pool = O.full_select(s_full, k)
+            return ref.attention(0, idx, tq=tm, tq_total=T)
+        pieces.append((tail, B * T))
+        pieces.append((lambda: O.quant_append_rows(rows, np.arange(n0, n0 + T), ref.cos, ref.sin,
+                                                   wl.rope_dim), B))
+        return pieces, len(wl.layers), (
+            f"query row {tm} of the {T}-token chunk: its scan of {vis} positions in "
+            f"{len(pieces) - 2} slices weighted by the chunk's summed visible length, its "
+            f"selection + attention weighted by {B * T}; the chunk's append as one piece"
+            + ("; Reindex layers are not timed" if len(wl.layers) > 1 else ""))
+
+    if wl.modes is None:
+        n = wl.lengths[0]
+        ref, score, s_full, tail = decode_parts(0, n, 0)
+        pieces = [(f, B) for f in _slices(score, n, per_step_s)] + [(tail, B)]
+        text = (f"sequence 0 of {B}: its Full scan of {n} positions in {len(pieces) - 1} slices, "
+                f"then append + select + dequantise + attend; each piece weighted by {B}")
+        if len(wl.layers) > 1:   # the group: Reindex over the Full layer's pool, then Reuse
+            idx, pool = O.full_select(s_full, k)
+            _, _, r_idx = ref.reindex(1, pool, k)
+
+            def reindex():
+                _, _, ri = ref.reindex(1, pool, k)
+                return ref.attention(1, ri)
+            pieces += [(reindex, B), (attend(ref, 2, r_idx), B)]
+            text += "; its Reindex (score the pool, select, attend) and Reuse (attend), weight " \
+                    f"{B} each"
+        return pieces, len(wl.layers), text
+
+    # ragged mixed modes: one sequence per mode stands for all of its mode
+    lens, modes = wl.lengths, wl.modes
+    full = [b for b in range(B) if modes[b] == FULL]
+    rei = [b for b in range(B) if modes[b] == REINDEX]
+    reu = [b for b in range(B) if modes[b] == REUSE]
+    pieces, parts = [], []
+    if full:
+        mean = sum(lens[b] for b in full) / len(full)
+        bf = min(full, key=lambda b: abs(lens[b] - mean))
+        ref, score, s_full, tail = decode_parts(bf, lens[bf], 0)
+        w = sum(lens[b] for b in full) / lens[bf]
+        sl = _slices(score, lens[bf], per_step_s)
+        pieces += [(f, w) for f in sl] + [(tail, len(full))]
+        parts.append(f"Full: sequence {bf} ({lens[bf]} positions) scanned in {len(sl)} slices "
+                     f"weighted by the Full sequences' summed length over its own, its tail "
+                     f"weighted by {len(full)}")
+    if rei:
+        br = rei[0]
+        ref = SeqRef(wl, br)
+        pool = supplied_pool(wl, br, lens[br])
+
+        def reindex():
+            _, _, ri = ref.reindex(1, pool, k)
+            return ref.attention(2, ri)
+        pieces.append((reindex, len(rei)))
+        parts.append(f"Reindex: sequence {br} (score its pool, select, attend), weight {len(rei)}")
+    if reu:
+        bu = reu[0]
+        ref = SeqRef(wl, bu)
+        pieces.append((attend(ref, 2, supplied_prior(wl, bu, lens[bu])), len(reu)))
+        parts.append(f"Reuse: sequence {bu} (attend), weight {len(reu)}")
+    return pieces, 1, "; ".join(parts)
 
 
 def reference_arm(args, budget_s=90.0):
-    """The oracle on the host cores.  Step i runs piece i mod (m + 1) of one
-    sequence's Full layer-step (oracle_pieces), with m chosen so that the
-    warm-up and timed steps together take about budget_s whatever --steps
-    is; one sequence's time is the sum over the pieces of each piece's mean
-    time."""
+    """The oracle on the host cores.  Step i runs piece i mod P of the
+    workload's layer-step (oracle_plan), with the pieces sized so that the
+    warm-up and timed steps together take about budget_s whatever --steps is.
+    `value` is layer-steps/s from each piece's mean time and weight;
+    `ms_per_step` is the measured wall time of one timed step (one piece)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    from synth.workloads import FULL, get_workload
+    from synth.workloads import get_workload
     wl = get_workload(args.workload)
-    if wl.prefill_tokens or wl.layers != [FULL] or wl.modes is not None or wl.compress != 1:
-        print(json.dumps({"impl": "reference", "unavailable":
-                          f"the oracle arm times single Full-layer decode workloads; "
-                          f"{wl.name} is not one"}), flush=True)
-        return
-    n = wl.lengths[0]
-    probe = oracle_pieces(wl, 0, min(n, 8192), 1)
-    t0 = time.perf_counter()
-    probe[0]()
-    per_pos = (time.perf_counter() - t0) / min(n, 8192)
     per_step = budget_s / max(1, args.steps + args.warmup)
-    m = max(1, min(256, math.ceil(per_pos * n / per_step)))
-    pieces = oracle_pieces(wl, 0, n, m)
+    pieces, layers, text = oracle_plan(wl, per_step)
     for i in range(args.warmup):
-        pieces[i % len(pieces)]()
+        pieces[i % len(pieces)][0]()
     times = [[] for _ in pieces]
     t_all = time.perf_counter()
     for i in range(args.steps):
         j = i % len(pieces)
         t0 = time.perf_counter()
-        pieces[j]()
+        pieces[j][0]()
         times[j].append(time.perf_counter() - t0)
     dt = time.perf_counter() - t_all
     missing = [j for j, t in enumerate(times) if not t]
     for j in missing:  # fewer steps than pieces: time the rest once, outside the step count
         t0 = time.perf_counter()
-        pieces[j]()
+        pieces[j][0]()
         times[j].append(time.perf_counter() - t0)
-    per_seq = sum(statistics.mean(t) for t in times)
-    value = 1.0 / (per_seq * wl.batch)
-    sample = (f"step i = piece i mod {m + 1} of one sequence's Full layer-step ({m} slices of "
-              f"{n} positions scored, then append + select + dequantise + attend); one "
-              f"sequence = the sum of the pieces' mean times, scaled by 1/{wl.batch} for the "
-              f"{wl.batch}-sequence layer-step; numpy fp64 with the host BLAS threads")
+    step_s = sum(w * statistics.mean(t) for (_, w), t in zip(pieces, times))
+    value = layers / step_s
+    sample = (f"step i = piece i mod {len(pieces)} of one layer-step: {text}; numpy fp64 with "
+              f"the host BLAS threads")
     cpu = {"value": value, "unit": "layer-steps/s", "cores": os.cpu_count(), "kind": "oracle",
            "sample": sample}
     line = {"impl": "reference",
-            "metric": "CSA2 decode layer-steps/s (achieved HBM GB/s vs GB300 peak in roofline)",
+            "metric": ("CSA2 decode layer-steps/s (achieved HBM GB/s vs GB300 peak in roofline)"
+                       if not wl.prefill_tokens else
+                       f"CSA2 multi-query layer-steps/s ({wl.prefill_tokens} tokens per sequence "
+                       f"per step)"),
             "value": value, "unit": "layer-steps/s", "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": per_seq * wl.batch * 1e3,
+            "warmup": args.warmup, "ms_per_step": dt / max(1, args.steps) * 1e3,
+            "layer_step_ms_estimated": step_s / layers * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": wl.name, "batch": wl.batch, "ctx": max(wl.lengths),
                        "topk": wl.topk, "window": wl.window, "dim": wl.dim,
                        "idx_heads": wl.idx_heads, "heads": wl.heads, "parallelism": "single",
-                       "launch": "host oracle", "tokens_per_step": wl.batch},
+                       "launch": "host oracle",
+                       "tokens_per_step": wl.batch * max(1, wl.prefill_tokens)},
             "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": "layer-steps/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
@@ -581,7 +688,8 @@ def model_bench(args):
             K.reset_status(w)
         torch.cuda.synchronize()
 
-    every = max(1, min(EVENT_EVERY, args.steps))
+    # kernel events in a second replay of the timed steps, >= 8 per kernel
+    every = max(1, min(EVENT_EVERY, args.steps // 8))
     sampled = lambda i: i % every == every // 2
     watch = {(20, "index"): K.KERNEL_INDEXER, (2, "index"): K.KERNEL_INDEXER,
              (24, "index"): K.KERNEL_INDEXER, (21, "attention"): K.KERNEL_ATTENTION}
@@ -618,11 +726,16 @@ def model_bench(args):
     reset()
     run_steps(args.warmup)
     reset()
-    graph = None
+    graph = graph_ev = None
     if not args.eager:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, capture_error_mode="thread_local"):
-            launches = run_steps(args.steps, True)
+            launches = run_steps(args.steps)
+        graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ev, capture_error_mode="thread_local"):
+            run_steps(args.steps, True)
+        reset()
+        graph_ev.replay()
         reset()
         graph.replay()
         torch.cuda.synchronize()
@@ -638,13 +751,20 @@ def model_bench(args):
     if graph is not None:
         graph.replay()
     else:
-        launches = run_steps(args.steps, True)
+        launches = run_steps(args.steps)
     t1.record()
     torch.cuda.synchronize()
     time.sleep(0.1)
     clk = clocks.stop()
     ms = max_over_ranks(t0.elapsed_time(t1), world)
     status = [K.get_status(w) for w in m.workspaces]
+    reset()                           # the kernel-timing replay of the same steps
+    if graph_ev is not None:
+        graph_ev.replay()
+    else:
+        run_steps(args.steps, True)
+    torch.cuda.synchronize()
+    status = [s0 | K.get_status(w) for s0, w in zip(status, m.workspaces)]
     us = {f"{l}:{ph}": statistics.mean(a.elapsed_time(b) for a, b in evs[(l, ph)][:n_ev]) * 1e3
           for (l, ph) in watch}
     value = job_throughput(layers_per * args.steps, world, ms)
@@ -664,8 +784,9 @@ def model_bench(args):
                 "flops_per_launch": attn_flops, "launch_us": attn_us,
                 "share_of_step": 38 * attn_us / (ms / args.steps * 1e3),
                 "timed_launches": n_ev,
-                "sampling": f"CUDA events on every {every}th timed step (layer 21's attention)"}
-    del graph
+                "sampling": f"CUDA events around layer 21's attention of every {every}th step, in "
+                            f"a second replay of the {args.steps} timed steps"}
+    del graph, graph_ev
 
     # ---- e2e through the API: per step the appended rows and every layer's
     # query-side inputs are copied from pinned host memory, and the last
@@ -860,10 +981,13 @@ def main():
         torch.cuda.synchronize()
 
     # ---- device-resident timed loop
-    # The indexer and attention launches of every EVENT_EVERY-th timed step
-    # are bracketed by CUDA events (each event record costs a few us of GPU
-    # time, so they are sampled rather than put on every step).
-    every = max(1, min(EVENT_EVERY, args.steps))
+    # `value` comes from the K timed steps with nothing else in them.  The
+    # per-kernel times come from a second replay of the same K steps in which
+    # the indexer and attention launches of every `every`-th step are
+    # bracketed by CUDA events (an event node between two kernels costs GPU
+    # time and stops the next launch from overlapping the previous kernel's
+    # tail), at least 8 launches of each whatever K is.
+    every = max(1, min(EVENT_EVERY, args.steps // 8))
 
     def sampled(i):
         return i % every == every // 2
@@ -889,15 +1013,21 @@ def main():
         a.record()
         b.record()
     torch.cuda.synchronize()
-    graph = None
+    graph = graph_ev = None
     if not args.eager:
-        # The K timed steps, unrolled into one CUDA graph; the sampled kernel
-        # events are external records, i.e. event nodes timed on every replay.
+        # The K timed steps, unrolled into one CUDA graph; a second graph of
+        # the same steps carries the sampled kernel events (external records,
+        # i.e. event nodes timed on every replay).
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, capture_error_mode="thread_local"):
-            launches = run_steps(args.steps, ev, eva)
+            launches = run_steps(args.steps)
+        graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ev, capture_error_mode="thread_local"):
+            run_steps(args.steps, ev, eva)
         reset()
-        graph.replay()                # warm-up replay (untimed)
+        graph_ev.replay()             # warm-up replays (untimed)
+        reset()
+        graph.replay()
         torch.cuda.synchronize()
         reset()
     t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -911,7 +1041,7 @@ def main():
     if graph is not None:
         graph.replay()
     else:
-        launches = run_steps(args.steps, ev, eva)
+        launches = run_steps(args.steps)
     t_end.record()
     torch.cuda.synchronize()
     time.sleep(0.1)
@@ -919,6 +1049,14 @@ def main():
     ms = t_begin.elapsed_time(t_end)
     ms = max_over_ranks(ms, world)
     status = K.get_status(st["dw"].ws)
+    # the kernel-timing replay of the same steps
+    reset()
+    if graph_ev is not None:
+        graph_ev.replay()
+    else:
+        run_steps(args.steps, ev, eva)
+    torch.cuda.synchronize()
+    status |= K.get_status(st["dw"].ws)
     idx_ms = [a.elapsed_time(b) for a, b in ev[:n_ev]]
     attn_ms = [a.elapsed_time(b) for a, b in eva[:n_ev]]
     # bytes of the sampled indexer launches (visible length grows by T per step)
@@ -955,11 +1093,12 @@ def main():
                     "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
                     "peak_source": peak_kind, "bytes_per_launch": statistics.mean(idx_bytes)}
     roofline.update({"launch_us": statistics.mean(idx_ms) * 1e3, "timed_launches": len(idx_ms),
-                     "sampling": f"CUDA events on every {every}th timed step"})
+                     "sampling": f"CUDA events around the launches of every {every}th step, in a "
+                                 f"second replay of the {args.steps} timed steps"})
     ms_step = ms / args.steps
     value = job_throughput(layers_per_step(wl) * args.steps, world, ms)
     path_gbs = sum(roof_bytes) / (ms * 1e-3) / 1e9
-    del graph
+    del graph, graph_ev
 
     # ---- end-to-end through the C ABI with host buffers.  Every step copies
     # its inputs from pinned host memory and reads its attention output back.

@@ -16,52 +16,81 @@
 // softmax weights are rounded to f16 before the P.V product and the same
 // rounded weights are summed for the normaliser.
 //
-// One CTA handles a contiguous range of 64-key chunks of one query row
-// (split-K over chunks).  The split CTAs of a row form one thread-block
-// cluster: each stages its unnormalised output and its per-head running
-// maximum and sum in shared memory, and after a cluster barrier every CTA
-// merges a slice of the channels from all of them through distributed
-// shared memory and writes the output.
-// Nine warps, three roles:
-//   data warps 4-7     gather each key's code and scale bytes (or window row)
-//                      with plain vector loads one chunk ahead (index
-//                      entries and page lookups two and three chunks ahead),
-//                      dequantise into f16 slabs [64 keys x 64 channels]
-//                      (128-byte rows, 128-byte swizzle; the X tile is double
-//                      buffered), rescale the output accumulator when the
-//                      running maximum jumps, and run the epilogue;
-//   softmax warps 0-3  one thread per head (lanes 0-15 of each warp, the
-//                      tensor-memory lanes an M=64 accumulator occupies):
-//                      running maximum, rescale decision, softmax weights P
-//                      (f16) for each chunk;
-//   MMA warp 8         S[heads x keys] = Q . X^T (M=64, N=64, K=16), double
-//                      buffered in tensor memory so that QK of chunk c+1 runs
-//                      while chunk c's softmax does;  O^T[d x heads] +=
-//                      X^T . P^T (M=128 channel tiles; A is the same slabs
-//                      read channel-major, N = 64 heads).
+// Work split.  The keys of one query row (its selected entries, then its
+// window rows) are cut into `splits` contiguous shares, one CTA each; the
+// CTAs of a row form one thread-block cluster and merge their partial
+// outputs through distributed shared memory at the end.  A CTA walks its
+// share in tiles of up to 112 keys, all of them resident at once:
+//
+//   S^T[keys x heads] = X . Q^T      tcgen05.mma M = 128 (the tile's keys;
+//                                    rows 112-127 are not used), N = 64
+//                                    heads, K = D in steps of 16;
+//   O^T[D x heads]  += X^T . P^T     M = 128 channels per accumulator tile,
+//                                    N = 64 heads, K = the tile's keys.
+//
+// With the keys as M the QK product runs at the M = 128 rate of the tensor
+// core (64 heads as M would run at the M = 64 rate), and each softmax thread
+// owns one key, so it writes its row of P^T (the PV product's B operand,
+// heads contiguous) without any exchange.  Tiles of 112 keys (not 128) make
+// X (126 KB), Q (72 KB) and P^T (14 KB) fit in shared memory together.
+//
+// Warps (320 threads):
+//   0-7  compute: dequantise tile i+1 into the X slabs while the tensor core
+//        runs PV of tile i (slab pair by slab pair, as each PV accumulator
+//        tile finishes with it), then the softmax of tile i+1 once its QK
+//        product lands: thread (key j = 32 (warp % 4) + lane, heads
+//        32 (warp / 4) .. +32).  The running maximum per head is raised
+//        lazily: only when a logit exceeds it by more than 2^8 (then O^T
+//        and the sums are rescaled in place); the raw bytes of the next
+//        tile's keys are loaded into registers one tile ahead.
+//   8    MMA issuer (lane 0) and tensor-memory owner.
+//   9    index warp: turns the tile's index entries into cache rows (page
+//        table, bounds checks) up to four tiles ahead, and copies the query
+//        rows in.
 #include "codec.cuh"
 #include "launch.h"
 
 namespace csa2 {
 
+constexpr int kTile = 112;          // keys per tile
+constexpr int kAttnThreads = 320;
+constexpr int kComputeThreads = 256;
+constexpr int kKtSlots = 4;         // key-table ring (tiles resolved ahead)
+
 template <int NSLAB>
 struct AttnCfg {
   static constexpr int D = NSLAB * 64;
-  static constexpr int NT = (NSLAB + 1) / 2;     // O^T tiles of 128 channels
-  static constexpr int kKeys = 64;
-  static constexpr int kSlab = 64 * 128;         // one [64 x 64] f16 slab
-  static constexpr int kXBytes = NSLAB * kSlab;  // one X tile (64 keys x D)
-  static constexpr int kQOff = 0;
-  static constexpr int kXOff = kXBytes;          // two X tiles follow Q
-  static constexpr int kPOff = 3 * kXBytes;
-  static constexpr int kMiscOff = kPOff + kSlab;
-  static constexpr int kMiscBytes = 2048;
+  static constexpr int NT = (NSLAB + 1) / 2;     // O^T accumulator tiles of 128 channels
+  static constexpr int kXSlab = kTile * 128;     // [112 keys x 64 channels] f16, 128-byte rows
+  static constexpr int kQSlab = 64 * 128;        // [64 heads x 64 channels] f16
+  static constexpr int kXOff = 0;
+  // Q directly after X: QK reads 128 rows of each X slab, and rows 112-127
+  // of the last slab fall on Q (finite values; those S^T rows are unused)
+  static constexpr int kQOff = NSLAB * kXSlab;
+  static constexpr int kPOff = kQOff + NSLAB * kQSlab;
+  static constexpr int kMiscOff = kPOff + kTile * 128;
+  // misc area (byte offsets)
+  static constexpr int kBars = 0;                // 32 mbarriers
+  static constexpr int kFlags = 256;             // abort flag, tensor-memory address
+  static constexpr int kQmul = 512;              // f32 [64] logit factor per head (log2 domain)
+  static constexpr int kMrow = 768;              // f32 [64] running maximum per head
+  static constexpr int kLrow = 1024;             // f32 [64] softmax denominator per head
+  static constexpr int kFw = 1280;               // f32 [64] merge factor per head
+  static constexpr int kLsum = 1536;             // f32 [4][64] per-quadrant partial sums
+  static constexpr int kTmax = 2560;             // f32 [4][64] per-quadrant tile maxima
+  static constexpr int kKtab = 3584;             // int32 [kKtSlots][kTile] key table
+  static constexpr int kMiscBytes = kKtab + kKtSlots * kTile * 4;
   static constexpr int kSmem = kMiscOff + kMiscBytes;
-  static_assert(2 * kXBytes >= 64 * D * 4, "the X tiles hold the merge stage");
-  static constexpr int kSCols = 2 * 64;          // two S buffers
-  static constexpr int kCols = kSCols + 64 * NT;
-  static constexpr int kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
-  static constexpr int kPerThread = (NSLAB + 1) / 2;  // slabs per data thread
+  static constexpr int kItems = (kTile * NSLAB + kComputeThreads - 1) / kComputeThreads;
+  // tensor memory: S^T x2 (128 columns), O^T (64 NT), the softmax sums (64)
+  static constexpr int kLCol = 128 + 64 * NT;
+  static constexpr int kTmemCols = kLCol + 64 <= 256 ? 256 : 512;
+  static_assert(kLCol + 64 <= 512, "tensor memory columns");
+  static_assert(kSmem <= 227 * 1024, "attention: shared memory");
+  static_assert((kXSlab % 1024) == 0 && (kQOff % 1024) == 0 && (kPOff % 1024) == 0,
+                "128-byte swizzle atoms need 1024-byte aligned slabs");
+  static_assert(NSLAB * kXSlab >= 64 * D * 2, "the X slabs hold the staged bf16 query");
+  static_assert(6 + 2 * NT + 2 * kKtSlots <= 32, "mbarrier area");
 };
 
 struct AttnParams {
@@ -119,7 +148,29 @@ __device__ __forceinline__ RowKeys row_keys(const AttnParams& p, int row, int D)
   return r;
 }
 
-constexpr int kLrowOff = 128 + 2 * 64 * 4;  // lrow's byte offset in the misc area
+// This CTA's share of the row's keys: selected entries [g0, g0+ng) of the
+// index list and window rows [w0, w0+nw); local key l < ng is entry g0 + l,
+// else window row w0 + l - ng.  Tiles hold ts keys (a multiple of 16, at most
+// kTile), the last one the remainder (never empty).
+struct CtaKeys {
+  int g0, ng, w0, nw, n, ntile, ts;
+  __device__ __forceinline__ int tile_keys(int i) const {
+    const int r = n - i * ts;
+    return r < ts ? r : ts;
+  }
+};
+
+__device__ __forceinline__ CtaKeys cta_keys(const RowKeys& rk, int split, int splits) {
+  CtaKeys k;
+  k.g0 = (int)((int64_t)rk.n_global * split / splits);
+  k.ng = (int)((int64_t)rk.n_global * (split + 1) / splits) - k.g0;
+  k.w0 = (int)((int64_t)rk.n_swa * split / splits);
+  k.nw = (int)((int64_t)rk.n_swa * (split + 1) / splits) - k.w0;
+  k.n = k.ng + k.nw;
+  k.ntile = (k.n + kTile - 1) / kTile;
+  k.ts = k.ntile ? ((k.n + k.ntile - 1) / k.ntile + 15) / 16 * 16 : 0;
+  return k;
+}
 
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -134,11 +185,76 @@ __device__ __forceinline__ bool named_sync_or(int id, int n, bool pred) {
       : "memory");
   return r != 0;
 }
+// Largest value over the 32 lanes of the warp.
+__device__ __forceinline__ float warp_max(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22; the
+// weights are rounded to f16 afterwards).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 16-byte store of f16x8 into row `row` (128-byte rows, 128-byte swizzle) of
+// a slab at chunk position c (0..7).
+__device__ __forceinline__ void st_swz(uint8_t* slab, int row, int c, uint4 v) {
+  *reinterpret_cast<uint4*>(slab + row * 128 + ((c ^ (row & 7)) << 4)) = v;
+}
+
+// 32 tensor-memory lanes x 32 consecutive 32-bit columns: lane i of the warp
+// reads TMEM lane (base lane + i).  Valid after tmem_ld_wait().
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16z(uint32_t taddr) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,"
+      "%1,%1};" ::"r"(taddr), "r"(0u)
+      : "memory");
+}
+__device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(const void* p, int rank) {
+  uint32_t r;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
 
 // f16 copy of the query rows [heads x D] (bf16, at qs) into the swizzled Q
-// slabs, by all 288 threads of the CTA (thread t of n), assuming no head needs
-// scaling; returns, over the CTA, whether some |q| >= 2^14 (then the data
-// warps redo the copy with a power-of-two scale per head).  Rows past `heads`
+// slabs by the compute threads (thread t of 256), assuming no head needs
+// scaling; returns, over the compute warps, whether some |q| >= 2^14 (then
+// the copy is redone with a power-of-two scale per head).  Rows past `heads`
 // are zero.
 template <int NSLAB>
 __device__ __forceinline__ bool convert_query(const uint8_t* qs, uint8_t* sq, int t, bool ok,
@@ -146,8 +262,8 @@ __device__ __forceinline__ bool convert_query(const uint8_t* qs, uint8_t* sq, in
   constexpr int D = NSLAB * 64;
   constexpr int kChunks = D / 8;     // 16-byte chunks per head row
   constexpr int kAll = 64 * kChunks;
-  constexpr int kSlab = 64 * 128;
-  constexpr int n = 288;
+  constexpr int kQSlab = 64 * 128;
+  constexpr int n = kComputeThreads;
   bool big = false;
   for (int i0 = t; i0 < kAll; i0 += 4 * n) {
     uint4 v[4];
@@ -171,210 +287,48 @@ __device__ __forceinline__ bool convert_query(const uint8_t* qs, uint8_t* sq, in
                                        __uint_as_float(w4[q] & 0xFFFF0000u));
         r[q] = *reinterpret_cast<uint32_t*>(&h2);
       }
-      *reinterpret_cast<uint4*>(sq + (c >> 3) * kSlab + h * 128 + (((c & 7) ^ (h & 7)) << 4)) =
+      *reinterpret_cast<uint4*>(sq + (c >> 3) * kQSlab + h * 128 + (((c & 7) ^ (h & 7)) << 4)) =
           make_uint4(r[0], r[1], r[2], r[3]);
     }
   }
-  return named_sync_or(4, 288, big);
+  return named_sync_or(1, kComputeThreads, big);
 }
 
-// 2^x with the hardware approximation (relative error about 2^-22; the
-// weights are rounded to f16 afterwards).
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// 16-byte store of f16x8 into row `row` (128-byte rows, 128-byte swizzle) of
-// a slab at chunk position c (0..7).
-__device__ __forceinline__ void st_swz(uint8_t* slab, int row, int c, uint4 v) {
-  *reinterpret_cast<uint4*>(slab + row * 128 + ((c ^ (row & 7)) << 4)) = v;
-}
-
-// 4-byte store at byte `b` (a multiple of 4) of 16-byte column c of a
-// swizzled slab row.
-__device__ __forceinline__ void st_swz4(uint8_t* slab, int row, int c, int b, uint32_t v) {
-  *reinterpret_cast<uint32_t*>(slab + row * 128 + ((c ^ (row & 7)) << 4) + b) = v;
-}
-
-// 16 tensor-memory lanes x 64 columns (16x256b shape, 8 repeats): thread t
-// gets lanes t/4 (registers 4k, 4k+1) and t/4 + 8 (registers 4k+2, 4k+3),
-// columns 8k + 2(t%4) and 8k + 2(t%4) + 1.
-__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-
-// Where one key's bytes live: kind 0 = absent, 1 = FP4 cache row, 2 = FP8
-// window row.
-struct KeySrc {
-  const uint8_t* a;  // codes row, or window row
-  const uint8_t* s;  // scales row
-  int kind;
+// Raw bytes of one (key, 64-channel slab) item: FP4 codes (32 B in a, b) and
+// the slab's four scale bytes (c.x), or an FP8 window row's 64 bytes.
+struct RawItem {
+  uint4 a, b, c, d;
 };
 
-// Raw bytes of one FP4 key for this thread's slabs: 32 code bytes and 4
-// scale bytes per slab.  Window keys are read when they are dequantised.
-template <int NP>
-struct RawKey {
-  uint4 c0[NP], c1[NP];
-  uint32_t sc[NP];
-};
-
-// O^T *= alpha (per head column), all 128 lanes of the four data warps.
-template <int NT>
-__device__ __forceinline__ void rescale_output(uint32_t tO, int quad, const float* alpha) {
-  tc_fence_after();
-#pragma unroll 1
-  for (int t = 0; t < NT; ++t) {
-    const uint32_t base = tO + 64 * t + ((uint32_t)(32 * quad) << 16);
-#pragma unroll
-    for (int c = 0; c < 64; c += 16) {
-      uint32_t v[16];
-      tmem_ld16(base + c, v);
-      tmem_ld_wait();
-      reg_fence(v);
-#pragma unroll
-      for (int u = 0; u < 16; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) * alpha[c + u]);
-      tmem_st16(base + c, v);
-    }
-  }
-  tmem_st_wait();
-  tc_fence_before();
-}
-
-// Split-K merge over the cluster of a query row:
-//   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s   per head,
-// M the largest m_s with l_s > 0.  Every CTA has staged its unnormalised
-// output [64][D] fp32 over its X tiles and its per-head (m, l); this CTA
-// writes the channels [D*r/C, D*(r+1)/C) (in float4 columns).  Kept out of
-// line so that nothing of it is live in the main loops.
 template <int NSLAB>
-__device__ __noinline__ void merge_splits(const AttnParams& p) {
-  using C_ = AttnCfg<NSLAB>;
-  constexpr int D = C_::D;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const float* st = reinterpret_cast<const float*>(smem + C_::kXOff);
-  float* wgt = reinterpret_cast<float*>(smem + C_::kPOff);  // [kMaxSplits][64] merge weights
-  float* inv_den = wgt + kMaxSplits * 64;                  // [64]
-  const float* lrow = reinterpret_cast<const float*>(smem + C_::kMiscOff + kLrowOff);
-  const float* mrow = lrow + 64;
-  const int tid = threadIdx.x, row = blockIdx.y, r = blockIdx.x, C = p.splits;
-  cluster_sync();  // every CTA's stage, mrow and lrow are written
-  if (tid < 64) {
-    float m[kMaxSplits], l[kMaxSplits];
-    float M = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < kMaxSplits; ++u) {
-      m[u] = -INFINITY;
-      l[u] = 0.0f;
-      if (u < C) {
-        m[u] = peer_f32(&mrow[tid], u);
-        l[u] = peer_f32(&lrow[tid], u);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kMaxSplits; ++u)
-      if (l[u] > 0.0f) M = fmaxf(M, m[u]);
-    float den = 0.0f;
-#pragma unroll
-    for (int u = 0; u < kMaxSplits; ++u) {
-      const float w = l[u] > 0.0f ? exp2f(m[u] - M) : 0.0f;
-      wgt[u * 64 + tid] = w;
-      den += w * l[u];
-    }
-    inv_den[tid] = den > 0.0f ? 1.0f / den : 0.0f;
-  }
-  __syncthreads();
-  constexpr int n4 = D / 4;
-  const int q0 = n4 * r / C, q1 = n4 * (r + 1) / C, nq = q1 - q0;
-  const int items = p.heads * nq;
-  // four outputs per thread at a time, each reading the C stages: up to 16
-  // remote float4 loads in flight
-#pragma unroll 1
-  for (int i0 = tid; i0 < items; i0 += 4 * blockDim.x) {
-#pragma unroll 1
-    for (int u0 = 0; u0 < C; u0 += 4) {
-      float4 v[4][4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const int i = i0 + a * blockDim.x;
-        const int hh = i / nq, d = 4 * (q0 + i - hh * nq);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (i >= items || u0 + j >= C) continue;
-          if (u0 + j == r)  // this CTA's own stage: a plain shared-memory load
-            v[a][j] = *reinterpret_cast<const float4*>(st + hh * D + d);
-          else
-            v[a][j] = peer_f32x4(st + hh * D + d, u0 + j);
-        }
-      }
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const int i = i0 + a * blockDim.x;
-        if (i >= items) continue;
-        const int hh = i / nq, d = 4 * (q0 + i - hh * nq);
-        float4 num = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        float4* dst = reinterpret_cast<float4*>(p.out + ((int64_t)row * p.heads + hh) * D + d);
-        if (u0 > 0) num = *dst;  // more than four splits: continue the sum
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (u0 + j < C) {
-            const float w = wgt[(u0 + j) * 64 + hh];
-            if (w != 0.0f) {
-              num.x += w * v[a][j].x;
-              num.y += w * v[a][j].y;
-              num.z += w * v[a][j].z;
-              num.w += w * v[a][j].w;
-            }
-          }
-        }
-        if (u0 + 4 >= C) {
-          const float id = inv_den[hh];
-          num = make_float4(num.x * id, num.y * id, num.z * id, num.w * id);
-        }
-        *dst = num;
-      }
-    }
-  }
-  cluster_sync();  // no CTA leaves while a peer may still read its shared memory
-}
-
-template <int NSLAB>
-__global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
+__global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p) {
   using C = AttnCfg<NSLAB>;
   constexpr int D = C::D;
-  constexpr int NP = C::kPerThread;
+  constexpr int NT = C::NT;
   extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* sx = smem + C::kXOff;
   uint8_t* sq = smem + C::kQOff;
-  uint8_t* sx = smem + C::kXOff;  // X tile b at sx + b * kXBytes
   uint8_t* sp = smem + C::kPOff;
   uint8_t* misc = smem + C::kMiscOff;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
-  uint64_t* x_full = bars + 0;    // [2] data warps -> MMA issuer (4 arrivals)
-  uint64_t* s_full = bars + 2;    // [2] QK of the chunk done
-  uint64_t* pv_done = bars + 4;   // [2] PV of the chunk done (X tile and P free)
-  uint64_t* dec = bars + 6;       // [2] softmax decision for the chunk (4 arrivals)
-  uint64_t* resc = bars + 8;      // output rescale finished (4 arrivals)
-  uint64_t* q_full = bars + 9;
-  uint64_t* drain = bars + 10;
-  uint64_t* p_full = bars + 11;   // softmax weights of the chunk written (4 arrivals)
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 96);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 100);
-  int* need_resc = reinterpret_cast<int*>(misc + 104);           // [2]
-  uint32_t* vmask = reinterpret_cast<uint32_t*>(misc + 112);     // [2][2]
-  float* qmul = reinterpret_cast<float*>(misc + 128);            // [64]
-  float* alpha = qmul + 64;                                      // [64]
-  float* lrow = alpha + 64;                                      // [64] at misc + kLrowOff
-  float* mrow = lrow + 64;                                       // [64]  (ends at misc + 1152)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc + C::kBars);
+  uint64_t* s_full = bars + 0;             // [2] QK of the tile landed (commit)
+  uint64_t* p_full = bars + 2;             // softmax weights written (8 warps)
+  uint64_t* q_full = bars + 3;             // query rows copied in (bulk copy)
+  uint64_t* q_ready = bars + 4;            // f16 query slabs written (8 warps)
+  uint64_t* drain = bars + 5;
+  uint64_t* xg = bars + 6;                 // [NT] X slab pair t of the tile written (8 warps)
+  uint64_t* pvt = bars + 6 + NT;           // [NT] PV accumulator tile t done (commit)
+  uint64_t* kt_full = bars + 6 + 2 * NT;   // [kKtSlots] key table written (index warp)
+  uint64_t* kt_empty = kt_full + kKtSlots; // [kKtSlots] key table consumed (8 warps)
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + C::kFlags);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + C::kFlags + 4);
+  float* qmul = reinterpret_cast<float*>(misc + C::kQmul);
+  float* mrow = reinterpret_cast<float*>(misc + C::kMrow);
+  float* lrow = reinterpret_cast<float*>(misc + C::kLrow);
+  float* fw = reinterpret_cast<float*>(misc + C::kFw);
+  float* lsum = reinterpret_cast<float*>(misc + C::kLsum);
+  float* tmax = reinterpret_cast<float*>(misc + C::kTmax);
+  int32_t* ktab = reinterpret_cast<int32_t*>(misc + C::kKtab);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   if ((smem_u32(smem) & 1023u) != 0) {
@@ -384,19 +338,24 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
   const int row = blockIdx.y, split = blockIdx.x;
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(x_full + i, 4);
-      mbar_init(s_full + i, 1);
-      mbar_init(pv_done + i, 1);
-      mbar_init(dec + i, 4);
-    }
-    mbar_init(resc, 4);
+    mbar_init(s_full + 0, 1);
+    mbar_init(s_full + 1, 1);
+    mbar_init(p_full, 8);
     mbar_init(q_full, 1);
+    mbar_init(q_ready, 8);
     mbar_init(drain, 1);
-    mbar_init(p_full, 4);
+    for (int t = 0; t < NT; ++t) {
+      mbar_init(xg + t, 8);
+      mbar_init(pvt + t, 1);
+    }
+    for (int s = 0; s < kKtSlots; ++s) {
+      mbar_init(kt_full + s, 1);
+      mbar_init(kt_empty + s, 8);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
+  if (tid < 64) mrow[tid] = -INFINITY;
   if (warp == 8) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -405,455 +364,535 @@ __global__ void __launch_bounds__(288, 1) attention_kernel(AttnParams p) {
   // selection, seq_len, and whatever wrote the query)
   griddep_wait();
   griddep_launch_dependents();
-  if (tid == 0) {
-    // the query rows [H, D] bf16 are contiguous: one bulk copy into X tile 1,
-    // which holds no slab before the second chunk
-    const uint32_t qbytes = (uint32_t)(p.heads * D * 2);
-    mbar_arrive_expect_tx(q_full, qbytes);
-    bulk_load(sx + C::kXBytes, p.q + (int64_t)row * p.heads * D, qbytes, q_full);
-  }
-  const RowKeys rk = row_keys(p, row, D);
-  const int nk = rk.n_global + rk.n_swa;
-  const int nchunk = (nk + C::kKeys - 1) / C::kKeys;
-  const int c0 = (int)((int64_t)nchunk * split / p.splits);
-  const int c1 = (int)((int64_t)nchunk * (split + 1) / p.splits);
-  const int nloc = c1 - c0;
-  const bool direct = p.splits == 1;
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tO = tmem + C::kSCols;
+  const uint32_t tO = tmem + 128;  // O^T tile t at columns 128 + 64 t
+  const RowKeys rk = row_keys(p, row, D);
+  const CtaKeys ck = cta_keys(rk, split, p.splits);
+  bool ok = true;  // this thread's view: false once a wait gave up
 
-  if (warp >= 4 && warp < 8) {
-    // =============================================================== data warps
-    const int dt = tid - 128;     // 0..127
-    const int quad = warp & 3;    // TMEM lane quadrant of this warp
-    // ---- gather / dequantise pipeline (its first index entries and rows are
-    // requested before the query conversion, which hides their latency)
-    const int j = dt & 63, sgrp = dt >> 6;
-    auto resolve_pos = [&](int c) -> int {  // chunk-local c -> index entry (or -1)
-      const int g = (c0 + c) * C::kKeys + j;
-      return (c < nloc && g < rk.n_global) ? __ldg(p.idx + (int64_t)row * p.kcap + g) : -1;
+  if (warp < 8) {
+    // ============================================================ compute warps
+    const int ct = tid;               // 0..255
+    const int quad = warp & 3, hf = warp >> 2;
+    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+    const int j = 32 * quad + lane;   // softmax: this thread's key slot
+    RawItem raw[C::kItems];
+    uint32_t kinds = 0;               // 2 bits per item: 0 zero row, 1 FP4 row, 2 FP8 window row
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      if (ok && !mbar_wait(bar, parity, abort_flag)) ok = false;
+      ok = __all_sync(0xffffffffu, ok);
     };
-    auto resolve_src = [&](int c, int pos) -> KeySrc {
-      KeySrc k{nullptr, nullptr, 0};
-      if (c >= nloc) return k;
-      const int g = (c0 + c) * C::kKeys + j;
-      if (g < rk.n_global) {
-        if (pos >= 0 && pos < rk.vis) {
-          const int64_t r = p.map.row(rk.b, pos);
-          if (r >= 0) {
-            k.a = p.codes + r * p.code_stride;
-            k.s = p.scales + r * p.scale_stride;
-            k.kind = 1;
-          } else if (sgrp == 0) {
-            set_status(p.status, CSA2_DEV_BAD_PAGE);
-          }
-        } else if (sgrp == 0) {
-          set_status(p.status, CSA2_DEV_BAD_INDEX);
-        }
-      } else if (g < nk) {
-        k.a = rk.swa0 + (int64_t)(g - rk.n_global) * D;
-        k.kind = 2;
-      }
-      return k;
-    };
-    auto load_raw = [&](const KeySrc& k, RawKey<NP>& raw) {
-      if (k.kind == 1) {
+    // raw bytes of tile i's keys for this thread's items
+    auto load_raw = [&](int i) {
+      const int32_t* tab = ktab + (i % kKtSlots) * kTile;
+      const int nk = ck.tile_keys(i);
+      kinds = 0;
 #pragma unroll
-        for (int i = 0; i < NP; ++i) {
-          const int s = sgrp + 2 * i;
-          if (s < NSLAB) {
-            raw.c0[i] = __ldg(reinterpret_cast<const uint4*>(k.a + s * 32));
-            raw.c1[i] = __ldg(reinterpret_cast<const uint4*>(k.a + s * 32 + 16));
-            raw.sc[i] = __ldg(reinterpret_cast<const uint32_t*>(k.s + s * 4));
+      for (int u = 0; u < C::kItems; ++u) {
+        const int it = ct + kComputeThreads * u;
+        if (ok && it < kTile * NSLAB) {
+          const int jj = it % kTile, s = it / kTile;
+          const int v = jj < nk ? tab[jj] : -1;
+          if (v >= 0) {
+            const uint8_t* cp = p.codes + (int64_t)v * p.code_stride + s * 32;
+            raw[u].a = __ldg(reinterpret_cast<const uint4*>(cp));
+            raw[u].b = __ldg(reinterpret_cast<const uint4*>(cp + 16));
+            raw[u].c.x = __ldg(reinterpret_cast<const uint32_t*>(p.scales + (int64_t)v * p.scale_stride + s * 4));
+            kinds |= 1u << (2 * u);
+          } else if (v <= -2) {
+            const uint4* wp = reinterpret_cast<const uint4*>(rk.swa0 + (int64_t)(-2 - v) * D + s * 64);
+            raw[u].a = __ldg(wp);
+            raw[u].b = __ldg(wp + 1);
+            raw[u].c = __ldg(wp + 2);
+            raw[u].d = __ldg(wp + 3);
+            kinds |= 2u << (2 * u);
           }
         }
       }
     };
-    // pipeline registers: raw bytes of chunk it+1, source of chunk it+2,
-    // index entry of chunk it+3
-    RawKey<NP> raw;
-    KeySrc src_next = resolve_src(0, resolve_pos(0));
-    load_raw(src_next, raw);
-    KeySrc src_n1 = resolve_src(1, resolve_pos(1));
-    int pos3 = resolve_pos(2);
-    // ---- query: f16 copy of the bf16 rows, by all nine warps.  When some
-    // |q| >= 2^14 the data warps redo it with each head scaled by a power of
-    // two so that its f16 copy stays exact.
-    bool ok = mbar_wait(q_full, 0, abort_flag);
-    ok = __all_sync(0xffffffffu, ok);
-    {
-      const uint8_t* qs = sx + C::kXBytes;
-      constexpr int kChunks = D / 8;  // 16-byte chunks per head row
-      if (!convert_query<NSLAB>(qs, sq, tid, ok, p.heads)) {
-        if (dt < 64) qmul[dt] = p.scale_log2;
-      } else {
-        constexpr int kPer = (kChunks + 31) / 32;
-        for (int hh = 0; hh < 16; ++hh) {
-          const int h = 16 * (warp - 4) + hh;
-          uint4 v[kPer];
-          float mx = 0.0f;
+    // ---- tile 0's table and raw bytes, requested before the query copy lands
+    if (ck.ntile > 0) {
+      wait_all(kt_full, 0);
+      load_raw(0);
+    }
+    // ---- query: f16 copy of the bf16 rows (staged in the X slabs).  When some
+    // |q| >= 2^14, each head is redone scaled by a power of two so that its
+    // f16 copy stays exact (the logit factor absorbs the power).
+    wait_all(q_full, 0);
+    if (!convert_query<NSLAB>(sx, sq, ct, ok, p.heads)) {
+      if (ct < 64) qmul[ct] = ct < p.heads ? p.scale_log2 : 0.0f;
+    } else {
+      constexpr int kChunks = D / 8;
+      constexpr int kPer = (kChunks + 31) / 32;
+      for (int hh = 0; hh < 8; ++hh) {
+        const int h = 8 * warp + hh;
+        uint4 v[kPer];
+        float mx = 0.0f;
 #pragma unroll
-          for (int i = 0; i < kPer; ++i) {
-            const int c = lane + 32 * i;
-            v[i] = make_uint4(0, 0, 0, 0);
-            if (ok && h < p.heads && c < kChunks)
-              v[i] = *reinterpret_cast<const uint4*>(qs + (h * D + c * 8) * 2);
+        for (int i = 0; i < kPer; ++i) {
+          const int c = lane + 32 * i;
+          v[i] = make_uint4(0, 0, 0, 0);
+          if (ok && h < p.heads && c < kChunks)
+            v[i] = *reinterpret_cast<const uint4*>(sx + (h * D + c * 8) * 2);
+          const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            mx = fmaxf(mx, fabsf(__uint_as_float(w4[u] << 16)));
+            mx = fmaxf(mx, fabsf(__uint_as_float(w4[u] & 0xFFFF0000u)));
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        int e = 0;
+        if (mx > 16384.0f) e = (int)ceilf(log2f(mx)) - 14;
+        const float inv = exp2f((float)-e);
+        if (lane == 0) qmul[h] = h < p.heads ? p.scale_log2 * exp2f((float)e) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int c = lane + 32 * i;
+          if (c < kChunks) {
             const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            uint32_t o[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              mx = fmaxf(mx, fabsf(__uint_as_float(w4[u] << 16)));
-              mx = fmaxf(mx, fabsf(__uint_as_float(w4[u] & 0xFFFF0000u)));
+              __half2 h2 = __floats2half2_rn(__uint_as_float(w4[u] << 16) * inv,
+                                             __uint_as_float(w4[u] & 0xFFFF0000u) * inv);
+              o[u] = *reinterpret_cast<uint32_t*>(&h2);
             }
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-          int e = 0;
-          if (mx > 16384.0f) e = (int)ceilf(log2f(mx)) - 14;
-          const float inv = exp2f((float)-e);
-          if (lane == 0) qmul[h] = p.scale_log2 * exp2f((float)e);
-#pragma unroll
-          for (int i = 0; i < kPer; ++i) {
-            const int c = lane + 32 * i;
-            if (c < kChunks) {
-              const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-              uint32_t o[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                __half2 h2 = __floats2half2_rn(__uint_as_float(w4[u] << 16) * inv,
-                                               __uint_as_float(w4[u] & 0xFFFF0000u) * inv);
-                o[u] = *reinterpret_cast<uint32_t*>(&h2);
-              }
-              st_swz(sq + (c >> 3) * C::kSlab, h, c & 7, make_uint4(o[0], o[1], o[2], o[3]));
-            }
+            st_swz(sq + (c >> 3) * C::kQSlab, h, c & 7, make_uint4(o[0], o[1], o[2], o[3]));
           }
         }
       }
     }
     fence_async_smem();
-    named_sync(1, 288);  // Q slabs written; X tile 1 free again
+    named_sync(1, kComputeThreads);  // Q slabs and qmul written; the staging area is free
+    if (lane == 0) mbar_arrive(q_ready);
 
-    for (int it = 0; it < nloc; ++it) {
-      const int buf = it & 1;
-      const KeySrc src_cur = src_next;
-      // X tile `buf` is free once PV of chunk it-2 has completed
-      if (ok && it >= 2 && !mbar_wait(pv_done + buf, ((it - 2) >> 1) & 1, abort_flag)) ok = false;
-      ok = __all_sync(0xffffffffu, ok);
-      uint8_t* tile = sx + buf * C::kXBytes;
-      if (ok) {
+    // Partial softmax denominators of this key slot and heads 32 hf .. +32
+    // live in tensor memory (lane j, columns kLCol + 32 hf ..), not registers.
+    const uint32_t tl = tmem + lane_base + C::kLCol + 32 * hf;
+    tmem_st16z(tl);
+    tmem_st16z(tl + 16);
+    tmem_st_wait();
+
+    for (int i = 0; i < ck.ntile; ++i) {
+      // ---- dequantise tile i, slab pair by slab pair: pair t is free once PV
+      // of tile i-1 has finished with accumulator tile t
+      const int nk = ck.tile_keys(i);
+      for (int t = 0; t < NT; ++t) {
+        if (i > 0) wait_all(pvt + t, (i - 1) & 1);
+        if (ok) {
 #pragma unroll
-        for (int i = 0; i < NP; ++i) {
-          const int s = sgrp + 2 * i;
-          if (s >= NSLAB) break;
-          uint8_t* slab = tile + s * C::kSlab;
-          if (src_cur.kind == 1) {
-            const uint32_t cw[8] = {raw.c0[i].x, raw.c0[i].y, raw.c0[i].z, raw.c0[i].w,
-                                    raw.c1[i].x, raw.c1[i].y, raw.c1[i].z, raw.c1[i].w};
+          for (int u = 0; u < C::kItems; ++u) {
+            const int it = ct + kComputeThreads * u;
+            if (it >= kTile * NSLAB) continue;
+            const int jj = it % kTile, s = it / kTile;
+            if ((s >> 1) != t) continue;
+            uint8_t* slab = sx + s * C::kXSlab;
+            const uint32_t kind = (kinds >> (2 * u)) & 3u;
+            if (kind == 1) {
+              const uint32_t cw[8] = {raw[u].a.x, raw[u].a.y, raw[u].a.z, raw[u].a.w,
+                                      raw[u].b.x, raw[u].b.y, raw[u].b.z, raw[u].b.w};
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {  // 8 channels = 4 code bytes, group c/2
-              const uint32_t sb = (raw.sc[i] >> (8 * (c >> 1))) & 0xFFu;
-              const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
-              const __half2 sh = *reinterpret_cast<const __half2*>(&s2);
-              uint32_t o[4];
+              for (int c = 0; c < 8; ++c) {  // 8 channels = 4 code bytes, group c/2
+                const uint32_t sb = (raw[u].c.x >> (8 * (c >> 1))) & 0xFFu;
+                const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
+                const __half2 sh = *reinterpret_cast<const __half2*>(&s2);
+                uint32_t o[4];
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const uint32_t v2 = e2m1x2_to_f16x2((cw[c] >> (8 * u)) & 0xFFu);
-                __half2 r2 = __hmul2(*reinterpret_cast<const __half2*>(&v2), sh);
-                o[u] = *reinterpret_cast<uint32_t*>(&r2);
+                for (int q = 0; q < 4; ++q) {
+                  const uint32_t v2 = e2m1x2_to_f16x2((cw[c] >> (8 * q)) & 0xFFu);
+                  __half2 r2 = __hmul2(*reinterpret_cast<const __half2*>(&v2), sh);
+                  o[q] = *reinterpret_cast<uint32_t*>(&r2);
+                }
+                st_swz(slab, jj, c, make_uint4(o[0], o[1], o[2], o[3]));
               }
-              st_swz(slab, j, c, make_uint4(o[0], o[1], o[2], o[3]));
+            } else if (kind == 2) {
+              const uint4 w[4] = {raw[u].a, raw[u].b, raw[u].c, raw[u].d};
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const uint32_t lo = (c & 1) ? w[c >> 1].z : w[c >> 1].x;
+                const uint32_t hi = (c & 1) ? w[c >> 1].w : w[c >> 1].y;
+                st_swz(slab, jj, c,
+                       make_uint4(e4m3x2_to_f16x2(lo & 0xFFFFu), e4m3x2_to_f16x2(lo >> 16),
+                                  e4m3x2_to_f16x2(hi & 0xFFFFu), e4m3x2_to_f16x2(hi >> 16)));
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 8; ++c) st_swz(slab, jj, c, make_uint4(0, 0, 0, 0));
             }
-          } else if (src_cur.kind == 2) {
-            const uint4* wr = reinterpret_cast<const uint4*>(src_cur.a + s * 64);
-            uint4 w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) w[u] = __ldg(wr + u);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint32_t lo = (c & 1) ? w[c >> 1].z : w[c >> 1].x;
-              const uint32_t hi = (c & 1) ? w[c >> 1].w : w[c >> 1].y;
-              st_swz(slab, j, c,
-                     make_uint4(e4m3x2_to_f16x2(lo & 0xFFFFu), e4m3x2_to_f16x2(lo >> 16),
-                                e4m3x2_to_f16x2(hi & 0xFFFFu), e4m3x2_to_f16x2(hi >> 16)));
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) st_swz(slab, j, c, make_uint4(0, 0, 0, 0));
           }
         }
-      }
-      if (sgrp == 0) {  // warps 4 and 5 hold keys 0-31 and 32-63
-        const uint32_t bal = __ballot_sync(0xffffffffu, src_cur.kind != 0);
-        if (lane == 0) vmask[buf * 2 + (warp & 1)] = bal;
-      }
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(x_full + buf);
-      // prefetch: raw bytes of chunk it+1, source of it+2, index entry of it+3
-      src_next = src_n1;
-      load_raw(src_next, raw);
-      src_n1 = resolve_src(it + 2, pos3);
-      pos3 = resolve_pos(it + 3);
-      // decision of the softmax warps for chunk it-1; PV(it-2) is complete
-      if (it >= 1) {
-        const int pb = (it - 1) & 1;
-        if (ok && !mbar_wait(dec + pb, ((it - 1) >> 1) & 1, abort_flag)) ok = false;
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok && need_resc[pb]) {
-          rescale_output<C::NT>(tO, quad, alpha);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(resc);
-        }
-      }
-    }
-    if (nloc >= 1) {
-      // decision of the last chunk (needs PV of the chunk before it)
-      const int last = nloc - 1, pb = last & 1;
-      if (ok && last >= 1 && !mbar_wait(pv_done + (pb ^ 1), ((last - 1) >> 1) & 1, abort_flag))
-        ok = false;
-      if (ok && !mbar_wait(dec + pb, (last >> 1) & 1, abort_flag)) ok = false;
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok && need_resc[pb]) {
-        rescale_output<C::NT>(tO, quad, alpha);
+        fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(resc);
+        if (lane == 0) mbar_arrive(xg + t);
       }
-      if (ok && !mbar_wait(pv_done + pb, (last >> 1) & 1, abort_flag)) ok = false;
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    tc_fence_after();
-    named_sync(2, 288);  // lrow written by the softmax warps
-    // ---- epilogue: O^T tiles, 32 channels per warp per tile; with several
-    // CTAs per row the unnormalised output goes to the stage [64][D] fp32
-    // (the X tiles, free now) for the cluster merge
-    float* stage = reinterpret_cast<float*>(sx);
-#pragma unroll 1
-    for (int t = 0; t < C::NT; ++t) {
-      const int s0 = (2 * t + 1 < NSLAB) ? 2 * t : NSLAB - 2;
-      const int local = 32 * quad + lane;
-      const int d = s0 * 64 + local;
-      const bool mine = !(t == C::NT - 1 && (NSLAB & 1) && local < 64);
-#pragma unroll 1
-      for (int c = 0; c < 64; c += 16) {
-        uint32_t v[16];
-        if (nloc > 0 && ok) {
-          tmem_ld16(tO + 64 * t + c + ((uint32_t)(32 * quad) << 16), v);
-          tmem_ld_wait();
-          reg_fence(v);
-        } else {
-#pragma unroll
-          for (int u = 0; u < 16; ++u) v[u] = 0u;
-        }
-        if (mine) {
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const int hh = c + u;
-            if (hh < p.heads) {
-              const float acc = __uint_as_float(v[u]);
-              if (direct) {
-                const float l = lrow[hh];
-                p.out[((int64_t)row * p.heads + hh) * D + d] = l > 0.0f ? acc / l : 0.0f;
-              } else {
-                stage[hh * D + d] = acc;
-              }
-            }
-          }
-        }
+      // ---- the next tile's raw bytes, one tile ahead
+      if (i + 1 < ck.ntile) {
+        wait_all(kt_full + ((i + 1) % kKtSlots), ((i + 1) / kKtSlots) & 1);
+        load_raw(i + 1);
       }
-    }
-  } else if (warp < 4) {
-    // ============================================================ softmax warps
-    // Row h of an M=64 accumulator sits in tensor-memory lane
-    // 32 * (h / 16) + h % 16.  A 16x256b load gives thread t of warp q the
-    // rows (heads) hA = 16 q + t / 4 and hB = hA + 8, columns (keys)
-    // 8 k + 2 (t % 4) + {0, 1}: each head is spread over the four threads
-    // t % 4 = 0..3, each holding 16 of its 64 keys.  Running maxima agree
-    // over the four threads; the sums stay per thread until the end.
-    const int hA = 16 * warp + (lane >> 2), hB = hA + 8;
-    const int cq = 2 * (lane & 3);  // this thread's first key in each group of 8
-    {  // a share of the query conversion
-      const bool okq = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag));
-      convert_query<NSLAB>(sx + C::kXBytes, sq, tid, okq, p.heads);
-    }
-    named_sync(1, 288);  // Q slabs written
-    float mA = -INFINITY, mB = -INFINITY, lA = 0.0f, lB = 0.0f;
-    const float qmA = qmul[hA], qmB = qmul[hB];
-    bool ok = true;
-    int n_resc = 0;
-    for (int it = 0; it < nloc; ++it) {
-      const int buf = it & 1;
-      if (ok && !mbar_wait(s_full + buf, (it >> 1) & 1, abort_flag)) ok = false;
-      ok = __all_sync(0xffffffffu, ok);
+      // ---- softmax of tile i
+      wait_all(s_full + (i & 1), (i >> 1) & 1);
       tc_fence_after();
       uint32_t sr[32];
-      float mxA = -INFINITY, mxB = -INFINITY;
       if (ok) {
-        tmem_ld_16x256b_x8(tmem + 64 * buf + ((uint32_t)(32 * warp) << 16), sr);
+        tmem_ld32(tmem + lane_base + 64 * (i & 1) + 32 * hf, sr);
         tmem_ld_wait();
-        reg_fence(*reinterpret_cast<uint32_t(*)[16]>(&sr[0]));
-        reg_fence(*reinterpret_cast<uint32_t(*)[16]>(&sr[16]));
-        const uint64_t mask = (uint64_t)vmask[buf * 2] | ((uint64_t)vmask[buf * 2 + 1] << 32);
+        reg_fence32(sr);
+      }
+      const int32_t* tab = ktab + (i % kKtSlots) * kTile;
+      const bool valid = ok && j < nk && tab[j] != -1;
+      float vmax = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+      for (int h = 0; h < 32; ++h) {
+        const float x = __uint_as_float(sr[h]) * qmul[32 * hf + h] - mrow[32 * hf + h];
+        vmax = fmaxf(vmax, valid ? x : -INFINITY);
+      }
+      // raise the running maximum when a logit exceeds it by more than 2^8
+      // (always on the first tile); uniform over the compute warps.  Lane h
+      // keeps the old and new maximum of head 32 hf + h.
+      const int hh = 32 * hf + lane;
+      float m_old = 0.0f, m_new = 0.0f;
+      const bool raise = named_sync_or(2, kComputeThreads, vmax > 8.0f);
+      if (raise) {
+        float mine = -INFINITY;
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const bool valid = (mask >> (8 * k + cq + e)) & 1;
-            const float vA = valid ? __uint_as_float(sr[4 * k + e]) * qmA : -INFINITY;
-            const float vB = valid ? __uint_as_float(sr[4 * k + 2 + e]) * qmB : -INFINITY;
-            sr[4 * k + e] = __float_as_uint(vA);
-            sr[4 * k + 2 + e] = __float_as_uint(vB);
-            mxA = fmaxf(mxA, vA);
-            mxB = fmaxf(mxB, vB);
-          }
+        for (int h = 0; h < 32; ++h) {
+          const float x = valid ? __uint_as_float(sr[h]) * qmul[32 * hf + h] : -INFINITY;
+          const float r = warp_max(x);
+          mine = lane == h ? r : mine;
         }
-        mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
-        mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
-        mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
-        mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
-      }
-      tc_fence_before();
-      // lazily raised running maximum: rescale only when it jumps by > 2^8
-      bool need = false;
-      float aA = 1.0f, aB = 1.0f;
-      if (mxA > -INFINITY && (mA == -INFINITY || mxA > mA + 8.0f)) {
-        need = true;
-        aA = (mA == -INFINITY) ? 0.0f : fast_exp2(mA - mxA);
-        mA = mxA;
-        lA *= aA;
-      }
-      if (mxB > -INFINITY && (mB == -INFINITY || mxB > mB + 8.0f)) {
-        need = true;
-        aB = (mB == -INFINITY) ? 0.0f : fast_exp2(mB - mxB);
-        mB = mxB;
-        lB *= aB;
-      }
-      if ((lane & 3) == 0) {
-        alpha[hA] = aA;
-        alpha[hB] = aB;
-      }
-      const bool resc_needed = named_sync_or(3, 128, need) && it > 0;
-      if (tid == 0) need_resc[buf] = resc_needed ? 1 : 0;
-      named_sync(3, 128);
-      if (lane == 0) mbar_arrive(dec + buf);
-      // P and the accumulator are free once PV of chunk it-1 is done
-      if (ok && it >= 1 && !mbar_wait(pv_done + (buf ^ 1), ((it - 1) >> 1) & 1, abort_flag))
-        ok = false;
-      if (resc_needed) {
-        if (ok && !mbar_wait(resc, n_resc & 1, abort_flag)) ok = false;
-        ++n_resc;
-      }
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) {
+        tmax[quad * 64 + hh] = mine;
+        named_sync(3, kComputeThreads);
+        m_old = mrow[hh];
+        m_new = fmaxf(fmaxf(m_old, fmaxf(tmax[hh], tmax[64 + hh])),
+                      fmaxf(tmax[128 + hh], tmax[192 + hh]));
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float vA0 = __uint_as_float(sr[4 * k]), vA1 = __uint_as_float(sr[4 * k + 1]);
-          const float vB0 = __uint_as_float(sr[4 * k + 2]), vB1 = __uint_as_float(sr[4 * k + 3]);
-          const float eA0 = vA0 == -INFINITY ? 0.0f : fast_exp2(vA0 - mA);
-          const float eA1 = vA1 == -INFINITY ? 0.0f : fast_exp2(vA1 - mA);
-          const float eB0 = vB0 == -INFINITY ? 0.0f : fast_exp2(vB0 - mB);
-          const float eB1 = vB1 == -INFINITY ? 0.0f : fast_exp2(vB1 - mB);
-          const __half2 pA = __floats2half2_rn(eA0, eA1), pB = __floats2half2_rn(eB0, eB1);
-          const float2 bA = __half22float2(pA), bB = __half22float2(pB);
-          lA += bA.x + bA.y;
-          lB += bB.x + bB.y;
-          st_swz4(sp, hA, k, 2 * cq, *reinterpret_cast<const uint32_t*>(&pA));
-          st_swz4(sp, hB, k, 2 * cq, *reinterpret_cast<const uint32_t*>(&pB));
+        for (int hb = 0; hb < 32; hb += 16) {
+          uint32_t lv[16];
+          tmem_ld16(tl + hb, lv);
+          tmem_ld_wait();
+          reg_fence(lv);
+#pragma unroll
+          for (int h = 0; h < 16; ++h) {
+            const float mo = __shfl_sync(0xffffffffu, m_old, hb + h);
+            const float mn = __shfl_sync(0xffffffffu, m_new, hb + h);
+            const float al = mo == -INFINITY ? (mn == -INFINITY ? 1.0f : 0.0f) : fast_exp2(mo - mn);
+            lv[h] = __float_as_uint(__uint_as_float(lv[h]) * al);
+          }
+          tmem_st16(tl + hb, lv);
+        }
+        tmem_st_wait();
+        named_sync(3, kComputeThreads);   // every thread has read mrow and tmax
+        if (quad == 0) mrow[hh] = m_new;
+        named_sync(3, kComputeThreads);   // the new maxima are in mrow
+      }
+      // weights p = 2^(logit - m), rounded to f16, summed as rounded; this
+      // key's row of P^T, 8 heads (16 bytes) at a time
+#pragma unroll
+      for (int hb = 0; hb < 32; hb += 16) {
+        uint32_t lv[16];
+        tmem_ld16(tl + hb, lv);
+        tmem_ld_wait();
+        reg_fence(lv);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int h = hb + 8 * u + 2 * e;
+            const float x0 = __uint_as_float(sr[h]) * qmul[32 * hf + h] - mrow[32 * hf + h];
+            const float x1 = __uint_as_float(sr[h + 1]) * qmul[32 * hf + h + 1] - mrow[32 * hf + h + 1];
+            const float e0 = valid ? fast_exp2(x0) : 0.0f;
+            const float e1 = valid ? fast_exp2(x1) : 0.0f;
+            const __half2 ph = __floats2half2_rn(e0, e1);
+            const float2 pf = __half22float2(ph);
+            lv[h - hb] = __float_as_uint(__uint_as_float(lv[h - hb]) + pf.x);
+            lv[h - hb + 1] = __float_as_uint(__uint_as_float(lv[h - hb + 1]) + pf.y);
+            pk[e] = *reinterpret_cast<const uint32_t*>(&ph);
+          }
+          if (j < kTile) st_swz(sp, j, (4 * hf + (hb >> 3) + u), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+        }
+        tmem_st16(tl + hb, lv);
+      }
+      tmem_st_wait();
+      if (raise && i > 0) {
+        // O^T *= 2^(m_old - m_new) per head column, once PV of tile i-1 is
+        // complete (before PV of this tile, which waits for p_full)
+        wait_all(pvt + NT - 1, (i - 1) & 1);
+        tc_fence_after();
+        if (ok) {
+#pragma unroll 1
+          for (int t = 0; t < NT; ++t) {
+            uint32_t v[32];
+            const uint32_t a = tO + lane_base + 64 * t + 32 * hf;
+            tmem_ld32(a, v);
+            tmem_ld_wait();
+            reg_fence32(v);
+#pragma unroll
+            for (int h = 0; h < 32; ++h) {
+              const float mo = __shfl_sync(0xffffffffu, m_old, h);
+              const float mn = __shfl_sync(0xffffffffu, m_new, h);
+              const float al = mo == -INFINITY ? (mn == -INFINITY ? 1.0f : 0.0f) : fast_exp2(mo - mn);
+              v[h] = __float_as_uint(__uint_as_float(v[h]) * al);
+            }
+            tmem_st32(a, v);
+          }
+          tmem_st_wait();
         }
       }
       fence_async_smem();
       tc_fence_before();
-      named_sync(3, 128);
-      if (lane == 0) mbar_arrive(p_full);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(p_full);
+        mbar_arrive(kt_empty + (i % kKtSlots));
+      }
     }
-    // per-head sums over the four threads that hold the head
-    lA += __shfl_xor_sync(0xffffffffu, lA, 1);
-    lA += __shfl_xor_sync(0xffffffffu, lA, 2);
-    lB += __shfl_xor_sync(0xffffffffu, lB, 1);
-    lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-    if ((lane & 3) == 0) {
-      lrow[hA] = (nloc > 0 && ok) ? lA : 0.0f;
-      mrow[hA] = (nloc > 0 && ok) ? mA : -INFINITY;
-      lrow[hB] = (nloc > 0 && ok) ? lB : 0.0f;
-      mrow[hB] = (nloc > 0 && ok) ? mB : -INFINITY;
+    // ---- after the last tile: per-head denominators (sum over the key slots)
+    if (ck.ntile > 0) wait_all(pvt + NT - 1, (ck.ntile - 1) & 1);
+    tc_fence_after();
+    float l[32];
+    {
+      uint32_t lv[32];
+      tmem_ld32(tl, lv);
+      tmem_ld_wait();
+      reg_fence32(lv);
+#pragma unroll
+      for (int h = 0; h < 32; ++h) l[h] = __uint_as_float(lv[h]);
     }
-    named_sync(2, 288);
-  } else {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int h = 0; h < off; ++h) {
+        const float send = upper ? l[h] : l[h + off];
+        const float keep = upper ? l[h + off] : l[h];
+        l[h] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+    }
+    lsum[quad * 64 + 32 * hf + lane] = l[0];   // lane holds head 32 hf + lane
+    named_sync(1, kComputeThreads);
+    if (ct < 64) {
+      const float s = (lsum[ct] + lsum[64 + ct]) + (lsum[128 + ct] + lsum[192 + ct]);
+      const bool any = ck.ntile > 0 && ok;
+      lrow[ct] = any ? s : 0.0f;
+      if (!any) mrow[ct] = -INFINITY;
+    }
+  } else if (warp == 8) {
     // ================================================================ MMA warp
-    {  // a share of the query conversion
-      const bool okq = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag));
-      convert_query<NSLAB>(sx + C::kXBytes, sq, tid, okq, p.heads);
-    }
-    named_sync(1, 288);  // Q slabs written
-    if (lane == 0 && nloc > 0) {
-      constexpr uint32_t idesc_qk = instr_desc(0, 0, false, false, 64, 64);
-      constexpr uint32_t idesc_pv = instr_desc(0, 0, true, false, 128, 64);
-      const uint32_t q0 = smem_u32(sq), xb = smem_u32(sx), p0 = smem_u32(sp);
-      auto issue_qk = [&](int c) {
-        const uint32_t x0 = xb + (c & 1) * C::kXBytes;
-        const uint32_t d = tmem + 64 * (c & 1);
-#pragma unroll 1
-        for (int s = 0; s < NSLAB; ++s) {
+    if (lane == 0 && ck.ntile > 0) {
+      constexpr uint32_t idesc_qk = instr_desc(0, 0, false, false, 128, 64);
+      constexpr uint32_t idesc_pv = instr_desc(0, 0, true, true, 128, 64);
+      const uint32_t xb = smem_u32(sx), qb = smem_u32(sq), pb = smem_u32(sp);
+      bool issued = false;
+      ok = mbar_wait(q_ready, 0, abort_flag);
+      for (int i = 0; ok && i < ck.ntile; ++i) {
+        const uint32_t sd = tmem + 64 * (i & 1);
+        for (int t = 0; t < NT; ++t) {
+          if (!mbar_wait(xg + t, i & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16(d, smem_desc(q0 + s * C::kSlab + kk * 32, 16, 1024, 2),
-                    smem_desc(x0 + s * C::kSlab + kk * 32, 16, 1024, 2), idesc_qk,
-                    (s | kk) != 0 ? 1u : 0u);
+          for (int s2 = 0; s2 < 2; ++s2) {
+            const int s = 2 * t + s2;
+            if (s >= NSLAB) break;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16(sd, smem_desc(xb + s * C::kXSlab + kk * 32, 16, 1024, 2),
+                      smem_desc(qb + s * C::kQSlab + kk * 32, 16, 1024, 2), idesc_qk,
+                      (s | kk) != 0 ? 1u : 0u);
+          }
+          issued = true;
         }
-        mma_commit(s_full + (c & 1));
-      };
-      bool ok = mbar_wait(x_full + 0, 0, abort_flag);
-      if (ok) {
+        if (!ok) break;
+        mma_commit(s_full + (i & 1));
+        if (!mbar_wait(p_full, i & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        issue_qk(0);
-      }
-      auto issue_pv = [&](int c) {
-        const uint32_t x0 = xb + (c & 1) * C::kXBytes;
-#pragma unroll
-        for (int t = 0; t < C::NT; ++t) {
-          const int s0 = (2 * t + 1 < NSLAB) ? 2 * t : NSLAB - 2;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16(tO + 64 * t, smem_desc(x0 + s0 * C::kSlab + kk * 2048, C::kSlab, 1024, 2),
-                    smem_desc(p0 + kk * 32, 16, 1024, 2), idesc_pv, (c > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(pv_done + (c & 1));
-      };
-      // Whatever is ready, PV first: PV(c) once chunk c's softmax weights
-      // are written, else the next QK once its X tile is dequantised.  QK can
-      // run two chunks ahead of PV, which keeps the tensor pipe busy during
-      // a chunk's softmax.  This is safe because X(q) is dequantised only
-      // after PV(q-2) has completed, hence after the softmax has read S(q-2),
-      // whose tensor-memory buffer QK(q) reuses.
-      int next_qk = 1, next_pv = 0;
-      const uint64_t t0 = globaltimer();
-      for (uint32_t spin = 0; ok && next_pv < nloc; ++spin) {
-        if (mbar_try_wait(p_full, next_pv & 1)) {
-          tc_fence_after();
-          issue_pv(next_pv);
-          ++next_pv;
-        } else if (next_qk < nloc &&
-                   mbar_try_wait(x_full + (next_qk & 1), (next_qk >> 1) & 1)) {
-          tc_fence_after();
-          issue_qk(next_qk);
-          ++next_qk;
-        } else if ((spin & 63) == 63 && (*abort_flag || globaltimer() - t0 > g_wait_ns)) {
-          *abort_flag = 1;
-          ok = false;
+        const int nks = (ck.tile_keys(i) + 15) / 16;
+        for (int t = 0; t < NT; ++t) {
+          // A = X^T read channel-major: channels of slabs 2t, 2t+1 (for an odd
+          // slab count the last tile's upper half falls on Q: unused rows)
+          for (int kk = 0; kk < nks; ++kk)
+            mma_f16(tO + 64 * t, smem_desc(xb + 2 * t * C::kXSlab + kk * 2048, C::kXSlab, 1024, 2),
+                    smem_desc(pb + kk * 2048, C::kXSlab, 1024, 2), idesc_pv,
+                    (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(pvt + t);
         }
       }
-      // let every issued MMA land before the tensor memory is freed
-      mma_commit(drain);
-      mbar_wait_drain(drain, 0);
+      if (issued) {  // let every issued MMA land before tensor memory is freed
+        mma_commit(drain);
+        mbar_wait_drain(drain, 0);
+      }
     }
     __syncwarp();
-    named_sync(2, 288);
+  } else {
+    // ============================================================== index warp
+    if (lane == 0) {
+      // the query rows [H, D] bf16 are contiguous: one bulk copy into the X
+      // slabs, which hold no key before the query is converted
+      const uint32_t qbytes = (uint32_t)(p.heads * D * 2);
+      mbar_arrive_expect_tx(q_full, qbytes);
+      bulk_load(sx, p.q + (int64_t)row * p.heads * D, qbytes, q_full);
+    }
+    for (int i = 0; i < ck.ntile; ++i) {
+      const int slot = i % kKtSlots;
+      if (i >= kKtSlots) {
+        if (ok && !mbar_wait(kt_empty + slot, ((i / kKtSlots) - 1) & 1, abort_flag)) ok = false;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      int32_t* tab = ktab + slot * kTile;
+      const int base = i * ck.ts;
+      const int nk = ck.tile_keys(i);
+      constexpr int kPer = (kTile + 31) / 32;
+      int pos[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {  // index entries first, all in flight
+        const int jj = lane + 32 * u;
+        const int l = base + jj;
+        pos[u] = (jj < nk && l < ck.ng) ? __ldg(p.idx + (int64_t)row * p.kcap + ck.g0 + l) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int jj = lane + 32 * u;
+        if (jj >= kTile) break;
+        const int l = base + jj;
+        int v = -1;
+        if (jj < nk) {
+          if (l < ck.ng) {
+            if (pos[u] >= 0 && pos[u] < rk.vis) {
+              const int64_t r = p.map.row(rk.b, pos[u]);
+              if (r >= 0) v = (int)r;
+              else set_status(p.status, CSA2_DEV_BAD_PAGE);
+            } else {
+              set_status(p.status, CSA2_DEV_BAD_INDEX);
+            }
+          } else {
+            v = -2 - (ck.w0 + l - ck.ng);
+          }
+        }
+        tab[jj] = v;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(kt_full + slot);
+    }
+    if (lane == 0) mbar_wait_drain(q_full, 0);  // the query copy, if a wait gave up early
+    __syncwarp();
   }
-  if (tid == 0) mbar_wait_drain(q_full, 0);  // the query copy, if a wait gave up early
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const bool any = ck.ntile > 0 && !*abort_flag;
+
+  if (p.splits == 1) {
+    // ---- output: o[h][c] = O^T[c][h] / l_h
+    if (warp < 8) {
+      const int quad = warp & 3, hf = warp >> 2;
+#pragma unroll 1
+      for (int t = 0; t < NT; ++t) {
+        const int c = 128 * t + 32 * quad + lane;
+        if (128 * t + 32 * quad >= D) continue;   // warp-uniform: channels past D
+        uint32_t v[32];
+        if (any) {
+          tmem_ld32(tO + ((uint32_t)(32 * quad) << 16) + 64 * t + 32 * hf, v);
+          tmem_ld_wait();
+          reg_fence32(v);
+        }
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+          const int head = 32 * hf + h;
+          if (head < p.heads) {
+            const float lh = lrow[head];
+            const float o = (any && lh > 0.0f) ? __uint_as_float(v[h]) / lh : 0.0f;
+            p.out[((int64_t)row * p.heads + head) * D + c] = o;
+          }
+        }
+      }
+    }
+  } else {
+    // ---- split-K merge over the cluster of the row:
+    //   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s  per head,
+    // M the largest m_s with l_s > 0.  Each CTA scales its own O^T by its
+    // factor 2^(m_s - M) / den and stores it straight into the shared memory
+    // of the CTA that owns each 32-channel group; after a cluster barrier every
+    // CTA sums the C partials of its own channels and writes them out.
+    const int Cn = p.splits;
+    constexpr int kGroups = D / 32;
+    const int slmax = 32 * ((kGroups + Cn - 1) / Cn);
+    float* recv = reinterpret_cast<float*>(smem);   // [C][64][slmax] (X and Q are free)
+    cluster_sync();  // every CTA's mrow / lrow final; every CTA is done with X and Q
+    if (tid < 64) {
+      float ms[kMaxSplits], ls[kMaxSplits];
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kMaxSplits; ++r) {
+        ms[r] = -INFINITY;
+        ls[r] = 0.0f;
+        if (r < Cn) {
+          ms[r] = peer_f32(&mrow[tid], r);
+          ls[r] = peer_f32(&lrow[tid], r);
+          if (ls[r] > 0.0f) M = fmaxf(M, ms[r]);
+        }
+      }
+      float den = 0.0f;
+#pragma unroll
+      for (int r = 0; r < kMaxSplits; ++r)
+        if (r < Cn && ls[r] > 0.0f) den += exp2f(ms[r] - M) * ls[r];
+      const float lm = lrow[tid];
+      fw[tid] = (lm > 0.0f && den > 0.0f) ? exp2f(mrow[tid] - M) / den : 0.0f;
+    }
+    __syncthreads();
+    if (warp < 8) {
+      const int quad = warp & 3, hf = warp >> 2;
+#pragma unroll 1
+      for (int t = 0; t < NT; ++t) {
+        const int g = 4 * t + quad;   // 32-channel group of this warp
+        if (g >= kGroups) continue;   // warp-uniform
+        int r = 0;
+        while (r + 1 < Cn && g >= (kGroups * (r + 1)) / Cn) ++r;
+        const int c0 = 32 * ((kGroups * r) / Cn);
+        const int cl = 32 * g + lane - c0;
+        uint32_t v[32];
+        if (any) {
+          tmem_ld32(tO + ((uint32_t)(32 * quad) << 16) + 64 * t + 32 * hf, v);
+          tmem_ld_wait();
+          reg_fence32(v);
+        }
+        const uint32_t dst = map_to_rank(recv + ((size_t)split * 64 + 32 * hf) * slmax + cl, r);
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+          const float f = fw[32 * hf + h];
+          const float o = (any && f != 0.0f) ? __uint_as_float(v[h]) * f : 0.0f;
+          st_cluster_f32(dst + (uint32_t)(h * slmax * 4), o);
+        }
+      }
+    }
+    cluster_sync();  // every partial is in its owner's shared memory
+    {
+      const int c0 = 32 * ((kGroups * split) / Cn);
+      const int w = 32 * ((kGroups * (split + 1)) / Cn) - c0;
+      const int n4 = w / 4;
+      const int items = p.heads * n4;
+      for (int it = tid; it < items; it += kAttnThreads) {
+        const int h = it / n4, c4 = it - h * n4;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int s = 0; s < Cn; ++s) {
+          const float4 x = *reinterpret_cast<const float4*>(recv + ((size_t)s * 64 + h) * slmax + 4 * c4);
+          acc.x += x.x;
+          acc.y += x.y;
+          acc.z += x.z;
+          acc.w += x.w;
+        }
+        *reinterpret_cast<float4*>(p.out + ((int64_t)row * p.heads + h) * D + c0 + 4 * c4) = acc;
+      }
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 8) tmem_dealloc(tmem, C::kTmemCols);
   if (tid == 0 && *abort_flag) set_status(p.status, CSA2_DEV_TIMEOUT);
-  if (p.splits > 1) merge_splits<NSLAB>(p);
 }
 
 cudaError_t set_wait_limit_attention(unsigned long long ns) { return set_wait_limit_here(ns); }
@@ -865,6 +904,11 @@ static cudaError_t run_attention(AttnParams p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e == cudaSuccess) e = prefer_max_shared(kern);
   if (e != cudaSuccess) return e;
+  // The merge stages C x 64 x (channels of the widest share) fp32 in the X,
+  // Q and P areas: fewer splits when that would not fit.
+  constexpr int kGroups = C::D / 32;
+  while (p.splits > 1 && p.splits * 64 * 32 * ((kGroups + p.splits - 1) / p.splits) * 4 > C::kMiscOff)
+    --p.splits;
   // A CTA takes a whole SM and a cluster must fit inside one GPC, so not every
   // cluster count runs at once: take the largest split count whose clusters
   // all run in one wave (the splits of a row must also be co-resident).
@@ -872,7 +916,7 @@ static cudaError_t run_attention(AttnParams p, cudaStream_t s) {
     static int fits[kMaxSplits + 1] = {};  // clusters of each size that run at once
     int splits = p.splits;
     while (splits > 1) {
-      if (!fits[splits]) fits[splits] = max_active_clusters(kern, splits, 288, C::kSmem) + 1;
+      if (!fits[splits]) fits[splits] = max_active_clusters(kern, splits, kAttnThreads, C::kSmem) + 1;
       if (fits[splits] - 1 >= p.n_rows) break;
       --splits;
     }
@@ -880,7 +924,7 @@ static cudaError_t run_attention(AttnParams p, cudaStream_t s) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.splits, (unsigned)p.n_rows, 1);
-  cfg.blockDim = dim3(288, 1, 1);
+  cfg.blockDim = dim3(kAttnThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)C::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -901,6 +945,9 @@ static cudaError_t run_attention(AttnParams p, cudaStream_t s) {
 cudaError_t launch_attention(const csa2_cache& c, const AttnArgs& a, const WsLayout& L,
                              uint8_t* ws, int num_sms, cudaStream_t s) {
   if (a.n_rows <= 0) return cudaSuccess;
+  // the key table holds cache rows as int32
+  const int64_t rows = c.page_size ? (int64_t)c.num_pages * c.page_size : (int64_t)c.batch * c.max_len;
+  if (rows > 0x7FFFFFFFll) return cudaErrorInvalidValue;
   AttnParams p;
   p.q = a.q;
   p.heads = a.heads;
@@ -919,8 +966,8 @@ cudaError_t launch_attention(const csa2_cache& c, const AttnArgs& a, const WsLay
   p.out = a.out;
   int splits = num_sms / a.n_rows;
   splits = splits < 1 ? 1 : (splits > kMaxSplits ? kMaxSplits : splits);
-  const int max_chunks = (a.kcap + a.window + 63) / 64;
-  if (splits > max_chunks) splits = max_chunks < 1 ? 1 : max_chunks;
+  const int max_tiles = (a.kcap + a.window + kTile - 1) / kTile;
+  if (splits > max_tiles) splits = max_tiles < 1 ? 1 : max_tiles;
   p.splits = splits;
   p.codes = c.kv_codes;
   p.scales = c.kv_scales;

@@ -1,7 +1,7 @@
 """bench.py --impl reference: the oracle arm prints one JSON line with the
-GPU arm's metric, unit and config keys, times every piece of a sequence's
-layer-step, and stays within its time budget; workloads it does not cover
-print an `unavailable` line."""
+GPU arm's metric, unit and config keys, times every piece of a layer-step,
+reports the measured wall time per step, and stays within its time budget,
+for decode, multi-query and ragged mixed-mode workloads."""
 import json
 import os
 import subprocess
@@ -35,6 +35,18 @@ def test_reference_arm_line_on_the_tiny_decode():
     assert wall < 300
 
 
-def test_reference_arm_unavailable_for_multi_query_workloads():
-    d, _ = run_ref("--workload", "6", "--steps", "2", "--warmup", "0")
-    assert d["impl"] == "reference" and "unavailable" in d
+def test_reference_arm_multi_query_workload():
+    d, wall = run_ref("--workload", "6", "--steps", "3", "--warmup", "0")
+    assert d["impl"] == "reference" and "unavailable" not in d
+    assert d["metric"].startswith("CSA2 multi-query layer-steps/s")
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["layer_step_ms_estimated"] > 0
+    assert d["config"]["tokens_per_step"] == 32 * 5
+    assert wall < 300
+
+
+def test_reference_arm_ragged_mixed_modes():
+    d, wall = run_ref("--workload", "5", "--steps", "4", "--warmup", "0")
+    assert d["impl"] == "reference" and d["value"] > 0
+    sample = d["cpu_baseline"]["sample"]
+    assert "Full:" in sample and "Reindex:" in sample and "Reuse:" in sample
+    assert wall < 400
