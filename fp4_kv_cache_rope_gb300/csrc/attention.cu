@@ -41,12 +41,13 @@
 //        product lands: thread (key j = 32 (warp % 4) + lane, heads
 //        32 (warp / 4) .. +32).  The running maximum per head is raised
 //        lazily: only when a logit exceeds it by more than 2^8 (then O^T
-//        and the sums are rescaled in place); the raw bytes of the next
-//        tile's keys are loaded into registers one tile ahead.
+//        and the sums are rescaled in place).  A tile's raw bytes are read
+//        (from L2) when its dequantisation starts, while PV of the previous
+//        tile still holds the first slab pair.
 //   8    MMA issuer (lane 0) and tensor-memory owner.
 //   9    index warp: turns the tile's index entries into cache rows (page
-//        table, bounds checks) up to four tiles ahead, and copies the query
-//        rows in.
+//        table, bounds checks) up to four tiles ahead and prefetches those
+//        rows from HBM into L2, so the compute warps' reads hit L2.
 #include "codec.cuh"
 #include "launch.h"
 
@@ -81,11 +82,22 @@ struct AttnCfg {
   static constexpr int kKtab = 3584;             // int32 [kKtSlots][kTile] key table
   static constexpr int kMiscBytes = kKtab + kKtSlots * kTile * 4;
   static constexpr int kSmem = kMiscOff + kMiscBytes;
-  static constexpr int kItems = (kTile * NSLAB + kComputeThreads - 1) / kComputeThreads;
-  // tensor memory: S^T x2 (128 columns), O^T (64 NT), the softmax sums (64)
-  static constexpr int kLCol = 128 + 64 * NT;
-  static constexpr int kTmemCols = kLCol + 64 <= 256 ? 256 : 512;
-  static_assert(kLCol + 64 <= 512, "tensor memory columns");
+  // Dequantisation items (key, 64-channel slab), laid out so that the 32
+  // lanes of a warp take kSG consecutive slabs of 32/kSG consecutive keys:
+  // each key's lanes read contiguous bytes of its row (few L1 wavefronts per
+  // load), and the 16-byte stores into the swizzled slabs hit every bank
+  // group equally.  Slabs past the last full group of kSG are taken 32 keys
+  // at a time.
+  static constexpr int kSG = NSLAB >= 4 ? 4 : NSLAB;
+  static constexpr int kKPG = 32 / kSG;                       // keys per group
+  static constexpr int kNFull = NSLAB / kSG;                  // full slab groups
+  static constexpr int kKG = kTile / kKPG;                    // key groups
+  static constexpr int kFullItems = kNFull * kKG * 32;
+  static constexpr int kAllItems = kFullItems + (NSLAB - kNFull * kSG) * 128;
+  static constexpr int kItems = (kAllItems + kComputeThreads - 1) / kComputeThreads;
+  static_assert(kTile % kKPG == 0 && kTile <= 128, "item layout");
+  // tensor memory: S^T x2 (128 columns), then O^T (64 NT)
+  static constexpr int kTmemCols = 128 + 64 * NT <= 256 ? 256 : 512;
   static_assert(kSmem <= 227 * 1024, "attention: shared memory");
   static_assert((kXSlab % 1024) == 0 && (kQOff % 1024) == 0 && (kPOff % 1024) == 0,
                 "128-byte swizzle atoms need 1024-byte aligned slabs");
@@ -231,15 +243,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
-__device__ __forceinline__ void tmem_st16z(uint32_t taddr) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,"
-      "%1,%1};" ::"r"(taddr), "r"(0u)
-      : "memory");
-}
 __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// Brings [p, p + bytes) from HBM into L2, one prefetch per 64 bytes (the
+// L2's fetch unit from HBM), each at an address inside the range (fire and
+// forget: nothing waits for them).
+__device__ __forceinline__ void prefetch_l2(const uint8_t* p, uint32_t bytes) {
+  for (uint32_t o = 0; o < bytes; o += 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o));
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p + bytes - 1));
 }
 
 __device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v) {
@@ -251,30 +265,31 @@ __device__ __forceinline__ uint32_t map_to_rank(const void* p, int rank) {
   return r;
 }
 
-// f16 copy of the query rows [heads x D] (bf16, at qs) into the swizzled Q
-// slabs by the compute threads (thread t of 256), assuming no head needs
-// scaling; returns, over the compute warps, whether some |q| >= 2^14 (then
-// the copy is redone with a power-of-two scale per head).  Rows past `heads`
-// are zero.
+// f16 copy of the query rows [heads x D] (bf16 in global memory at qs) into
+// the swizzled Q slabs by the compute threads (thread t of 256), every load
+// in flight at once, assuming no head needs scaling; returns, over the
+// compute warps, whether some |q| >= 2^14 (then the copy is redone with a
+// power-of-two scale per head).  Rows past `heads` are zero.
 template <int NSLAB>
-__device__ __forceinline__ bool convert_query(const uint8_t* qs, uint8_t* sq, int t, bool ok,
-                                              int heads) {
+__device__ __forceinline__ bool convert_query(const uint8_t* qs, uint8_t* sq, int t, int heads) {
   constexpr int D = NSLAB * 64;
   constexpr int kChunks = D / 8;     // 16-byte chunks per head row
   constexpr int kAll = 64 * kChunks;
   constexpr int kQSlab = 64 * 128;
   constexpr int n = kComputeThreads;
+  constexpr int kBatch = 6;            // loads in flight per thread and round
   bool big = false;
-  for (int i0 = t; i0 < kAll; i0 += 4 * n) {
-    uint4 v[4];
+  for (int i0 = t; i0 < kAll; i0 += kBatch * n) {
+    constexpr int kPer = kBatch;
+    uint4 v[kPer];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kPer; ++u) {
       const int i = i0 + n * u;
-      v[u] = (ok && i < kAll && i / kChunks < heads) ? *reinterpret_cast<const uint4*>(qs + i * 16)
-                                                     : make_uint4(0, 0, 0, 0);
+      v[u] = (i < kAll && i / kChunks < heads) ? __ldg(reinterpret_cast<const uint4*>(qs) + i)
+                                               : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kPer; ++u) {
       const int i = i0 + n * u;
       if (i >= kAll) break;
       const int h = i / kChunks, c = i - h * kChunks;
@@ -292,6 +307,80 @@ __device__ __forceinline__ bool convert_query(const uint8_t* qs, uint8_t* sq, in
     }
   }
   return named_sync_or(1, kComputeThreads, big);
+}
+
+// Raises the running maximum of every head to cover the current tile (the
+// softmax warps' rare path; uniform over them): the tile's maximum per head
+// from this thread's logits sr (key slot of lane, heads 32 hf ..) through the
+// warps' maxima in tmax, the sums l and, past the first tile, the O^T columns
+// rescaled by 2^(m_old - m_new) once PV of the previous tile is complete,
+// and the new maxima written to mrow.
+template <int NT>
+__device__ __noinline__ void raise_running_max(const uint32_t* sr, float* l, bool valid, int i,
+                                               const float* qmul, float* mrow, float* tmax, int quad,
+                                               int hf, int lane, uint32_t tO, uint32_t lane_base,
+                                               uint64_t* pvt, volatile int* abort_flag, bool& ok) {
+  const int hh = 32 * hf + lane;   // the head this lane publishes
+  float mine = -INFINITY;
+#pragma unroll
+  for (int h = 0; h < 32; ++h) {
+    const float x = valid ? __uint_as_float(sr[h]) * qmul[32 * hf + h] : -INFINITY;
+    const float r = warp_max(x);
+    mine = lane == h ? r : mine;
+  }
+  tmax[quad * 64 + hh] = mine;
+  named_sync(3, kComputeThreads);
+  const float m_old = mrow[hh];
+  const float m_new = fmaxf(fmaxf(m_old, fmaxf(tmax[hh], tmax[64 + hh])),
+                            fmaxf(tmax[128 + hh], tmax[192 + hh]));
+  const float alpha = m_old == -INFINITY ? (m_new == -INFINITY ? 1.0f : 0.0f)
+                                         : fast_exp2(m_old - m_new);
+#pragma unroll
+  for (int h = 0; h < 32; ++h) l[h] *= __shfl_sync(0xffffffffu, alpha, h);
+  if (i > 0) {
+    // O^T *= alpha per head column, once PV of tile i-1 is complete (PV of
+    // this tile waits for the softmax warps' p_full arrivals)
+    if (ok && !mbar_wait(pvt + NT - 1, (i - 1) & 1, abort_flag)) ok = false;
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    if (ok) {
+#pragma unroll 1
+      for (int t2 = 0; t2 < 2 * NT; ++t2) {
+        uint32_t v[16];
+        const int hb = 16 * (t2 & 1);
+        const uint32_t a = tO + lane_base + 64 * (t2 >> 1) + 32 * hf + hb;
+        tmem_ld16(a, v);
+        tmem_ld_wait();
+        reg_fence(v);
+#pragma unroll
+        for (int h = 0; h < 16; ++h)
+          v[h] = __float_as_uint(__uint_as_float(v[h]) * __shfl_sync(0xffffffffu, alpha, hb + h));
+        tmem_st16(a, v);
+      }
+      tmem_st_wait();
+    }
+  }
+  named_sync(3, kComputeThreads);   // every thread has read mrow and tmax
+  if (quad == 0) mrow[hh] = m_new;
+  named_sync(3, kComputeThreads);   // the new maxima are in mrow
+}
+
+// Key slot jj and slab s of dequantisation item `it` (see AttnCfg); false
+// for the unused slots of the last partial group.
+template <int NSLAB>
+__device__ __forceinline__ bool item_of(int it, int& jj, int& s) {
+  using C = AttnCfg<NSLAB>;
+  if (it < C::kFullItems) {
+    const int g = it >> 5, l = it & 31;
+    const int kg = g % C::kKG, sg = g / C::kKG;
+    jj = C::kKPG * kg + l % C::kKPG;
+    s = C::kSG * sg + l / C::kKPG;
+    return true;
+  }
+  const int it2 = it - C::kFullItems;
+  jj = it2 & 127;
+  s = C::kNFull * C::kSG + (it2 >> 7);
+  return it2 < C::kAllItems - C::kFullItems && jj < kTile;
 }
 
 // Raw bytes of one (key, 64-channel slab) item: FP4 codes (32 B in a, b) and
@@ -313,7 +402,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc + C::kBars);
   uint64_t* s_full = bars + 0;             // [2] QK of the tile landed (commit)
   uint64_t* p_full = bars + 2;             // softmax weights written (8 warps)
-  uint64_t* q_full = bars + 3;             // query rows copied in (bulk copy)
   uint64_t* q_ready = bars + 4;            // f16 query slabs written (8 warps)
   uint64_t* drain = bars + 5;
   uint64_t* xg = bars + 6;                 // [NT] X slab pair t of the tile written (8 warps)
@@ -341,7 +429,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
     mbar_init(s_full + 0, 1);
     mbar_init(s_full + 1, 1);
     mbar_init(p_full, 8);
-    mbar_init(q_full, 1);
     mbar_init(q_ready, 8);
     mbar_init(drain, 1);
     for (int t = 0; t < NT; ++t) {
@@ -376,22 +463,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
     const int quad = warp & 3, hf = warp >> 2;
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const int j = 32 * quad + lane;   // softmax: this thread's key slot
-    RawItem raw[C::kItems];
-    uint32_t kinds = 0;               // 2 bits per item: 0 zero row, 1 FP4 row, 2 FP8 window row
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       if (ok && !mbar_wait(bar, parity, abort_flag)) ok = false;
       ok = __all_sync(0xffffffffu, ok);
     };
     // raw bytes of tile i's keys for this thread's items
-    auto load_raw = [&](int i) {
+    auto load_raw = [&](int i, RawItem (&raw)[C::kItems], uint32_t& kinds) {
       const int32_t* tab = ktab + (i % kKtSlots) * kTile;
       const int nk = ck.tile_keys(i);
       kinds = 0;
 #pragma unroll
       for (int u = 0; u < C::kItems; ++u) {
-        const int it = ct + kComputeThreads * u;
-        if (ok && it < kTile * NSLAB) {
-          const int jj = it % kTile, s = it / kTile;
+        int jj, s;
+        if (ok && item_of<NSLAB>(ct + kComputeThreads * u, jj, s)) {
           const int v = jj < nk ? tab[jj] : -1;
           if (v >= 0) {
             const uint8_t* cp = p.codes + (int64_t)v * p.code_stride + s * 32;
@@ -410,16 +494,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
         }
       }
     };
-    // ---- tile 0's table and raw bytes, requested before the query copy lands
-    if (ck.ntile > 0) {
-      wait_all(kt_full, 0);
-      load_raw(0);
-    }
-    // ---- query: f16 copy of the bf16 rows (staged in the X slabs).  When some
-    // |q| >= 2^14, each head is redone scaled by a power of two so that its
-    // f16 copy stays exact (the logit factor absorbs the power).
-    wait_all(q_full, 0);
-    if (!convert_query<NSLAB>(sx, sq, ct, ok, p.heads)) {
+    // ---- query: f16 copy of the bf16 rows.  When some |q| >= 2^14, each
+    // head is redone scaled by a power of two so that its f16 copy stays
+    // exact (the logit factor absorbs the power).
+    const uint8_t* qg = reinterpret_cast<const uint8_t*>(p.q + (int64_t)row * p.heads * D);
+    if (!convert_query<NSLAB>(qg, sq, ct, p.heads)) {
       if (ct < 64) qmul[ct] = ct < p.heads ? p.scale_log2 : 0.0f;
     } else {
       constexpr int kChunks = D / 8;
@@ -432,8 +511,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
         for (int i = 0; i < kPer; ++i) {
           const int c = lane + 32 * i;
           v[i] = make_uint4(0, 0, 0, 0);
-          if (ok && h < p.heads && c < kChunks)
-            v[i] = *reinterpret_cast<const uint4*>(sx + (h * D + c * 8) * 2);
+          if (h < p.heads && c < kChunks)
+            v[i] = __ldg(reinterpret_cast<const uint4*>(qg + (h * D + c * 8) * 2));
           const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -465,29 +544,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
       }
     }
     fence_async_smem();
-    named_sync(1, kComputeThreads);  // Q slabs and qmul written; the staging area is free
+    named_sync(1, kComputeThreads);  // Q slabs and qmul written
     if (lane == 0) mbar_arrive(q_ready);
 
-    // Partial softmax denominators of this key slot and heads 32 hf .. +32
-    // live in tensor memory (lane j, columns kLCol + 32 hf ..), not registers.
-    const uint32_t tl = tmem + lane_base + C::kLCol + 32 * hf;
-    tmem_st16z(tl);
-    tmem_st16z(tl + 16);
-    tmem_st_wait();
+    float l[32];  // partial softmax denominators: this key slot, heads 32 hf + h
+#pragma unroll
+    for (int h = 0; h < 32; ++h) l[h] = 0.0f;
 
+    // Raw bytes of the tile to dequantise next, loaded one tile ahead (right
+    // after the previous dequantisation), so that their latency is hidden
+    // behind that tile's QK product, softmax and PV product.
+    RawItem raw[C::kItems];
+    uint32_t kinds = 0;
+    if (ck.ntile > 0) {
+      wait_all(kt_full, 0);
+      load_raw(0, raw, kinds);
+    }
     for (int i = 0; i < ck.ntile; ++i) {
-      // ---- dequantise tile i, slab pair by slab pair: pair t is free once PV
-      // of tile i-1 has finished with accumulator tile t
       const int nk = ck.tile_keys(i);
-      for (int t = 0; t < NT; ++t) {
-        if (i > 0) wait_all(pvt + t, (i - 1) & 1);
+      // ---- dequantise tile i, four slabs at a time (a warp's items cover
+      // four consecutive slabs): slabs 4q .. 4q+3 are free once PV of tile
+      // i-1 has finished with accumulator tiles 2q and 2q+1
+      for (int q = 0; 2 * q < NT; ++q) {
+        const bool two = 2 * q + 1 < NT;
+        if (i > 0) {
+          wait_all(pvt + 2 * q, (i - 1) & 1);
+          if (two) wait_all(pvt + 2 * q + 1, (i - 1) & 1);
+        }
         if (ok) {
 #pragma unroll
           for (int u = 0; u < C::kItems; ++u) {
-            const int it = ct + kComputeThreads * u;
-            if (it >= kTile * NSLAB) continue;
-            const int jj = it % kTile, s = it / kTile;
-            if ((s >> 1) != t) continue;
+            int jj, s;
+            if (!item_of<NSLAB>(ct + kComputeThreads * u, jj, s) || (s >> 2) != q) continue;
             uint8_t* slab = sx + s * C::kXSlab;
             const uint32_t kind = (kinds >> (2 * u)) & 3u;
             if (kind == 1) {
@@ -525,12 +613,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
         }
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(xg + t);
+        if (lane == 0) {
+          mbar_arrive(xg + 2 * q);
+          if (two) mbar_arrive(xg + 2 * q + 1);
+        }
       }
-      // ---- the next tile's raw bytes, one tile ahead
+      // ---- the next tile's raw bytes
       if (i + 1 < ck.ntile) {
         wait_all(kt_full + ((i + 1) % kKtSlots), ((i + 1) / kKtSlots) & 1);
-        load_raw(i + 1);
+        load_raw(i + 1, raw, kinds);
       }
       // ---- softmax of tile i
       wait_all(s_full + (i & 1), (i >> 1) & 1);
@@ -543,104 +634,65 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
       }
       const int32_t* tab = ktab + (i % kKtSlots) * kTile;
       const bool valid = ok && j < nk && tab[j] != -1;
+      const float4* qm4 = reinterpret_cast<const float4*>(qmul + 32 * hf);
+      const float4* mr4 = reinterpret_cast<const float4*>(mrow + 32 * hf);
       float vmax = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < 32; ++h) {
-        const float x = __uint_as_float(sr[h]) * qmul[32 * hf + h] - mrow[32 * hf + h];
-        vmax = fmaxf(vmax, valid ? x : -INFINITY);
+      for (int h4 = 0; h4 < 8; ++h4) {
+        const float4 q = qm4[h4], m = mr4[h4];
+        vmax = fmaxf(vmax, __uint_as_float(sr[4 * h4]) * q.x - m.x);
+        vmax = fmaxf(vmax, __uint_as_float(sr[4 * h4 + 1]) * q.y - m.y);
+        vmax = fmaxf(vmax, __uint_as_float(sr[4 * h4 + 2]) * q.z - m.z);
+        vmax = fmaxf(vmax, __uint_as_float(sr[4 * h4 + 3]) * q.w - m.w);
       }
+      if (!valid) vmax = -INFINITY;
       // raise the running maximum when a logit exceeds it by more than 2^8
-      // (always on the first tile); uniform over the compute warps.  Lane h
-      // keeps the old and new maximum of head 32 hf + h.
-      const int hh = 32 * hf + lane;
-      float m_old = 0.0f, m_new = 0.0f;
-      const bool raise = named_sync_or(2, kComputeThreads, vmax > 8.0f);
-      if (raise) {
-        float mine = -INFINITY;
+      // (always on the first tile); uniform over the compute warps.  On that
+      // rare path S^T is read again from tensor memory afterwards, so that
+      // its registers are free while O^T and the sums are rescaled.
+      if (named_sync_or(2, kComputeThreads, vmax > 8.0f)) {
+        // (out of line, so that the rare path's registers do not weigh on
+        // the main loop; S^T is read again afterwards)
+        float lt[32];   // copies: only these have their address taken
+        uint32_t st[32];
 #pragma unroll
         for (int h = 0; h < 32; ++h) {
-          const float x = valid ? __uint_as_float(sr[h]) * qmul[32 * hf + h] : -INFINITY;
-          const float r = warp_max(x);
-          mine = lane == h ? r : mine;
+          lt[h] = l[h];
+          st[h] = sr[h];
         }
-        tmax[quad * 64 + hh] = mine;
-        named_sync(3, kComputeThreads);
-        m_old = mrow[hh];
-        m_new = fmaxf(fmaxf(m_old, fmaxf(tmax[hh], tmax[64 + hh])),
-                      fmaxf(tmax[128 + hh], tmax[192 + hh]));
+        raise_running_max<NT>(st, lt, valid, i, qmul, mrow, tmax, quad, hf, lane, tO, lane_base,
+                              pvt, abort_flag, ok);
 #pragma unroll
-        for (int hb = 0; hb < 32; hb += 16) {
-          uint32_t lv[16];
-          tmem_ld16(tl + hb, lv);
+        for (int h = 0; h < 32; ++h) l[h] = lt[h];
+        tc_fence_after();
+        if (ok) {
+          tmem_ld32(tmem + lane_base + 64 * (i & 1) + 32 * hf, sr);
           tmem_ld_wait();
-          reg_fence(lv);
-#pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            const float mo = __shfl_sync(0xffffffffu, m_old, hb + h);
-            const float mn = __shfl_sync(0xffffffffu, m_new, hb + h);
-            const float al = mo == -INFINITY ? (mn == -INFINITY ? 1.0f : 0.0f) : fast_exp2(mo - mn);
-            lv[h] = __float_as_uint(__uint_as_float(lv[h]) * al);
-          }
-          tmem_st16(tl + hb, lv);
+          reg_fence32(sr);
         }
-        tmem_st_wait();
-        named_sync(3, kComputeThreads);   // every thread has read mrow and tmax
-        if (quad == 0) mrow[hh] = m_new;
-        named_sync(3, kComputeThreads);   // the new maxima are in mrow
       }
       // weights p = 2^(logit - m), rounded to f16, summed as rounded; this
       // key's row of P^T, 8 heads (16 bytes) at a time
 #pragma unroll
-      for (int hb = 0; hb < 32; hb += 16) {
-        uint32_t lv[16];
-        tmem_ld16(tl + hb, lv);
-        tmem_ld_wait();
-        reg_fence(lv);
+      for (int u = 0; u < 4; ++u) {
+        uint32_t pk[4];
+        const float4 qa = qm4[2 * u], qb = qm4[2 * u + 1], ma = mr4[2 * u], mb = mr4[2 * u + 1];
+        const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int h = hb + 8 * u + 2 * e;
-            const float x0 = __uint_as_float(sr[h]) * qmul[32 * hf + h] - mrow[32 * hf + h];
-            const float x1 = __uint_as_float(sr[h + 1]) * qmul[32 * hf + h + 1] - mrow[32 * hf + h + 1];
-            const float e0 = valid ? fast_exp2(x0) : 0.0f;
-            const float e1 = valid ? fast_exp2(x1) : 0.0f;
-            const __half2 ph = __floats2half2_rn(e0, e1);
-            const float2 pf = __half22float2(ph);
-            lv[h - hb] = __float_as_uint(__uint_as_float(lv[h - hb]) + pf.x);
-            lv[h - hb + 1] = __float_as_uint(__uint_as_float(lv[h - hb + 1]) + pf.y);
-            pk[e] = *reinterpret_cast<const uint32_t*>(&ph);
-          }
-          if (j < kTile) st_swz(sp, j, (4 * hf + (hb >> 3) + u), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+        for (int e = 0; e < 4; ++e) {
+          const int h = 8 * u + 2 * e;
+          const float x0 = __uint_as_float(sr[h]) * qv[2 * e] - mv[2 * e];
+          const float x1 = __uint_as_float(sr[h + 1]) * qv[2 * e + 1] - mv[2 * e + 1];
+          const float e0 = valid ? fast_exp2(x0) : 0.0f;
+          const float e1 = valid ? fast_exp2(x1) : 0.0f;
+          const __half2 ph = __floats2half2_rn(e0, e1);
+          const float2 pf = __half22float2(ph);
+          l[h] += pf.x;
+          l[h + 1] += pf.y;
+          pk[e] = *reinterpret_cast<const uint32_t*>(&ph);
         }
-        tmem_st16(tl + hb, lv);
-      }
-      tmem_st_wait();
-      if (raise && i > 0) {
-        // O^T *= 2^(m_old - m_new) per head column, once PV of tile i-1 is
-        // complete (before PV of this tile, which waits for p_full)
-        wait_all(pvt + NT - 1, (i - 1) & 1);
-        tc_fence_after();
-        if (ok) {
-#pragma unroll 1
-          for (int t = 0; t < NT; ++t) {
-            uint32_t v[32];
-            const uint32_t a = tO + lane_base + 64 * t + 32 * hf;
-            tmem_ld32(a, v);
-            tmem_ld_wait();
-            reg_fence32(v);
-#pragma unroll
-            for (int h = 0; h < 32; ++h) {
-              const float mo = __shfl_sync(0xffffffffu, m_old, h);
-              const float mn = __shfl_sync(0xffffffffu, m_new, h);
-              const float al = mo == -INFINITY ? (mn == -INFINITY ? 1.0f : 0.0f) : fast_exp2(mo - mn);
-              v[h] = __float_as_uint(__uint_as_float(v[h]) * al);
-            }
-            tmem_st32(a, v);
-          }
-          tmem_st_wait();
-        }
+        if (j < kTile) st_swz(sp, j, 4 * hf + u, make_uint4(pk[0], pk[1], pk[2], pk[3]));
       }
       fence_async_smem();
       tc_fence_before();
@@ -653,15 +705,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
     // ---- after the last tile: per-head denominators (sum over the key slots)
     if (ck.ntile > 0) wait_all(pvt + NT - 1, (ck.ntile - 1) & 1);
     tc_fence_after();
-    float l[32];
-    {
-      uint32_t lv[32];
-      tmem_ld32(tl, lv);
-      tmem_ld_wait();
-      reg_fence32(lv);
-#pragma unroll
-      for (int h = 0; h < 32; ++h) l[h] = __uint_as_float(lv[h]);
-    }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
       const bool upper = (lane & off) != 0;
@@ -685,7 +728,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
     if (lane == 0 && ck.ntile > 0) {
       constexpr uint32_t idesc_qk = instr_desc(0, 0, false, false, 128, 64);
       constexpr uint32_t idesc_pv = instr_desc(0, 0, true, true, 128, 64);
-      const uint32_t xb = smem_u32(sx), qb = smem_u32(sq), pb = smem_u32(sp);
+      // Descriptors are built once; an operand's descriptor at a byte offset
+      // o from its base is the base descriptor plus o/16 (the start-address
+      // field holds address/16 in its low 14 bits, and shared-memory
+      // addresses stay below 2^18).  This keeps the issue loop to one add
+      // per operand: the issuing thread shares its scheduler with two busy
+      // compute warps, and each MMA takes only ~50 cycles of tensor time.
+      const uint64_t qk_a = smem_desc(smem_u32(sx), 16, 1024, 2);
+      const uint64_t qk_b = smem_desc(smem_u32(sq), 16, 1024, 2);
+      const uint64_t pv_a = smem_desc(smem_u32(sx), C::kXSlab, 1024, 2);
+      const uint64_t pv_b = smem_desc(smem_u32(sp), C::kXSlab, 1024, 2);
       bool issued = false;
       ok = mbar_wait(q_ready, 0, abort_flag);
       for (int i = 0; ok && i < ck.ntile; ++i) {
@@ -693,15 +745,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
         for (int t = 0; t < NT; ++t) {
           if (!mbar_wait(xg + t, i & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
+          const uint64_t a_t = qk_a + (uint64_t)(t * (2 * C::kXSlab / 16));
+          const uint64_t b_t = qk_b + (uint64_t)(t * (2 * C::kQSlab / 16));
 #pragma unroll
           for (int s2 = 0; s2 < 2; ++s2) {
-            const int s = 2 * t + s2;
-            if (s >= NSLAB) break;
+            if (2 * t + s2 >= NSLAB) break;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_f16(sd, smem_desc(xb + s * C::kXSlab + kk * 32, 16, 1024, 2),
-                      smem_desc(qb + s * C::kQSlab + kk * 32, 16, 1024, 2), idesc_qk,
-                      (s | kk) != 0 ? 1u : 0u);
+              mma_f16(sd, a_t + (uint64_t)((s2 * C::kXSlab + kk * 32) / 16),
+                      b_t + (uint64_t)((s2 * C::kQSlab + kk * 32) / 16), idesc_qk,
+                      (t | s2 | kk) != 0 ? 1u : 0u);
           }
           issued = true;
         }
@@ -710,13 +763,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
         if (!mbar_wait(p_full, i & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const int nks = (ck.tile_keys(i) + 15) / 16;
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
         for (int t = 0; t < NT; ++t) {
           // A = X^T read channel-major: channels of slabs 2t, 2t+1 (for an odd
           // slab count the last tile's upper half falls on Q: unused rows)
-          for (int kk = 0; kk < nks; ++kk)
-            mma_f16(tO + 64 * t, smem_desc(xb + 2 * t * C::kXSlab + kk * 2048, C::kXSlab, 1024, 2),
-                    smem_desc(pb + kk * 2048, C::kXSlab, 1024, 2), idesc_pv,
-                    (i > 0 || kk > 0) ? 1u : 0u);
+          const uint64_t a_t = pv_a + (uint64_t)(t * (2 * C::kXSlab / 16));
+          const uint32_t d_t = tO + 64 * t;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            if (kk < nks)
+              mma_f16(d_t, a_t + (uint64_t)(kk * 2048 / 16), pv_b + (uint64_t)(kk * 2048 / 16),
+                      idesc_pv, kk > 0 ? 1u : acc0);
           mma_commit(pvt + t);
         }
       }
@@ -728,13 +785,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
     __syncwarp();
   } else {
     // ============================================================== index warp
-    if (lane == 0) {
-      // the query rows [H, D] bf16 are contiguous: one bulk copy into the X
-      // slabs, which hold no key before the query is converted
-      const uint32_t qbytes = (uint32_t)(p.heads * D * 2);
-      mbar_arrive_expect_tx(q_full, qbytes);
-      bulk_load(sx, p.q + (int64_t)row * p.heads * D, qbytes, q_full);
-    }
+    constexpr uint32_t kCodeBytes = D / 2;
+    constexpr uint32_t kScaleBytes = D / 16;
     for (int i = 0; i < ck.ntile; ++i) {
       const int slot = i % kKtSlots;
       if (i >= kKtSlots) {
@@ -763,13 +815,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
           if (l < ck.ng) {
             if (pos[u] >= 0 && pos[u] < rk.vis) {
               const int64_t r = p.map.row(rk.b, pos[u]);
-              if (r >= 0) v = (int)r;
-              else set_status(p.status, CSA2_DEV_BAD_PAGE);
+              if (r >= 0) {
+                v = (int)r;
+                prefetch_l2(p.codes + r * p.code_stride, kCodeBytes);
+                prefetch_l2(p.scales + r * p.scale_stride, kScaleBytes);
+              } else {
+                set_status(p.status, CSA2_DEV_BAD_PAGE);
+              }
             } else {
               set_status(p.status, CSA2_DEV_BAD_INDEX);
             }
           } else {
             v = -2 - (ck.w0 + l - ck.ng);
+            prefetch_l2(rk.swa0 + (int64_t)(ck.w0 + l - ck.ng) * D, (uint32_t)D);
           }
         }
         tab[jj] = v;
@@ -777,7 +835,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
       __syncwarp();
       if (lane == 0) mbar_arrive(kt_full + slot);
     }
-    if (lane == 0) mbar_wait_drain(q_full, 0);  // the query copy, if a wait gave up early
     __syncwarp();
   }
   tc_fence_before();
