@@ -1031,7 +1031,7 @@ cudaError_t launch_attention(const csa2_cache& c, const AttnArgs& a, const WsLay
   p.code_stride = c.code_stride;
   p.scale_stride = c.scale_stride;
   p.seq_len = c.seq_len;
-  p.map = RowMap{c.page_table, c.page_size, c.max_pages_per_seq, c.max_len, c.num_pages};
+  p.map = row_map_of(c);
   p.status = reinterpret_cast<uint32_t*>(ws + L.status);
   switch (c.dim / 64) {
     case 2: return run_attention<2>(p, s);

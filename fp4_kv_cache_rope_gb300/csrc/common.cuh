@@ -115,17 +115,34 @@ __device__ __forceinline__ float peer_f32(const void* p, int rank) {
 }
 
 // Physical cache row of (sequence b, position t); -1 when the page id is bad.
+// Positions are below max_len (an int32), so page arithmetic runs in 32 bits:
+// a shift for power-of-two page sizes, one unsigned division otherwise (a
+// 64-bit division is a long software sequence on the GPU).
 struct RowMap {
   const int32_t* page_table;
   int32_t page_size, max_pages_per_seq, max_len, num_pages;
+  int32_t page_shift;  // log2(page_size) when it is a power of two, else -1
+  __device__ __forceinline__ uint32_t page_of(uint32_t t) const {
+    return page_shift >= 0 ? t >> page_shift : t / (uint32_t)page_size;
+  }
+  __device__ __forceinline__ uint32_t in_page(uint32_t t) const {
+    return page_shift >= 0 ? t & (uint32_t)(page_size - 1) : t % (uint32_t)page_size;
+  }
   __device__ __forceinline__ int64_t row(int b, int64_t t) const {
     if (page_size == 0) return (int64_t)b * max_len + t;
-    int64_t pg = t / page_size;
+    const uint32_t pg = page_of((uint32_t)t);
     int32_t phys = page_table[(int64_t)b * max_pages_per_seq + pg];
     if (phys < 0 || phys >= num_pages) return -1;
-    return (int64_t)phys * page_size + (t - pg * page_size);
+    return (int64_t)phys * page_size + in_page((uint32_t)t);
   }
 };
+inline RowMap row_map_of(const csa2_cache& c) {
+  int32_t shift = -1;
+  if (c.page_size > 0 && (c.page_size & (c.page_size - 1)) == 0)
+    for (shift = 0; (1 << shift) < c.page_size; ++shift) {
+    }
+  return RowMap{c.page_table, c.page_size, c.max_pages_per_seq, c.max_len, c.num_pages, shift};
+}
 
 // ------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -320,154 +320,154 @@ __global__ void __launch_bounds__(192, kIdxCtasPerSm)
   bool issued_mma = false;
 
   if (t_begin < t_end) {
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
       // ------------------------------------------------------ TMA producer
+      // The whole warp runs the loop.  Lane 0 waits on the ring and arms its
+      // barriers; each lane issues the copies of the units it owns, so the
+      // page-table lookups of a tile run in parallel.  On a paged cache the
+      // lanes also hold a window of the row's page-table entries (pages
+      // wb .. wb+63, two per lane), refilled 32 pages ahead of use: a lookup
+      // that waits for memory in every tile would bound the scan, because the
+      // copies of randomly placed pages keep address translation busy.
+      const bool leader = lane == 0;
+      auto wait_bcast = [&](uint64_t* bar, uint32_t parity) -> bool {
+        int ok = 0;
+        if (leader) ok = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
+        return __shfl_sync(0xffffffffu, ok, 0) != 0;
+      };
       RowCursor rc;
       rc.init(pre, lens, p.n_rows, t_begin);
       int qn = 0, stage = 0, armed = 0;
       uint32_t phase = 0;
       int b = row_seq(p, rc.row), tq = rc.row % p.tq;
+      int wseq = -1, wb = 0;          // sequence and first page of the window
+      int32_t wcur = -1, wnext = -1;  // entries wb + lane and wb + 32 + lane
+      const int mpp = p.map.max_pages_per_seq;
+      auto pt_entry = [&](int bb, int pg) -> int32_t {
+        return pg < mpp ? __ldg(p.map.page_table + (int64_t)bb * mpp + pg) : -1;
+      };
       for (int t = t_begin; t < t_end; ++t) {
         const bool fresh = rc.advance(p, t) || t == t_begin;
         if (fresh) {
           b = row_seq(p, rc.row);
           tq = rc.row % p.tq;
           const int qs = qn & 1;
-          if (!mbar_wait(qempty + qs, ((qn >> 1) & 1) ^ 1, abort_flag)) break;
-          mbar_arrive_expect_tx(qfull + qs, (uint32_t)(p.hi * DI));
-          tma_load_2d(qbuf + qs * C::kQBytes, &tm_q, 0, (int)(((int64_t)b * p.tq + tq) * p.hi),
-                      qfull + qs);
+          if (!wait_bcast(qempty + qs, ((qn >> 1) & 1) ^ 1)) break;
+          if (leader) {
+            mbar_arrive_expect_tx(qfull + qs, (uint32_t)(p.hi * DI));
+            tma_load_2d(qbuf + qs * C::kQBytes, &tm_q, 0, (int)(((int64_t)b * p.tq + tq) * p.hi),
+                        qfull + qs);
+          }
           ++qn;
         }
-        if (!mbar_wait(empty + stage, phase ^ 1, abort_flag)) break;
+        if (!wait_bcast(empty + stage, phase ^ 1)) break;
         const int j = t - rc.begin;
         const int len = rc.len;
         uint8_t* dst = stages + stage * C::kStageBytes;
-        uint32_t bytes = 0;
+        // this lane's unit of the tile: its first cache row (-1: none), the
+        // rows it copies and its scale bytes
+        int64_t src = -1;
+        int rows = 0;
+        uint32_t sf_bytes = 0;
+        int unit_rows = 0;
         if (p.mode == 0) {
-          const int64_t t0 = (int64_t)j * 128;
+          const int t0 = j * 128;
           if (p.map.page_size == 0) {
-            const int64_t r0 = (int64_t)b * p.map.max_len + t0;
-            bytes = 128 * C::kKRowBytes;
-            uint32_t sf_bytes = 0;
-            if (MX) {  // the tile's scale rows, cut at the end of the sequence
-              const int64_t n = p.map.max_len - t0 < 128 ? p.map.max_len - t0 : 128;
-              sf_bytes = (uint32_t)(4 * n);
+            if (leader) {
+              src = (int64_t)b * p.map.max_len + t0;
+              rows = 128;
+              if (MX) {  // the tile's scale rows, cut at the end of the sequence
+                const int n = p.map.max_len - t0 < 128 ? p.map.max_len - t0 : 128;
+                sf_bytes = (uint32_t)(4 * n);
+              }
             }
-            mbar_arrive_expect_tx(full + stage, bytes + sf_bytes);
-            tma_load_2d(dst, &tm_k, 0, (int)r0, full + stage);
-            if (MX) bulk_load(sfbuf + stage * C::kSfTileBytes, p.idx_scales + 4 * r0, sf_bytes,
-                              full + stage);
+            unit_rows = 128;
           } else {
             const int rpl = p.rows_per_load;
-            const int nu = 128 / rpl;
-            int nload = 0;
-            int64_t src_rows[16];
-            // the units' page-table entries, all requested before any is used
-            const int32_t* pt = p.map.page_table + (int64_t)b * p.map.max_pages_per_seq;
-            int32_t phys[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const int64_t pg = (t0 + (int64_t)u * rpl) / p.map.page_size;
-              phys[u] = u < nu ? __ldg(pt + (pg < p.map.max_pages_per_seq ? pg : p.map.max_pages_per_seq - 1))
-                               : -1;
+            const int nu = 128 / rpl;  // units of the tile: pages pg0 .. pg0 + nu - 1
+            const int pg0 = (int)p.map.page_of((uint32_t)t0);
+            if (b != wseq || pg0 < wb || pg0 >= wb + 64) {
+              wseq = b;
+              wb = pg0;
+              wcur = pt_entry(b, wb + lane);
+              wnext = pt_entry(b, wb + 32 + lane);
+            } else if (pg0 >= wb + 32) {
+              wb += 32;
+              wcur = wnext;
+              wnext = pt_entry(b, wb + 32 + lane);
             }
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const int64_t pos = t0 + (int64_t)u * rpl;
-              src_rows[u] = -1;
-              if (u < nu && pos < len) {
-                if (phys[u] < 0 || phys[u] >= p.map.num_pages) {
-                  set_status(p.status, CSA2_DEV_BAD_PAGE);
-                } else {
-                  src_rows[u] = (int64_t)phys[u] * p.map.page_size + pos % p.map.page_size;
-                  ++nload;
-                }
+            const int idx = pg0 + lane - wb;  // < 64 for the lanes that own a unit
+            const int32_t e_cur = __shfl_sync(0xffffffffu, wcur, idx & 31);
+            const int32_t e_next = __shfl_sync(0xffffffffu, wnext, idx & 31);
+            const int32_t phys = idx < 32 ? e_cur : e_next;
+            const int pos = t0 + lane * rpl;
+            if (lane < nu && pos < len) {
+              if (phys < 0 || phys >= p.map.num_pages) {
+                set_status(p.status, CSA2_DEV_BAD_PAGE);
+              } else {
+                src = (int64_t)phys * p.map.page_size + p.map.in_page((uint32_t)pos);
+                rows = rpl;
+                sf_bytes = MX ? (uint32_t)(rpl * 4) : 0u;
               }
             }
-            bytes = (uint32_t)(nload * rpl * (C::kKRowBytes + (MX ? 4 : 0)));
-            mbar_arrive_expect_tx(full + stage, bytes);
-            for (int u = 0; u < 128 / rpl; ++u)
-              if (src_rows[u] >= 0) {
-                tma_load_2d(dst + u * rpl * DI, &tm_k, 0, (int)src_rows[u], full + stage);
-                if (MX)
-                  bulk_load(sfbuf + stage * C::kSfTileBytes + u * rpl * 4,
-                            p.idx_scales + 4 * src_rows[u], (uint32_t)(rpl * 4), full + stage);
-              }
+            unit_rows = rpl;
           }
         } else {
           int pc = p.pool_cnt[(int64_t)b * p.tq + tq];
           pc = pc < 0 ? 0 : (pc > kPoolBlocks ? kPoolBlocks : pc);
           const int32_t* pool = p.pool_blocks + ((int64_t)b * p.tq + tq) * kPoolBlocks;
-          // the tile's 16 block ids, then (paged caches) their page-table
-          // entries, each as 16 loads in flight at once: loads issued one
-          // after another behind their checks would cost one L2 round trip
-          // each (clamped indices keep every load inside its array)
-          int blk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int pi = j * 16 + e;
-            blk[e] = __ldg(pool + (pi < kPoolBlocks ? pi : kPoolBlocks - 1));
-          }
-          int32_t phys[16];
-          if (p.map.page_size != 0) {
-            const int32_t* pt = p.map.page_table + (int64_t)b * p.map.max_pages_per_seq;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int64_t pg = (int64_t)(blk[e] > 0 ? blk[e] : 0) * kBlock / p.map.page_size;
-              phys[e] = __ldg(pt + (pg < p.map.max_pages_per_seq ? pg : p.map.max_pages_per_seq - 1));
-            }
-          }
-          int64_t src_rows[16];
-          int nload = 0;
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            src_rows[e] = -1;
-            if (j * 16 + e < pc) {
-              const int64_t t0b = (int64_t)blk[e] * kBlock;
-              if (blk[e] < 0 || t0b >= len) {
-                set_status(p.status, CSA2_DEV_BAD_POOL);
-              } else if (p.map.page_size == 0) {
-                src_rows[e] = (int64_t)b * p.map.max_len + t0b;
-                ++nload;
-              } else if (phys[e] < 0 || phys[e] >= p.map.num_pages) {
+          // lane e < 16 owns the tile's pool block e: its id, then (paged
+          // caches) its page-table entry; clamped indices keep every load
+          // inside its array
+          const int pi = j * 16 + lane;
+          if (lane < 16 && pi < pc) {
+            const int blk = __ldg(pool + (pi < kPoolBlocks ? pi : kPoolBlocks - 1));
+            const int64_t t0b = (int64_t)blk * kBlock;
+            if (blk < 0 || t0b >= len) {
+              set_status(p.status, CSA2_DEV_BAD_POOL);
+            } else if (p.map.page_size == 0) {
+              src = (int64_t)b * p.map.max_len + t0b;
+            } else {
+              const uint32_t pg = p.map.page_of((uint32_t)t0b);
+              const int32_t phys = pt_entry(b, (int)pg);
+              if (phys < 0 || phys >= p.map.num_pages)
                 set_status(p.status, CSA2_DEV_BAD_PAGE);
-              } else {
-                src_rows[e] = (int64_t)phys[e] * p.map.page_size + t0b % p.map.page_size;
-                ++nload;
+              else
+                src = (int64_t)phys * p.map.page_size + p.map.in_page((uint32_t)t0b);
+            }
+            if (src >= 0) {
+              rows = kBlock;
+              // scale rows of a block, cut at the last physical row (a block
+              // may run past the end of the sequence's rows; the key box is
+              // clipped by the tensor map, the scale copy here)
+              if (MX) {
+                const int64_t n = p.phys_rows - src;
+                sf_bytes = (uint32_t)(4 * (n < kBlock ? n : kBlock));
               }
             }
           }
-          // scale rows of a block, cut at the last physical row (a block may
-          // run past the end of the sequence's rows; the key box is clipped
-          // by the tensor map, the scale copy here)
-          uint32_t sf_n[16];
-          uint32_t sf_total = 0;
-          for (int e = 0; e < 16; ++e) {
-            sf_n[e] = 0;
-            if (MX && src_rows[e] >= 0) {
-              const int64_t n = p.phys_rows - src_rows[e];
-              sf_n[e] = (uint32_t)(n < kBlock ? n : kBlock);
-              sf_total += 4 * sf_n[e];
-            }
-          }
-          bytes = (uint32_t)(nload * kBlock * C::kKRowBytes) + sf_total;
-          mbar_arrive_expect_tx(full + stage, bytes);
-          for (int e = 0; e < 16; ++e)
-            if (src_rows[e] >= 0) {
-              tma_load_2d(dst + e * kBlock * DI, &tm_k, 0, (int)src_rows[e], full + stage);
-              if (MX)
-                bulk_load(sfbuf + stage * C::kSfTileBytes + e * kBlock * 4,
-                          p.idx_scales + 4 * src_rows[e], 4 * sf_n[e], full + stage);
-            }
+          unit_rows = kBlock;
+        }
+        uint32_t bytes = (uint32_t)(rows * C::kKRowBytes) + sf_bytes;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        if (leader) mbar_arrive_expect_tx(full + stage, bytes);
+        __syncwarp();
+        if (src >= 0) {
+          tma_load_2d(dst + lane * unit_rows * DI, &tm_k, 0, (int)src, full + stage);
+          if (MX && sf_bytes)
+            bulk_load(sfbuf + stage * C::kSfTileBytes + lane * unit_rows * 4, p.idx_scales + 4 * src,
+                      sf_bytes, full + stage);
         }
         ++armed;
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
       // a CTA must not exit while a copy it started still writes its shared
       // memory: after a timeout the consumers may have stopped reading the ring
-      drain_armed(full, C::kStages, armed);
-      drain_armed(qfull, 2, qn);
+      if (leader) {
+        drain_armed(full, C::kStages, armed);
+        drain_armed(qfull, 2, qn);
+      }
     } else if (warp == 1 && (MX || lane == 0)) {
       // --------------------------------------------------------- MMA issuer
       // Lane 0 issues.  With MXFP4 keys the whole warp runs the loop: it
@@ -799,15 +799,29 @@ __global__ void __launch_bounds__(kMqThreads, kIdxCtasPerSm)
           tma_load_2d(dst, &tm_k, 0, (int)((int64_t)g.b * p.map.max_len + t0), full + stage);
         } else {
           const int rpl = p.rows_per_load;
+          const int nu = 128 / rpl;
           int nload = 0;
           int64_t src_rows[16];
-          for (int u = 0; u < 128 / rpl; ++u) {
+          // page-table entries all requested before any is used (see above)
+          const int32_t* pt = p.map.page_table + (int64_t)g.b * p.map.max_pages_per_seq;
+          int32_t phys[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const uint32_t pg = p.map.page_of((uint32_t)(t0 + u * rpl));
+            phys[u] = u < nu ? __ldg(pt + (pg < (uint32_t)p.map.max_pages_per_seq ? pg : p.map.max_pages_per_seq - 1))
+                             : -1;
+          }
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
             const int64_t pos = t0 + (int64_t)u * rpl;
             src_rows[u] = -1;
-            if (pos < vmax) {
-              const int64_t r = p.map.row(g.b, pos);
-              if (r < 0) set_status(p.status, CSA2_DEV_BAD_PAGE);
-              else { src_rows[u] = r; ++nload; }
+            if (u < nu && pos < vmax) {
+              if (phys[u] < 0 || phys[u] >= p.map.num_pages) {
+                set_status(p.status, CSA2_DEV_BAD_PAGE);
+              } else {
+                src_rows[u] = (int64_t)phys[u] * p.map.page_size + p.map.in_page((uint32_t)pos);
+                ++nload;
+              }
             }
           }
           mbar_arrive_expect_tx(full + stage, (uint32_t)(nload * rpl * DI));
@@ -1044,7 +1058,7 @@ cudaError_t launch_indexer(const csa2_cache& c, const RowSet& rows, int mode, co
   p.pool_blocks = pool_blocks;
   p.pool_cnt = pool_cnt;
   p.w = w;
-  p.map = RowMap{c.page_table, c.page_size, c.max_pages_per_seq, c.max_len, c.num_pages};
+  p.map = row_map_of(c);
   p.row_len = reinterpret_cast<int32_t*>(ws + L.row_len);
   p.tile_prefix = reinterpret_cast<int32_t*>(ws + L.tile_prefix);
   p.scores = reinterpret_cast<float*>(ws + L.scores);

@@ -308,7 +308,7 @@ cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const floa
   p.seq_len = c.seq_len;
   p.rope_cos = c.rope_cos;
   p.rope_sin = c.rope_sin;
-  p.map = RowMap{c.page_table, c.page_size, c.max_pages_per_seq, c.max_len, c.num_pages};
+  p.map = row_map_of(c);
   p.B = c.batch;
   p.T = T;
   p.D = c.dim;
