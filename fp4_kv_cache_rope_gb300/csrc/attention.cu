@@ -102,7 +102,7 @@ struct AttnCfg {
   static_assert((kXSlab % 1024) == 0 && (kQOff % 1024) == 0 && (kPOff % 1024) == 0,
                 "128-byte swizzle atoms need 1024-byte aligned slabs");
   static_assert(NSLAB * kXSlab >= 64 * D * 2, "the X slabs hold the staged bf16 query");
-  static_assert(6 + 2 * NT + 2 * kKtSlots <= 32, "mbarrier area");
+  static_assert(7 + 2 * NT + 2 * kKtSlots <= 32, "mbarrier area");
 };
 
 struct AttnParams {
@@ -265,11 +265,11 @@ __device__ __forceinline__ uint32_t map_to_rank(const void* p, int rank) {
   return r;
 }
 
-// f16 copy of the query rows [heads x D] (bf16 in global memory at qs) into
-// the swizzled Q slabs by the compute threads (thread t of 256), every load
-// in flight at once, assuming no head needs scaling; returns, over the
-// compute warps, whether some |q| >= 2^14 (then the copy is redone with a
-// power-of-two scale per head).  Rows past `heads` are zero.
+// f16 copy of the query rows [heads x D] (bf16, staged row-major in shared
+// memory at qs) into the swizzled Q slabs by the compute threads (thread t of
+// 256), assuming no head needs scaling; returns, over the compute warps,
+// whether some |q| >= 2^14 (then the copy is redone with a power-of-two scale
+// per head).  Rows past `heads` are zero.
 template <int NSLAB>
 __device__ __forceinline__ bool convert_query(const uint8_t* qs, uint8_t* sq, int t, int heads) {
   constexpr int D = NSLAB * 64;
@@ -285,7 +285,7 @@ __device__ __forceinline__ bool convert_query(const uint8_t* qs, uint8_t* sq, in
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int i = i0 + n * u;
-      v[u] = (i < kAll && i / kChunks < heads) ? __ldg(reinterpret_cast<const uint4*>(qs) + i)
+      v[u] = (i < kAll && i / kChunks < heads) ? reinterpret_cast<const uint4*>(qs)[i]
                                                : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
@@ -408,6 +408,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
   uint64_t* pvt = bars + 6 + NT;           // [NT] PV accumulator tile t done (commit)
   uint64_t* kt_full = bars + 6 + 2 * NT;   // [kKtSlots] key table written (index warp)
   uint64_t* kt_empty = kt_full + kKtSlots; // [kKtSlots] key table consumed (8 warps)
+  uint64_t* q_land = kt_empty + kKtSlots;  // the query row's bulk copy landed
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + C::kFlags);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + C::kFlags + 4);
   float* qmul = reinterpret_cast<float*>(misc + C::kQmul);
@@ -439,6 +440,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
       mbar_init(kt_full + s, 1);
       mbar_init(kt_empty + s, 8);
     }
+    mbar_init(q_land, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -447,15 +449,101 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // everything read from here on may come from the previous kernels (the
-  // selection, seq_len, and whatever wrote the query)
-  griddep_wait();
-  griddep_launch_dependents();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tO = tmem + 128;  // O^T tile t at columns 128 + 64 t
+  bool ok = true;  // this thread's view: false once a wait gave up
+  // ---- Before the dependency wait: the query, which the selection does not
+  // produce (the kernels ahead of the one this launch depends on have all
+  // completed when it starts), so its copy and conversion overlap the tail
+  // of the selection.  One bulk copy per 32 KB brings the row (bf16
+  // [heads x D], contiguous and 16-byte aligned) into the X slabs.
+  if (warp == 9 && lane == 1) {
+    // the output row's first and last lines (their address translation is
+    // then ready when the merge writes them)
+    const float* o0 = p.out + (int64_t)row * p.heads * D;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(o0));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(o0 + (int64_t)p.heads * D - 1));
+  }
+  if (warp == 9 && lane == 0) {
+    const uint8_t* qg = reinterpret_cast<const uint8_t*>(p.q + (int64_t)row * p.heads * D);
+    const uint32_t qbytes = (uint32_t)p.heads * D * 2;
+    mbar_arrive_expect_tx(q_land, qbytes);
+    for (uint32_t o = 0; o < qbytes; o += 32768u)
+      bulk_load(sx + o, qg + o, qbytes - o < 32768u ? qbytes - o : 32768u, q_land);
+  }
+  if (warp < 8) {
+    const int ct = tid;
+    // ---- query: f16 copy of the bf16 rows, staged in the X slabs by the
+    // bulk copy above.  When some |q| >= 2^14, each head is redone scaled by
+    // a power of two so that its f16 copy stays exact (the logit factor
+    // absorbs the power).
+    const uint8_t* qs = sx;
+    if (!mbar_wait(q_land, 0, abort_flag)) ok = false;
+    ok = __all_sync(0xffffffffu, ok);
+    if (!convert_query<NSLAB>(qs, sq, ct, p.heads)) {
+      if (ct < 64) qmul[ct] = ct < p.heads ? p.scale_log2 : 0.0f;
+    } else {
+      constexpr int kChunks = D / 8;
+      constexpr int kPer = (kChunks + 31) / 32;
+      for (int hh = 0; hh < 8; ++hh) {
+        const int h = 8 * warp + hh;
+        uint4 v[kPer];
+        float mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int c = lane + 32 * i;
+          v[i] = make_uint4(0, 0, 0, 0);
+          if (h < p.heads && c < kChunks)
+            v[i] = *reinterpret_cast<const uint4*>(qs + (h * D + c * 8) * 2);
+          const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            mx = fmaxf(mx, fabsf(__uint_as_float(w4[u] << 16)));
+            mx = fmaxf(mx, fabsf(__uint_as_float(w4[u] & 0xFFFF0000u)));
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        int e = 0;
+        if (mx > 16384.0f) e = (int)ceilf(log2f(mx)) - 14;
+        const float inv = exp2f((float)-e);
+        if (lane == 0) qmul[h] = h < p.heads ? p.scale_log2 * exp2f((float)e) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int c = lane + 32 * i;
+          if (c < kChunks) {
+            const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              __half2 h2 = __floats2half2_rn(__uint_as_float(w4[u] << 16) * inv,
+                                             __uint_as_float(w4[u] & 0xFFFF0000u) * inv);
+              o[u] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            st_swz(sq + (c >> 3) * C::kQSlab, h, c & 7, make_uint4(o[0], o[1], o[2], o[3]));
+          }
+        }
+      }
+    }
+    fence_async_smem();
+    named_sync(1, kComputeThreads);  // Q slabs and qmul written; the staged rows are free
+    if (lane == 0) mbar_arrive(q_ready);
+  }
+  // everything read from here on may come from the previous kernels (the
+  // selection and seq_len)
+  griddep_wait();
+  griddep_launch_dependents();
+  if (warp == 9) {
+    // this CTA's share of the index list requested into L1 before the row's
+    // counts are known, its start taken for a full selection (a shorter one
+    // only makes part of the prefetch miss)
+    const int g0s = (int)((int64_t)p.kcap * split / p.splits);
+    const int g1s = (int)((int64_t)p.kcap * (split + 1) / p.splits);
+    for (int e = g0s + 32 * lane; e < g1s; e += 32 * 32)
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(p.idx + (int64_t)row * p.kcap + e));
+  }
   const RowKeys rk = row_keys(p, row, D);
   const CtaKeys ck = cta_keys(rk, split, p.splits);
-  bool ok = true;  // this thread's view: false once a wait gave up
 
   if (warp < 8) {
     // ============================================================ compute warps
@@ -494,58 +582,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
         }
       }
     };
-    // ---- query: f16 copy of the bf16 rows.  When some |q| >= 2^14, each
-    // head is redone scaled by a power of two so that its f16 copy stays
-    // exact (the logit factor absorbs the power).
-    const uint8_t* qg = reinterpret_cast<const uint8_t*>(p.q + (int64_t)row * p.heads * D);
-    if (!convert_query<NSLAB>(qg, sq, ct, p.heads)) {
-      if (ct < 64) qmul[ct] = ct < p.heads ? p.scale_log2 : 0.0f;
-    } else {
-      constexpr int kChunks = D / 8;
-      constexpr int kPer = (kChunks + 31) / 32;
-      for (int hh = 0; hh < 8; ++hh) {
-        const int h = 8 * warp + hh;
-        uint4 v[kPer];
-        float mx = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-          const int c = lane + 32 * i;
-          v[i] = make_uint4(0, 0, 0, 0);
-          if (h < p.heads && c < kChunks)
-            v[i] = __ldg(reinterpret_cast<const uint4*>(qg + (h * D + c * 8) * 2));
-          const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            mx = fmaxf(mx, fabsf(__uint_as_float(w4[u] << 16)));
-            mx = fmaxf(mx, fabsf(__uint_as_float(w4[u] & 0xFFFF0000u)));
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        int e = 0;
-        if (mx > 16384.0f) e = (int)ceilf(log2f(mx)) - 14;
-        const float inv = exp2f((float)-e);
-        if (lane == 0) qmul[h] = h < p.heads ? p.scale_log2 * exp2f((float)e) : 0.0f;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-          const int c = lane + 32 * i;
-          if (c < kChunks) {
-            const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-            uint32_t o[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              __half2 h2 = __floats2half2_rn(__uint_as_float(w4[u] << 16) * inv,
-                                             __uint_as_float(w4[u] & 0xFFFF0000u) * inv);
-              o[u] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            st_swz(sq + (c >> 3) * C::kQSlab, h, c & 7, make_uint4(o[0], o[1], o[2], o[3]));
-          }
-        }
-      }
-    }
-    fence_async_smem();
-    named_sync(1, kComputeThreads);  // Q slabs and qmul written
-    if (lane == 0) mbar_arrive(q_ready);
 
     float l[32];  // partial softmax denominators: this key slot, heads 32 hf + h
 #pragma unroll
@@ -560,6 +596,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
       wait_all(kt_full, 0);
       load_raw(0, raw, kinds);
     }
+
     for (int i = 0; i < ck.ntile; ++i) {
       const int nk = ck.tile_keys(i);
       // ---- dequantise tile i, four slabs at a time (a warp's items cover
@@ -805,36 +842,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
         const int l = base + jj;
         pos[u] = (jj < nk && l < ck.ng) ? __ldg(p.idx + (int64_t)row * p.kcap + ck.g0 + l) : 0;
       }
+      int vv[kPer];
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
         const int jj = lane + 32 * u;
-        if (jj >= kTile) break;
         const int l = base + jj;
         int v = -1;
         if (jj < nk) {
           if (l < ck.ng) {
             if (pos[u] >= 0 && pos[u] < rk.vis) {
               const int64_t r = p.map.row(rk.b, pos[u]);
-              if (r >= 0) {
-                v = (int)r;
-                prefetch_l2(p.codes + r * p.code_stride, kCodeBytes);
-                prefetch_l2(p.scales + r * p.scale_stride, kScaleBytes);
-              } else {
-                set_status(p.status, CSA2_DEV_BAD_PAGE);
-              }
+              if (r >= 0) v = (int)r;
+              else set_status(p.status, CSA2_DEV_BAD_PAGE);
             } else {
               set_status(p.status, CSA2_DEV_BAD_INDEX);
             }
           } else {
             v = -2 - (ck.w0 + l - ck.ng);
-            prefetch_l2(rk.swa0 + (int64_t)(ck.w0 + l - ck.ng) * D, (uint32_t)D);
           }
         }
-        tab[jj] = v;
+        vv[u] = v;
+        if (jj < kTile) tab[jj] = v;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(kt_full + slot);
+      // the tile's rows into L2 once its table is out (the compute warps
+      // read them from there; tile 0's reads may already be under way)
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        if (vv[u] >= 0) {
+          prefetch_l2(p.codes + (int64_t)vv[u] * p.code_stride, kCodeBytes);
+          prefetch_l2(p.scales + (int64_t)vv[u] * p.scale_stride, kScaleBytes);
+        } else if (vv[u] <= -2) {
+          prefetch_l2(rk.swa0 + (int64_t)(-2 - vv[u]) * D, (uint32_t)D);
+        }
+      }
     }
+    // the CTA must not exit while the query copy may still write its shared
+    // memory (the compute warps stop waiting for it after a timeout)
+    if (lane == 0) mbar_wait_drain(q_land, 0);
     __syncwarp();
   }
   tc_fence_before();
@@ -872,8 +918,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
     //   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s  per head,
     // M the largest m_s with l_s > 0.  Each CTA scales its own O^T by its
     // factor 2^(m_s - M) / den and stores it straight into the shared memory
-    // of the CTA that owns each 32-channel group; after a cluster barrier every
-    // CTA sums the C partials of its own channels and writes them out.
+    // of the CTA that owns each 32-channel group (a warp's stores cover 128
+    // contiguous bytes of one head's row, the form distributed shared memory
+    // moves fastest; the CTA's own share is stored locally); after a cluster
+    // barrier every CTA sums the C partials of its own channels and writes
+    // them out.
     const int Cn = p.splits;
     constexpr int kGroups = D / 32;
     const int slmax = 32 * ((kGroups + Cn - 1) / Cn);
@@ -902,6 +951,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
     __syncthreads();
     if (warp < 8) {
       const int quad = warp & 3, hf = warp >> 2;
+      float f[32];
+#pragma unroll
+      for (int h = 0; h < 32; ++h) f[h] = fw[32 * hf + h];
 #pragma unroll 1
       for (int t = 0; t < NT; ++t) {
         const int g = 4 * t + quad;   // 32-channel group of this warp
@@ -916,12 +968,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
           tmem_ld_wait();
           reg_fence32(v);
         }
-        const uint32_t dst = map_to_rank(recv + ((size_t)split * 64 + 32 * hf) * slmax + cl, r);
+        float* dst = recv + ((size_t)split * 64 + 32 * hf) * slmax + cl;
+        if (r == split) {
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          const float f = fw[32 * hf + h];
-          const float o = (any && f != 0.0f) ? __uint_as_float(v[h]) * f : 0.0f;
-          st_cluster_f32(dst + (uint32_t)(h * slmax * 4), o);
+          for (int h = 0; h < 32; ++h)
+            dst[h * slmax] = (any && f[h] != 0.0f) ? __uint_as_float(v[h]) * f[h] : 0.0f;
+        } else {
+          const uint32_t da = map_to_rank(dst, r);
+#pragma unroll
+          for (int h = 0; h < 32; ++h)
+            st_cluster_f32(da + (uint32_t)(h * slmax * 4),
+                           (any && f[h] != 0.0f) ? __uint_as_float(v[h]) * f[h] : 0.0f);
         }
       }
     }
@@ -931,17 +988,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
       const int w = 32 * ((kGroups * (split + 1)) / Cn) - c0;
       const int n4 = w / 4;
       const int items = p.heads * n4;
-      for (int it = tid; it < items; it += kAttnThreads) {
-        const int h = it / n4, c4 = it - h * n4;
-        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        for (int s = 0; s < Cn; ++s) {
-          const float4 x = *reinterpret_cast<const float4*>(recv + ((size_t)s * 64 + h) * slmax + 4 * c4);
-          acc.x += x.x;
-          acc.y += x.y;
-          acc.z += x.z;
-          acc.w += x.w;
+      // four items per thread and round, every load of the round in flight
+      // before the sums
+      constexpr int kU = 4;
+      for (int it0 = tid; it0 < items; it0 += kU * kAttnThreads) {
+        float4 acc[kU];
+        int hh[kU], cc[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int it = it0 + u * kAttnThreads;
+          hh[u] = it < items ? it / n4 : 0;
+          cc[u] = it < items ? it - hh[u] * n4 : 0;
+          acc[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
-        *reinterpret_cast<float4*>(p.out + ((int64_t)row * p.heads + h) * D + c0 + 4 * c4) = acc;
+#pragma unroll
+        for (int sp2 = 0; sp2 < kMaxSplits; ++sp2) {
+          if (sp2 < Cn) {
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+              const float4 x = *reinterpret_cast<const float4*>(recv + ((size_t)sp2 * 64 + hh[u]) * slmax + 4 * cc[u]);
+              acc[u].x += x.x;
+              acc[u].y += x.y;
+              acc[u].z += x.z;
+              acc[u].w += x.w;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+          if (it0 + u * kAttnThreads < items)
+            *reinterpret_cast<float4*>(p.out + ((int64_t)row * p.heads + hh[u]) * D + c0 + 4 * cc[u]) = acc[u];
       }
     }
   }
