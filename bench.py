@@ -256,6 +256,20 @@ def build_run(wid, extra_capacity, batch=None):
     return st
 
 
+def append_roofline(wl, rows, ms, peak):
+    """Algorithmic bytes of one quant_append launch of `rows` rows (read the
+    fp32 row, the fp32 indexer key and the position's cos/sin row of the
+    rotary table; write the FP4 codes, the E4M3 scales and the indexer key)
+    over its event-timed duration, against the measured HBM peak."""
+    per_row = (wl.dim * 4 + wl.idx_dim * 4 + wl.rope_dim * 4 + wl.dim // 2 + wl.dim // 16
+               + wl.idx_entry_bytes())
+    b = rows * per_row
+    gbs = b / (ms * 1e-3) / 1e9 if ms > 0 else None
+    return {"rows_per_launch": rows, "bytes_per_launch": b, "launch_us": ms * 1e3,
+            "achieved_gbs": gbs, "peak": peak, "unit": "GB/s",
+            "frac": gbs / peak if gbs else None}
+
+
 def append_launches(wl, T):
     """Kernel launches of one quant_append of T tokens per sequence."""
     groups = wl.batch * T * (wl.dim + wl.idx_dim) // 16
@@ -267,21 +281,38 @@ def index_launches(rows):
     return 2 if rows <= 1024 else 3
 
 
-def step_multi_query(st, i, ev=None, ev_attn=None):
+def arm(K, family, pair):
+    """Brackets the next launches of a kernel family with the CUDA events of
+    `pair` (None disarms)."""
+    if pair is not None:
+        K.set_launch_events(family, pair[0], pair[1])
+
+
+def disarm(K, family, pair):
+    if pair is not None:
+        K.set_launch_events(family)
+
+
+def step_multi_query(st, i, ev=None, ev_attn=None, ev_more=None):
     """One step of a multi-query workload: T new tokens per sequence appended,
     then every layer of the chunk (Full, optionally Reindex over the Full
     layer's per-query pools) indexed and attended for all T queries."""
     K, wl, dw, ins, T = st["K"], st["wl"], st["dw"], st["inputs"], st["T"]
     B, k, ws, c = wl.batch, wl.topk, dw.ws, dw.cache
     q_pos = st["q_pos_buf"] if "q_pos_buf" in st else st["q_pos_all"][i]
+    em = ev_more or {}
+    arm(K, K.KERNEL_QUANT, em.get("append"))
     K.quant_append(c, st["new_kv"], st["new_idx"], T, ws)
+    disarm(K, K.KERNEL_QUANT, em.get("append"))
     launches = append_launches(wl, T)
     reindex = len(wl.layers) > 1
     if ev is not None:
         K.set_launch_events(K.KERNEL_INDEXER, ev[0], ev[1])
+    arm(K, K.KERNEL_SELECT, em.get("select"))
     K.index_full(c, ins[0]["q_idx"], ins[0]["w"], wl.idx_heads, T, q_pos, None, B, k,
                  st["idx"][0], st["cnt"][0], st["pool"] if reindex else None,
                  st["pool_cnt"] if reindex else None, ws)
+    disarm(K, K.KERNEL_SELECT, em.get("select"))
     if ev is not None:
         K.set_launch_events(K.KERNEL_INDEXER)
     launches += index_launches(B * T)
@@ -301,20 +332,25 @@ def step_multi_query(st, i, ev=None, ev_attn=None):
     return launches
 
 
-def step(st, ev=None, ev_attn=None, i=0):
+def step(st, ev=None, ev_attn=None, i=0, ev_more=None):
     """One layer-step (or one CSA2 group step for the group workload)."""
     K, wl, dw, ins = st["K"], st["wl"], st["dw"], st["inputs"]
     if wl.prefill_tokens:
-        return step_multi_query(st, i, ev, ev_attn)
+        return step_multi_query(st, i, ev, ev_attn, ev_more)
     B, k, ws, c = wl.batch, wl.topk, dw.ws, dw.cache
+    em = ev_more or {}
+    arm(K, K.KERNEL_QUANT, em.get("append"))
     K.quant_append(c, st["new_kv"], st["new_idx"], 1, ws)
+    disarm(K, K.KERNEL_QUANT, em.get("append"))
     launches = 1  # quant_append (one cluster launch that also advances seq_len)
     if ev is not None:
         K.set_launch_events(K.KERNEL_INDEXER, ev[0], ev[1])
     if wl.modes is None:
         # Full layer (layer 0); the group workload adds Reindex and Reuse
+        arm(K, K.KERNEL_SELECT, em.get("select"))
         K.index_full(c, ins[0]["q_idx"], ins[0]["w"], wl.idx_heads, 1, None, None, B, k,
                      st["idx"][0], st["cnt"][0], st["pool"], st["pool_cnt"], ws)
+        disarm(K, K.KERNEL_SELECT, em.get("select"))
         if ev is not None:
             K.set_launch_events(K.KERNEL_INDEXER)
         launches += 2
@@ -337,8 +373,10 @@ def step(st, ev=None, ev_attn=None, i=0):
     else:
         nf, nr = st["counts"]["full"], st["counts"]["reindex"]
         if nf:
+            arm(K, K.KERNEL_SELECT, em.get("select"))
             K.index_full(c, ins[0]["q_idx"], ins[0]["w"], wl.idx_heads, 1, None, st["full_ids"],
                          nf, k, st["idx"][0], st["cnt"][0], None, None, ws)
+            disarm(K, K.KERNEL_SELECT, em.get("select"))
             launches += 2
         if ev is not None:
             K.set_launch_events(K.KERNEL_INDEXER)
@@ -408,57 +446,22 @@ def roofline_bytes_per_step(wl, n_at):
 
 
 # ------------------------------------------------------------- CPU baseline
-def oracle_sample(wl, b, n, layer=0):
-    """One sequence of a Full layer-step on the oracle: inputs are prepared
-    untimed; the returned callable is the timed work."""
-    import numpy as np
-    import synth
-    from oracle import csa2 as O
-    from oracle.formats import bf16_bits_to_f64
-    from oracle.workload import SeqRef
-    from synth.host import host_rows_normal
-    ref = SeqRef(wl, b, n=n)
-    ik = ref.idxk_all(n)
-    inp = ref.inputs(layer)
-    newrow = host_rows_normal(wl.seed, synth.T_KV, b, [n], wl.dim, ref.mult)
-    q64 = bf16_bits_to_f64(inp["q_bf16"][0])
-    swa = O.swa_rows_decode(inp["swa"][: wl.window])
-
-    def run():
-        O.quant_append_rows(newrow, np.array([n]), ref.cos, ref.sin, wl.rope_dim)
-        if wl.idx_format == "mxfp4":
-            q = O.e4m3_decode(inp["q_idx"][0]).reshape(wl.idx_heads, -1)
-            s = O.indexer_scores_values(q, inp["w"][0], O.dequantize_mxfp4(ik[0], ik[1],
-                                                                           wl.idx_dim))
-        else:
-            s = O.indexer_scores(inp["q_idx"][0], inp["w"][0], ik)
-        idx, pool = O.full_select(s, wl.topk)
-        # the selected rows' cache bytes (regenerated and quantised here; the
-        # oracle keeps no cache of its own)
-        xh = ref.dequant_rows(idx)
-        return O.sparse_attention(q64, np.concatenate([xh, swa]))
-    return run
-
-
-def cpu_baseline(wl, samples=4, budget_s=20.0):
-    run = None
+def cpu_baseline(wl, per_piece_s=2.0):
+    """The oracle on the host cores over one bounded sample of the workload's
+    layer-step: the pieces of oracle_plan (the same plan the reference arm
+    times), each run once and weighted by the share of the step it stands for."""
+    pieces, layers, text = oracle_plan(wl, per_piece_s)
     times = []
-    t_start = time.time()
-    for b in range(samples):
-        run = oracle_sample(wl, b, wl.lengths[b])
+    for run, _w in pieces:
         t0 = time.perf_counter()
         run()
         times.append(time.perf_counter() - t0)
-        if time.time() - t_start > budget_s:
-            break
-    per_seq = statistics.mean(times)
-    value = 1.0 / (per_seq * wl.batch)
-    return {"value": value, "unit": "layer-steps/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{len(times)} of {wl.batch} sequences of one Full layer-step (quantise the "
-                      f"new row, score {wl.lengths[0]} positions, select, re-quantise and "
-                      f"dequantise the selected rows, attend) in numpy fp64 with the host BLAS "
-                      f"threads; scaled to the whole batch",
-            "seconds_per_sequence": per_seq}
+    step_s = sum(w * t for (_, w), t in zip(pieces, times))
+    return {"value": layers / step_s, "unit": "layer-steps/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{text}; each of the {len(pieces)} pieces run once, numpy fp64 with the "
+                      f"host BLAS threads",
+            "seconds_sampled": sum(times)}
 
 
 def _score_fn(wl, inp, ik, tq=0):
@@ -1040,12 +1043,13 @@ def main():
     def sampled(i):
         return i % every == every // 2
 
-    def run_steps(n, evs=None, evas=None, state=None):
+    def run_steps(n, evs=None, evas=None, state=None, evms=None):
         count = 0
         for i in range(n):
             j = i // every
             take = evs is not None and sampled(i)
-            count += step(state or st, evs[j] if take else None, evas[j] if take else None, i)
+            count += step(state or st, evs[j] if take else None, evas[j] if take else None, i,
+                          evms[j] if take and evms is not None else None)
         return count
 
     reset()
@@ -1057,7 +1061,9 @@ def main():
           for _ in range(max(n_ev, 1))]
     eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(max(n_ev, 1))]
-    for a, b in ev + eva:   # torch creates the CUDA event on the first record
+    evm = [{key: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for key in ("append", "select")} for _ in range(max(n_ev, 1))]
+    for a, b in ev + eva + [pr for d in evm for pr in d.values()]:   # torch creates the CUDA event on the first record
         a.record()
         b.record()
     torch.cuda.synchronize()
@@ -1071,7 +1077,7 @@ def main():
             launches = run_steps(args.steps)
         graph_ev = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph_ev, capture_error_mode="thread_local"):
-            run_steps(args.steps, ev, eva)
+            run_steps(args.steps, ev, eva, evms=evm)
         reset()
         graph_ev.replay()             # warm-up replays (untimed)
         reset()
@@ -1102,11 +1108,13 @@ def main():
     if graph_ev is not None:
         graph_ev.replay()
     else:
-        run_steps(args.steps, ev, eva)
+        run_steps(args.steps, ev, eva, evms=evm)
     torch.cuda.synchronize()
     status |= K.get_status(st["dw"].ws)
     idx_ms = [a.elapsed_time(b) for a, b in ev[:n_ev]]
     attn_ms = [a.elapsed_time(b) for a, b in eva[:n_ev]]
+    app_ms = [d["append"][0].elapsed_time(d["append"][1]) for d in evm[:n_ev]]
+    sel_ms = [d["select"][0].elapsed_time(d["select"][1]) for d in evm[:n_ev]]
     # bytes of the sampled indexer launches (visible length grows by T per step)
     T = st["T"]
     if wl.prefill_tokens:
@@ -1270,7 +1278,10 @@ def main():
             "path_hbm": {"bytes_per_step": statistics.mean(roof_bytes), "achieved_gbs": path_gbs,
                          "frac": path_gbs / peak},
             "kernels_us": {"indexer": statistics.mean(idx_ms) * 1e3,
-                           "attention": statistics.mean(attn_ms) * 1e3},
+                           "attention": statistics.mean(attn_ms) * 1e3,
+                           "select": statistics.mean(sel_ms) * 1e3,
+                           "append": statistics.mean(app_ms) * 1e3},
+            "append": append_roofline(wl, B * st["T"], statistics.mean(app_ms), peak),
             "e2e": {"value": e2e_value, "unit": "layer-steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e_steps,
                     "cuda_graph": e2e_graph is not None, "eager_value": e2e_eager,

@@ -13,7 +13,7 @@ import re
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PRODUCT = "fp4_kv_cache_rope_gb300"
-BENCH_ORACLE_USERS = {"oracle_sample", "oracle_plan", "_score_fn", "cpu_baseline",
+BENCH_ORACLE_USERS = {"oracle_plan", "_score_fn", "cpu_baseline",
                       "reference_arm", "model_oracle_sample", "model_bench_cpu"}
 
 
