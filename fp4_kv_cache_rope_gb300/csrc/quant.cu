@@ -42,6 +42,8 @@ struct QuantParams {
   RowMap map;
   int32_t B, T, D, R, di;
   int32_t groups_main, groups_total;  // per row
+  int32_t row0;                         // first row (b * T + i) of this launch
+  uint32_t n_groups;                    // groups of this launch (< 2^31)
   uint32_t* status;
 };
 
@@ -130,12 +132,17 @@ __device__ __noinline__ void quant_idx_mx(const QuantParams& p, int64_t row, int
   p.idx_scales[r * 4 + gi] = (uint8_t)code;
 }
 
-// Quantises group gid (row gid / groups_total, group gid % groups_total).
-__device__ __forceinline__ void quant_group(const QuantParams& p, int64_t gid) {
-  const int64_t row = gid / p.groups_total;
-  const int g = (int)(gid - row * p.groups_total);
-  const int b = (int)(row / p.T);
-  const int i = (int)(row - (int64_t)b * p.T);
+// Quantises group gid of the launch (row row0 + gid / groups_total, group
+// gid % groups_total).  Rows (B * T) and a launch's groups fit in 31 bits, so
+// the index arithmetic is 32-bit (a 64-bit division is a long software
+// sequence on the GPU).
+__device__ __forceinline__ void quant_group(const QuantParams& p, uint32_t gid) {
+  const uint32_t lrow = gid / (uint32_t)p.groups_total;
+  const int g = (int)(gid - lrow * (uint32_t)p.groups_total);
+  const int32_t row32 = p.row0 + (int32_t)lrow;
+  const int b = row32 / p.T;
+  const int i = row32 - b * p.T;
+  const int64_t row = row32;
   const bool is_idx = g >= p.groups_main;
   if (is_idx && p.idx_mx) {
     quant_idx_mx(p, row, b, i, g - p.groups_main);
@@ -238,19 +245,25 @@ __device__ __forceinline__ void quant_group(const QuantParams& p, int64_t gid) {
 }
 
 __global__ void __launch_bounds__(256) quant_append_kernel(QuantParams p) {
-  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (gid < (int64_t)p.B * p.T * p.groups_total) quant_group(p, gid);
+  const uint32_t gid = blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid < p.n_groups) quant_group(p, gid);
 }
 
 // Small appends (decode): one thread-block cluster of up to 8 CTAs does every
 // group; after a cluster barrier (every read of seq_len precedes it) CTA 0
 // advances seq_len, so no second launch is needed.
+//
+// The groups are quantised and stored before the dependency wait, so that
+// they overlap the previous kernel's tail (on the SMs it leaves free): the
+// new rows go to positions >= seq_len, which no kernel of the path reads
+// before they are appended, and seq_len itself is written only by appends.
+// Only the seq_len update waits, because the previous kernel may still read
+// seq_len.  The inputs are the caller's (see csa2_quant_append).
 __global__ void __launch_bounds__(512) quant_append_cluster_kernel(QuantParams p) {
-  griddep_wait();  // the previous kernel reads seq_len, which this one advances
+  const uint32_t gid = blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid < p.n_groups) quant_group(p, gid);
+  griddep_wait();
   griddep_launch_dependents();
-  const int64_t total = (int64_t)p.B * p.T * p.groups_total;
-  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (gid < total) quant_group(p, gid);
   cluster_sync();
   if (blockIdx.x == 0) {
     for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
@@ -317,8 +330,11 @@ cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const floa
   p.groups_main = c.dim / kGroup;
   p.groups_total = p.groups_main + (idx_in ? c.idx_dim / (p.idx_mx ? 32 : 16) : 0);
   p.status = status;
+  p.row0 = 0;
   const int64_t total = (int64_t)c.batch * T * p.groups_total;
+  if ((int64_t)c.batch * T > 0x7FFFFFFFll) return cudaErrorInvalidValue;
   if (total <= kSmallAppendGroups) {
+    p.n_groups = (uint32_t)total;
     const int ctas = (int)((total + 511) / 512);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas, 1, 1);
@@ -340,11 +356,18 @@ cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const floa
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
-  const int64_t blocks = (total + 255) / 256;
   prefer_max_shared(quant_append_kernel);
   prefer_max_shared(advance_len_kernel);
+  // launches of at most 2^30 groups (whole rows), each indexed in 32 bits
+  const int64_t rows = (int64_t)c.batch * T;
+  const int64_t rows_per = ((int64_t)1 << 30) / p.groups_total;
   record_launch_begin(CSA2_KERNEL_QUANT, s);
-  quant_append_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+  for (int64_t r0 = 0; r0 < rows; r0 += rows_per) {
+    const int64_t nr = rows - r0 < rows_per ? rows - r0 : rows_per;
+    p.row0 = (int32_t)r0;
+    p.n_groups = (uint32_t)(nr * p.groups_total);
+    quant_append_kernel<<<(unsigned)((p.n_groups + 255) / 256), 256, 0, s>>>(p);
+  }
   record_launch_end(CSA2_KERNEL_QUANT, s);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -168,6 +168,13 @@ csa2_status csa2_fp8_quant(const float *x, int64_t n, uint8_t *out, void *stream
  * saturating, sign copied), all codes 0 when the scale decodes to 0.
  * Afterwards seq_len[b] += T.  A row with p >= max_len is skipped and sets
  * CSA2_DEV_OVERFLOW.
+ * Ordering: small appends (decode sizes) are launched so that they may start
+ * while the previous kernel on the stream finishes, when that kernel allows
+ * its dependents to launch early (the library's own kernels do); they read
+ * kv / idx_k_in and write the new rows before waiting for it, and update
+ * seq_len only after it completes.  The kernel just before this call must
+ * therefore not write kv or idx_k_in after allowing early launch (kernels
+ * that do not use programmatic launch never overlap it).
  */
 csa2_status csa2_quant_append(const csa2_cache *cache, const float *kv, const float *idx_k_in,
                               int32_t T, void *ws, void *stream);
@@ -191,7 +198,8 @@ csa2_status csa2_quant_append(const csa2_cache *cache, const float *kv, const fl
  * kv, z:    device fp32 [B, 2T, D] source rows before rotation and their
  *           compression logits, 16-byte aligned.
  * idx_k_in: device fp32 [B, T, di] (one indexer key per entry) or NULL.
- * Afterwards seq_len[b] += T (entries).  Errors as csa2_quant_append.
+ * Afterwards seq_len[b] += T (entries).  Errors and ordering (kv, z and
+ * idx_k_in read before the previous kernel completes) as csa2_quant_append.
  */
 csa2_status csa2_quant_append_pairs(const csa2_cache *cache, const float *kv, const float *z,
                                     const float *idx_k_in, int32_t T, void *ws, void *stream);
