@@ -110,7 +110,12 @@ def mini_workload(page_size=64):
                     page_size=page_size, outlier_frac=0.02)
 
 
-@pytest.fixture(scope="module", params=[64, 0], ids=["paged64", "contiguous"])
+# Page sizes: the common 64, none, and the other layouts the indexer's
+# producer handles differently: 8-32-row pages (several pages per 128-position
+# tile, page-table windows shifted every few tiles), 256-row pages (two tiles
+# per page) and 384-row pages (not a power of two: a division, not a shift).
+@pytest.fixture(scope="module", params=[64, 0, 8, 16, 32, 256, 384],
+                ids=["paged64", "contiguous", "paged8", "paged16", "paged32", "paged256", "paged384"])
 def mini(request):
     wl = mini_workload(request.param)
     return wl, DeviceWorkload(wl)
