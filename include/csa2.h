@@ -295,6 +295,12 @@ csa2_status csa2_index_reindex(const csa2_cache *cache, const uint8_t *q_idx, co
  * When the SMs outnumber the query rows, the keys of a row are split over a
  * thread-block cluster of up to 8 CTAs whose partial results are merged in
  * distributed shared memory; the workspace holds no partial outputs.
+ * Ordering: the kernel may start while the previous kernel on the stream
+ * finishes, when that kernel allows its dependents to launch early (the
+ * library's own kernels do), and copies q before waiting for it; idx, cnt,
+ * seq_len and the cache rows are read only after it completes.  The kernel
+ * just before this call must therefore not write q after allowing early
+ * launch.
  */
 csa2_status csa2_attn_decode(const csa2_cache *cache, const uint16_t *q, int32_t H,
                              const int32_t *idx, const int32_t *cnt, int32_t kcap,
@@ -308,7 +314,7 @@ csa2_status csa2_attn_decode(const csa2_cache *cache, const uint16_t *q, int32_t
  * swa: E4M3 band [B, Tq + W - 1, D]; band row r holds position
  * q_pos[b][0] - (W - 1) + r, and query tq attends to band rows tq .. tq+W-1
  * whose positions are >= 0 (the W most recent positions up to itself).
- * out: fp32 [B, Tq, H, D], 16-byte aligned.
+ * out: fp32 [B, Tq, H, D], 16-byte aligned.  Ordering as csa2_attn_decode.
  */
 csa2_status csa2_attn_prefill(const csa2_cache *cache, const uint16_t *q, int32_t H, int32_t Tq,
                               const int32_t *q_pos, const int32_t *idx, const int32_t *cnt,
