@@ -42,13 +42,13 @@ HBM_FALLBACK_GBS = 6800.0
 EVENT_EVERY = 25  # timed steps per sampled pair of kernel events
 # DRAM bytes (read + write) per visible position of indexer_kernel<64,128,false>,
 # from one ncu capture of that kernel on 8 of the 32 sequences of the 128K
-# decode workload (134.53 MB read + 4.66 MB written for 1,048,592 positions;
+# decode workload (134.49 MB read + 4.41 MB written for 1,048,592 positions;
 # the indexer summary under profiles/).  Scaled to a launch by its visible
 # positions; must be re-measured whenever the kernel changes.
-INDEXER_TRAFFIC_B_PER_POS = 139.18592e6 / 1048592
-# The same figure for the MXFP4-key indexer (71.51 MB read + 1.17 MB written for
+INDEXER_TRAFFIC_B_PER_POS = 138.904064e6 / 1048592
+# The same figure for the MXFP4-key indexer (71.47 MB read + 0.73 MB written for
 # the same 1,048,592 positions; profiles/indexer_kernel_mxfp4-decode-b8-n131072.md).
-MX_INDEXER_TRAFFIC_B_PER_POS = 72.680704e6 / 1048592
+MX_INDEXER_TRAFFIC_B_PER_POS = 72.197888e6 / 1048592
 
 
 def peaks():
