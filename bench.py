@@ -743,7 +743,14 @@ def model_bench(args):
     every = max(1, min(EVENT_EVERY, args.steps // 8))
     sampled = lambda i: i % every == every // 2
     watch = {(20, "index"): K.KERNEL_INDEXER, (2, "index"): K.KERNEL_INDEXER,
-             (24, "index"): K.KERNEL_INDEXER, (21, "attention"): K.KERNEL_ATTENTION}
+             (24, "index"): K.KERNEL_INDEXER}
+    # one attention launch of each launch size (layers per launch), the
+    # decoder's first launch (layers 20..) among them
+    attn_key = {}
+    for c in sorted(sch.chunks, key=lambda c: c[0].layer != 20):
+        attn_key.setdefault(len(c), (c[0].layer, "attention"))
+    for key in attn_key.values():
+        watch[key] = K.KERNEL_ATTENTION
     n_ev = sum(1 for i in range(args.steps) if sampled(i))
     evs = {key: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                  for _ in range(max(n_ev, 1))] for key in watch}
@@ -819,10 +826,14 @@ def model_bench(args):
     us = {f"{l}:{ph}": statistics.mean(a.elapsed_time(b) for a, b in evs[(l, ph)][:n_ev]) * 1e3
           for (l, ph) in watch}
     value = job_throughput(layers_per * args.steps, world, ms)
-    # the dominant kernel: 38 attention launches per step against 8 indexer
-    # launches; attention flops per launch = 4 H (k + W) D per sequence
-    attn_flops = 4.0 * base.heads * (base.topk + base.window) * base.dim * B
-    attn_us = us["21:attention"]
+    # the dominant kernel: the attention launches (len(sch.chunks) per step,
+    # each over one to several layers) against 8 indexer launches; attention
+    # flops = 4 H (k + W) D per sequence and layer; the roofline is taken on
+    # the decoder's first launch (layers 20..)
+    dec_chunk = next(c for c in sch.chunks if c[0].layer == 20)
+    attn_flops = 4.0 * base.heads * (base.topk + base.window) * base.dim * B * len(dec_chunk)
+    attn_us = us["20:attention"]
+    attn_step_us = sum(us["%d:attention" % attn_key[len(c)][0]] for c in sch.chunks)
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             tf_peak, tf_kind = float(json.load(f)["bf16_tflops_sustained"]), "measured (sustained)"
@@ -833,10 +844,12 @@ def model_bench(args):
     roofline = {"bound": "tensor", "kernel": "attention_kernel", "achieved": ach, "peak": tf_peak,
                 "unit": "TFLOP/s", "frac": ach / tf_peak, "traffic": None, "peak_source": tf_kind,
                 "flops_per_launch": attn_flops, "launch_us": attn_us,
-                "share_of_step": 38 * attn_us / (ms / args.steps * 1e3),
+                "layers_per_launch": len(dec_chunk),
+                "share_of_step": attn_step_us / (ms / args.steps * 1e3),
                 "timed_launches": n_ev,
-                "sampling": f"CUDA events around layer 21's attention of every {every}th step, in "
-                            f"a second replay of the {args.steps} timed steps"}
+                "sampling": f"CUDA events around the attention launch of layers "
+                            f"{dec_chunk[0].layer}-{dec_chunk[-1].layer} of every {every}th step, "
+                            f"in a second replay of the {args.steps} timed steps"}
     del graph, graph_ev
 
     # ---- e2e through the API: per step the appended rows and every layer's
@@ -971,8 +984,13 @@ def model_bench(args):
             "roofline": roofline,
             "kernels_us": {"decoder_full_indexer": us["20:index"],
                            "encoder_full_indexer": us["2:index"],
-                           "reindex_indexer": us["24:index"], "attention": attn_us,
-                           "indexers_per_step": idx_total, "attention_per_step": 38 * attn_us},
+                           "reindex_indexer": us["24:index"],
+                           "attention_launch": {"layers %d-%d" % (c[0].layer, c[-1].layer):
+                                                us["%d:attention" % c[0].layer]
+                                                for c in sch.chunks
+                                                if (c[0].layer, "attention") in watch},
+                           "attention_launches_per_step": len(sch.chunks),
+                           "indexers_per_step": idx_total, "attention_per_step": attn_step_us},
             "e2e": {"value": e2e_value, "unit": "layer-steps/s",
                     "h2d_bytes_per_step": (h2d_even + h2d_odd) / 2, "d2h_bytes_per_step": d2h,
                     "steps": e_steps, "cuda_graph": e2e_graph is not None, "eager_value": e2e_eager,

@@ -71,6 +71,8 @@ _index_reindex = _sig("csa2_index_reindex", [_CP, _p, _p, _i32, _i32, _p, _p, _p
                                              _i32, _p, _p, _p, _p])
 _attn_decode = _sig("csa2_attn_decode", [_CP, _p, _i32, _p, _p, _i32, _p, _p, _i32,
                                          ctypes.c_float, _p, _p, _p])
+_attn_decode_layers = _sig("csa2_attn_decode_layers", [_CP, _i32, _p, _i32, _p, _p, _i32, _p, _p,
+                                                       _i32, ctypes.c_float, _p, _p, _p])
 _attn_prefill = _sig("csa2_attn_prefill", [_CP, _p, _i32, _i32, _p, _p, _p, _i32, _p, _i32,
                                            ctypes.c_float, _p, _p, _p])
 _get_status = _sig("csa2_get_status", [_p, ctypes.POINTER(ctypes.c_uint32), _p])
@@ -84,7 +86,7 @@ EXPORTED = ["csa2_workspace_size", "csa2_entry_bytes", "csa2_fp8_quant", "csa2_q
             "csa2_index_full", "csa2_index_reindex", "csa2_attn_decode", "csa2_attn_prefill",
             "csa2_get_status", "csa2_reset_status", "csa2_status_string",
             "csa2_set_launch_events", "csa2_index_full_noalloc", "csa2_quant_append_pairs",
-            "csa2_set_wait_limit"]
+            "csa2_set_wait_limit", "csa2_attn_decode_layers"]
 
 
 class Csa2Error(RuntimeError):
@@ -175,6 +177,26 @@ def attn_decode(cache, q, heads, idx, cnt, kcap, swa, swa_cnt, window, softmax_s
     _check(_attn_decode(ctypes.byref(cache.struct), _ptr(q), heads, _ptr(idx), _ptr(cnt), kcap,
                         _ptr(swa), _ptr(swa_cnt), window, float(softmax_scale), _ptr(out),
                         _ptr(ws), _stream(stream)), "csa2_attn_decode")
+
+
+MAX_ATTN_LAYERS = 8
+
+
+def attn_decode_layers(cache, qs, heads, idx, cnt, kcap, swas, swa_cnt, window, softmax_scale,
+                       outs, ws, stream=None):
+    """csa2_attn_decode_layers: qs, swas, outs are sequences of one tensor per
+    layer (the host pointer arrays are built here)."""
+    n = len(qs)
+    if not 1 <= n <= MAX_ATTN_LAYERS or len(outs) != n or len(swas) != n:
+        raise Csa2Error("csa2_attn_decode_layers: 1..%d layers, one q, swa and out each"
+                        % MAX_ATTN_LAYERS)
+    arr = ctypes.c_void_p * n
+    qa, sa, oa = arr(*[_ptr(x) for x in qs]), arr(*[_ptr(x) for x in swas]), arr(*[_ptr(x) for x in outs])
+    _check(_attn_decode_layers(ctypes.byref(cache.struct), n, ctypes.cast(qa, ctypes.c_void_p),
+                               heads, _ptr(idx), _ptr(cnt), kcap, ctypes.cast(sa, ctypes.c_void_p),
+                               _ptr(swa_cnt), window, float(softmax_scale),
+                               ctypes.cast(oa, ctypes.c_void_p), _ptr(ws), _stream(stream)),
+           "csa2_attn_decode_layers")
 
 
 def attn_prefill(cache, q, heads, tq, q_pos, idx, cnt, kcap, swa, window, softmax_scale, out, ws,

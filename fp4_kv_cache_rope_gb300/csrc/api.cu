@@ -195,19 +195,31 @@ csa2_status csa2_index_reindex(const csa2_cache* cache, const uint8_t* q_idx, co
                       n_batch, k, out_idx, out_cnt, nullptr, nullptr, ws, stream);
 }
 
-static csa2_status attn_common(const csa2_cache* cache, const uint16_t* q, int32_t H, int32_t Tq,
-                               const int32_t* q_pos, const int32_t* idx, const int32_t* cnt,
-                               int32_t kcap, const uint8_t* swa, const int32_t* swa_cnt,
-                               int32_t W, float scale, float* out, void* ws, void* stream) {
+static csa2_status attn_common(const csa2_cache* cache, int32_t L, const uint16_t* const* q,
+                               int32_t H, int32_t Tq, const int32_t* q_pos, const int32_t* idx,
+                               const int32_t* cnt, int32_t kcap, const uint8_t* const* swa,
+                               const int32_t* swa_cnt, int32_t W, float scale, float* const* out,
+                               void* ws, void* stream) {
   if (!cache_ok(cache) || !q || !idx || !cnt || !out || !ws) return CSA2_ERR_INVALID;
+  if (L < 1 || L > CSA2_MAX_ATTN_LAYERS) return CSA2_ERR_INVALID;
   if (H < 1 || H > 64 || kcap < 0 || W < 0 || Tq < 1) return CSA2_ERR_INVALID;
   if (W > 0 && !swa) return CSA2_ERR_INVALID;
-  if (!aligned16(q) || !aligned16(ws) || !aligned16(out) || (swa && !aligned16(swa)))
-    return CSA2_ERR_INVALID;
+  for (int l = 0; l < L; ++l) {
+    if (!q[l] || !out[l] || !aligned16(q[l]) || !aligned16(out[l])) return CSA2_ERR_INVALID;
+    if (W > 0 && (!swa[l] || !aligned16(swa[l]))) return CSA2_ERR_INVALID;
+  }
+  if (!aligned16(ws)) return CSA2_ERR_INVALID;
   if (isnan(scale)) return CSA2_ERR_INVALID;
   const int64_t rows = (int64_t)cache->batch * Tq;
+  if ((int64_t)L * rows > 65535) return CSA2_ERR_INVALID;
   AttnArgs a;
-  a.q = q;
+  a.n_layers = L;
+  for (int l = 0; l < CSA2_MAX_ATTN_LAYERS; ++l) {
+    const int k = l < L ? l : 0;
+    a.q[l] = q[k];
+    a.swa[l] = W > 0 ? swa[k] : nullptr;
+    a.out[l] = out[k];
+  }
   a.heads = H;
   a.n_rows = (int32_t)rows;
   a.tq = Tq;
@@ -215,13 +227,11 @@ static csa2_status attn_common(const csa2_cache* cache, const uint16_t* q, int32
   a.idx = idx;
   a.cnt = cnt;
   a.kcap = kcap;
-  a.swa = swa;
   a.swa_cnt = swa_cnt;
   a.window = W;
   a.scale = scale;
-  a.out = out;
-  const WsLayout L = layout_for(cache, rows);
-  return from_cuda(launch_attention(*cache, a, L, static_cast<uint8_t*>(ws), num_sms(),
+  const WsLayout Lw = layout_for(cache, rows);
+  return from_cuda(launch_attention(*cache, a, Lw, static_cast<uint8_t*>(ws), num_sms(),
                                     (cudaStream_t)stream));
 }
 
@@ -229,8 +239,18 @@ csa2_status csa2_attn_decode(const csa2_cache* cache, const uint16_t* q, int32_t
                              const int32_t* idx, const int32_t* cnt, int32_t kcap,
                              const uint8_t* swa, const int32_t* swa_cnt, int32_t W,
                              float softmax_scale, float* out, void* ws, void* stream) {
-  return attn_common(cache, q, H, 1, nullptr, idx, cnt, kcap, swa, swa_cnt, W, softmax_scale, out,
-                     ws, stream);
+  return attn_common(cache, 1, &q, H, 1, nullptr, idx, cnt, kcap, &swa, swa_cnt, W,
+                     softmax_scale, &out, ws, stream);
+}
+
+csa2_status csa2_attn_decode_layers(const csa2_cache* cache, int32_t L, const uint16_t* const* q,
+                                    int32_t H, const int32_t* idx, const int32_t* cnt,
+                                    int32_t kcap, const uint8_t* const* swa,
+                                    const int32_t* swa_cnt, int32_t W, float softmax_scale,
+                                    float* const* out, void* ws, void* stream) {
+  if (!q || !out || (W > 0 && !swa)) return CSA2_ERR_INVALID;
+  return attn_common(cache, L, q, H, 1, nullptr, idx, cnt, kcap, swa, swa_cnt, W, softmax_scale,
+                     out, ws, stream);
 }
 
 csa2_status csa2_attn_prefill(const csa2_cache* cache, const uint16_t* q, int32_t H, int32_t Tq,
@@ -239,8 +259,8 @@ csa2_status csa2_attn_prefill(const csa2_cache* cache, const uint16_t* q, int32_
                               float* out, void* ws, void* stream) {
   if (!q_pos) return CSA2_ERR_INVALID;
   if (W < 1) return CSA2_ERR_INVALID;
-  return attn_common(cache, q, H, Tq, q_pos, idx, cnt, kcap, swa, nullptr, W, softmax_scale, out,
-                     ws, stream);
+  return attn_common(cache, 1, &q, H, Tq, q_pos, idx, cnt, kcap, &swa, nullptr, W, softmax_scale,
+                     &out, ws, stream);
 }
 
 csa2_status csa2_get_status(void* ws, uint32_t* host_status, void* stream) {

@@ -106,17 +106,20 @@ struct AttnCfg {
 };
 
 struct AttnParams {
-  const uint16_t* q;
+  // per layer (the layers of one call share the selection and the cache):
+  // queries, window rows and outputs
+  const uint16_t* q[CSA2_MAX_ATTN_LAYERS];
+  const uint8_t* swa[CSA2_MAX_ATTN_LAYERS];
+  float* out[CSA2_MAX_ATTN_LAYERS];
+  int32_t n_layers;
   int32_t heads, n_rows, tq, batch;
   const int32_t* q_pos;
   const int32_t* idx;
   const int32_t* cnt;
   int32_t kcap;
-  const uint8_t* swa;
   const int32_t* swa_cnt;
   int32_t window;
   float scale_log2;  // softmax scale * log2(e)
-  float* out;
   int32_t splits;    // CTAs per query row (the cluster size)
   const uint8_t* codes;
   const uint8_t* scales;
@@ -131,7 +134,8 @@ struct RowKeys {
   const uint8_t* swa0;  // first window row of this query
 };
 
-__device__ __forceinline__ RowKeys row_keys(const AttnParams& p, int row, int D) {
+__device__ __forceinline__ RowKeys row_keys(const AttnParams& p, int row, int D,
+                                            const uint8_t* swa) {
   RowKeys r;
   const int b = row / p.tq, tq = row % p.tq;
   r.b = b;
@@ -146,7 +150,7 @@ __device__ __forceinline__ RowKeys row_keys(const AttnParams& p, int row, int D)
   if (p.q_pos == nullptr) {
     int w = p.swa_cnt ? p.swa_cnt[b] : p.window;
     r.n_swa = w < 0 ? 0 : (w > p.window ? p.window : w);
-    r.swa0 = p.swa + (int64_t)b * p.window * D;
+    r.swa0 = swa + (int64_t)b * p.window * D;
   } else {
     // band row r holds position q_pos[b][0] - (W - 1) + r; query tq sees band
     // rows tq .. tq + W - 1 with a position >= 0
@@ -155,7 +159,7 @@ __device__ __forceinline__ RowKeys row_keys(const AttnParams& p, int row, int D)
     lo = lo > tq ? lo : tq;
     const int hi = tq + p.window;  // exclusive
     r.n_swa = hi > lo ? hi - lo : 0;
-    r.swa0 = p.swa + ((int64_t)b * (p.tq + p.window - 1) + lo) * D;
+    r.swa0 = swa + ((int64_t)b * (p.tq + p.window - 1) + lo) * D;
   }
   return r;
 }
@@ -424,7 +428,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
     if (tid == 0) set_status(p.status, CSA2_DEV_BAD_ALIGN);
     return;
   }
-  const int row = blockIdx.y, split = blockIdx.x;
+  const int split = blockIdx.x;
+  const int layer = (int)blockIdx.y / p.n_rows;  // grid rows: layer-major, then query row
+  const int row = (int)blockIdx.y - layer * p.n_rows;
+  const uint16_t* q_l = p.q[0];
+  const uint8_t* swa_l = p.swa[0];
+  float* out_l = p.out[0];
+#pragma unroll
+  for (int l = 1; l < CSA2_MAX_ATTN_LAYERS; ++l)
+    if (l == layer) {
+      q_l = p.q[l];
+      swa_l = p.swa[l];
+      out_l = p.out[l];
+    }
 
   if (tid == 0) {
     mbar_init(s_full + 0, 1);
@@ -460,12 +476,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
   if (warp == 9 && lane == 1) {
     // the output row's first and last lines (their address translation is
     // then ready when the merge writes them)
-    const float* o0 = p.out + (int64_t)row * p.heads * D;
+    const float* o0 = out_l + (int64_t)row * p.heads * D;
     asm volatile("prefetch.global.L2 [%0];" ::"l"(o0));
     asm volatile("prefetch.global.L2 [%0];" ::"l"(o0 + (int64_t)p.heads * D - 1));
   }
   if (warp == 9 && lane == 0) {
-    const uint8_t* qg = reinterpret_cast<const uint8_t*>(p.q + (int64_t)row * p.heads * D);
+    const uint8_t* qg = reinterpret_cast<const uint8_t*>(q_l + (int64_t)row * p.heads * D);
     const uint32_t qbytes = (uint32_t)p.heads * D * 2;
     mbar_arrive_expect_tx(q_land, qbytes);
     for (uint32_t o = 0; o < qbytes; o += 32768u)
@@ -542,7 +558,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
     for (int e = g0s + 32 * lane; e < g1s; e += 32 * 32)
       asm volatile("prefetch.global.L1 [%0];" ::"l"(p.idx + (int64_t)row * p.kcap + e));
   }
-  const RowKeys rk = row_keys(p, row, D);
+  const RowKeys rk = row_keys(p, row, D, swa_l);
   const CtaKeys ck = cta_keys(rk, split, p.splits);
 
   if (warp < 8) {
@@ -908,7 +924,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
           if (head < p.heads) {
             const float lh = lrow[head];
             const float o = (any && lh > 0.0f) ? __uint_as_float(v[h]) / lh : 0.0f;
-            p.out[((int64_t)row * p.heads + head) * D + c] = o;
+            out_l[((int64_t)row * p.heads + head) * D + c] = o;
           }
         }
       }
@@ -1017,7 +1033,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(AttnParams p
 #pragma unroll
         for (int u = 0; u < kU; ++u)
           if (it0 + u * kAttnThreads < items)
-            *reinterpret_cast<float4*>(p.out + ((int64_t)row * p.heads + hh[u]) * D + c0 + 4 * cc[u]) = acc[u];
+            *reinterpret_cast<float4*>(out_l + ((int64_t)row * p.heads + hh[u]) * D + c0 + 4 * cc[u]) = acc[u];
       }
     }
   }
@@ -1050,13 +1066,13 @@ static cudaError_t run_attention(AttnParams p, cudaStream_t s) {
     int splits = p.splits;
     while (splits > 1) {
       if (!fits[splits]) fits[splits] = max_active_clusters(kern, splits, kAttnThreads, C::kSmem) + 1;
-      if (fits[splits] - 1 >= p.n_rows) break;
+      if (fits[splits] - 1 >= p.n_layers * p.n_rows) break;
       --splits;
     }
     p.splits = splits;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.splits, (unsigned)p.n_rows, 1);
+  cfg.gridDim = dim3((unsigned)p.splits, (unsigned)(p.n_layers * p.n_rows), 1);
   cfg.blockDim = dim3(kAttnThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)C::kSmem;
   cfg.stream = s;
@@ -1078,11 +1094,20 @@ static cudaError_t run_attention(AttnParams p, cudaStream_t s) {
 cudaError_t launch_attention(const csa2_cache& c, const AttnArgs& a, const WsLayout& L,
                              uint8_t* ws, int num_sms, cudaStream_t s) {
   if (a.n_rows <= 0) return cudaSuccess;
+  if (a.n_layers < 1 || a.n_layers > CSA2_MAX_ATTN_LAYERS) return cudaErrorInvalidValue;
+  // grid rows: one per (layer, query row)
+  if ((int64_t)a.n_layers * a.n_rows > 65535) return cudaErrorInvalidConfiguration;
   // the key table holds cache rows as int32
   const int64_t rows = c.page_size ? (int64_t)c.num_pages * c.page_size : (int64_t)c.batch * c.max_len;
   if (rows > 0x7FFFFFFFll) return cudaErrorInvalidValue;
   AttnParams p;
-  p.q = a.q;
+  p.n_layers = a.n_layers;
+  for (int l = 0; l < CSA2_MAX_ATTN_LAYERS; ++l) {
+    const int k = l < a.n_layers ? l : 0;
+    p.q[l] = a.q[k];
+    p.swa[l] = a.swa[k];
+    p.out[l] = a.out[k];
+  }
   p.heads = a.heads;
   p.n_rows = a.n_rows;
   p.tq = a.tq;
@@ -1091,13 +1116,12 @@ cudaError_t launch_attention(const csa2_cache& c, const AttnArgs& a, const WsLay
   p.idx = a.idx;
   p.cnt = a.cnt;
   p.kcap = a.kcap;
-  p.swa = a.swa;
   p.swa_cnt = a.swa_cnt;
   p.window = a.window;
   const float scale = a.scale > 0.0f ? a.scale : 1.0f / sqrtf((float)c.dim);
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.out = a.out;
-  int splits = num_sms / a.n_rows;
+  // as many CTAs per (layer, row) as fill the SMs once
+  int splits = (int)(num_sms / ((int64_t)a.n_layers * a.n_rows));
   splits = splits < 1 ? 1 : (splits > kMaxSplits ? kMaxSplits : splits);
   const int max_tiles = (a.kcap + a.window + kTile - 1) / kTile;
   if (splits > max_tiles) splits = max_tiles < 1 ? 1 : max_tiles;

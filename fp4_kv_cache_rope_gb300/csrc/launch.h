@@ -89,7 +89,11 @@ cudaError_t launch_select(const csa2_cache& c, const RowSet& rows, int mode, int
 
 // attention.cu
 struct AttnArgs {
-  const uint16_t* q;        // bf16 [rows, H, D]
+  // per layer (n_layers of them; the layers share idx, cnt and swa_cnt)
+  const uint16_t* q[CSA2_MAX_ATTN_LAYERS];    // bf16 [rows, H, D]
+  const uint8_t* swa[CSA2_MAX_ATTN_LAYERS];   // decode [B, W, D]; prefill band [B, Tq+W-1, D]
+  float* out[CSA2_MAX_ATTN_LAYERS];           // [rows, H, D]
+  int32_t n_layers;
   int32_t heads;
   int32_t n_rows;           // B * Tq
   int32_t tq;               // 1 for decode
@@ -97,11 +101,9 @@ struct AttnArgs {
   const int32_t* idx;       // [rows, kcap]
   const int32_t* cnt;       // [rows]
   int32_t kcap;
-  const uint8_t* swa;       // decode [B, W, D]; prefill band [B, Tq+W-1, D]
   const int32_t* swa_cnt;   // decode only, or null
   int32_t window;
   float scale;
-  float* out;               // [rows, H, D]
 };
 cudaError_t launch_attention(const csa2_cache& c, const AttnArgs& a, const WsLayout& L,
                              uint8_t* ws, int num_sms, cudaStream_t s);

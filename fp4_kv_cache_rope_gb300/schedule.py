@@ -20,7 +20,11 @@ section "CSA2 cross-layer KV and index reuse"):
   CSA2 layers the pages count).
 
 Every CSA2 layer computes its own query and SWA window and attends; Reuse
-layers take the most recent selection of their group.
+layers take the most recent selection of their group.  The layers of a group
+share one cache and one selection, so their attentions go to the GPU together:
+one ``csa2_attn_decode_layers`` launch serves up to ``floor(SMs / B)`` of them
+(at most ``MAX_ATTN_LAYERS``), which fills the SMs with whole sequences
+instead of splitting each sequence's keys over several CTAs and merging.
 """
 from __future__ import annotations
 
@@ -63,6 +67,20 @@ def layer_plan() -> list:
     return plan
 
 
+def attention_chunks(plan, per_launch: int) -> list:
+    """The plan's layers cut into attention launches: consecutive layers with
+    the same cache and selection, at most per_launch of them per launch."""
+    chunks = []
+    for p in plan:
+        c = chunks[-1] if chunks else None
+        if (c and len(c) < per_launch and c[0].cache == p.cache
+                and c[0].selection == p.selection):
+            c.append(p)
+        else:
+            chunks.append([p])
+    return chunks
+
+
 class DecodeSchedule:
     """Runs the 38 CSA2 layers of one decode token for a batch of sequences.
 
@@ -73,15 +91,20 @@ class DecodeSchedule:
     topk, window, heads, idx_heads: the layer shapes (shared by all layers).
     """
 
-    def __init__(self, caches, workspaces, heads, idx_heads, topk, window):
+    def __init__(self, caches, workspaces, heads, idx_heads, topk, window, layers_per_launch=None):
         import torch
-        from . import POOL_BLOCKS
+        from . import MAX_ATTN_LAYERS, POOL_BLOCKS
         assert len(caches) == 4 and len(workspaces) == 4
         self.caches, self.ws = caches, workspaces
         self.heads, self.idx_heads, self.topk, self.window = heads, idx_heads, topk, window
         self.plan = layer_plan()
         B = caches[3].batch
         dev = caches[3].codes.device
+        if layers_per_launch is None:
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            layers_per_launch = sms // B
+        self.layers_per_launch = max(1, min(MAX_ATTN_LAYERS, int(layers_per_launch)))
+        self.chunks = attention_chunks(self.plan, self.layers_per_launch)
         heads_ = {p.selection for p in self.plan}
         self.idx = {h: torch.zeros((B, topk), dtype=torch.int32, device=dev) for h in heads_}
         self.cnt = {h: torch.zeros((B,), dtype=torch.int32, device=dev) for h in heads_}
@@ -106,14 +129,18 @@ class DecodeSchedule:
                        and, for Full / Reindex layers, q_idx (E4M3 [B, 1, Hi, di])
                        and w (fp32 [B, 1, Hi]).
         out[layer]:    fp32 [B, H, D], written.
-        on_layer(plan_entry, phase): optional hook called around the calls
-                       ("index" / "attention", before and after), e.g. for events.
+        on_layer(plan_entry, phase, before): optional hook called before and
+                       after each call, e.g. for events.  phase "index" names
+                       the indexing layer; phase "attention" names the first
+                       layer of the launch (``self.chunks``).
         """
-        from . import attn_decode, index_full, index_reindex
+        from . import attn_decode, attn_decode_layers, index_full, index_reindex
         B, k = self.caches[3].batch, self.topk
-        for p in self.plan:
-            c, ws, inp = self.caches[p.cache], self.ws[p.cache], inputs[p.layer]
+        for chunk in self.chunks:
+            p = chunk[0]
+            c, ws = self.caches[p.cache], self.ws[p.cache]
             if p.mode != REUSE:
+                inp = inputs[p.layer]
                 h = p.selection
                 sel = self.idx[h].view(B, 1, k)
                 cnt = self.cnt[h].view(B, 1)
@@ -131,15 +158,22 @@ class DecodeSchedule:
                     on_layer(p, "index", False)
             if on_layer:
                 on_layer(p, "attention", True)
-            attn_decode(c, inp["q"], self.heads, self.idx[p.selection], self.cnt[p.selection], k,
-                        inp["swa"], None, self.window, 0.0, out[p.layer], ws)
+            if len(chunk) == 1:
+                inp = inputs[p.layer]
+                attn_decode(c, inp["q"], self.heads, self.idx[p.selection], self.cnt[p.selection],
+                            k, inp["swa"], None, self.window, 0.0, out[p.layer], ws)
+            else:
+                attn_decode_layers(c, [inputs[x.layer]["q"] for x in chunk], self.heads,
+                                   self.idx[p.selection], self.cnt[p.selection], k,
+                                   [inputs[x.layer]["swa"] for x in chunk], None, self.window,
+                                   0.0, [out[x.layer] for x in chunk], ws)
             if on_layer:
                 on_layer(p, "attention", False)
 
     def launches(self, pair_appended):
         """Kernel launches of one token (append clusters, 2 per index call, 1
-        per attention)."""
+        per attention launch)."""
         n = 1 + (3 if pair_appended else 0)
         n += sum(2 for p in self.plan if p.mode != REUSE)
-        n += len(self.plan)
+        n += len(self.chunks)
         return n

@@ -72,6 +72,7 @@ typedef enum csa2_status {
 
 /* Largest k and the pool capacity (blocks of 8 positions). */
 #define CSA2_MAX_TOPK 2048
+#define CSA2_MAX_ATTN_LAYERS 8   /* layers of one csa2_attn_decode_layers call */
 #define CSA2_POOL_BLOCKS 2048
 #define CSA2_BLOCK 8
 /* Longest sequence (positions) the selection kernels accept. */
@@ -306,6 +307,26 @@ csa2_status csa2_attn_decode(const csa2_cache *cache, const uint16_t *q, int32_t
                              const int32_t *idx, const int32_t *cnt, int32_t kcap,
                              const uint8_t *swa, const int32_t *swa_cnt, int32_t W,
                              float softmax_scale, float *out, void *ws, void *stream);
+
+/*
+ * Steps 4-5, decode, for L layers that attend over the same selection of the
+ * same cache: the CSA2 groups of "DeepSeek-V4.1-Flash: Pushing the Limits of
+ * KV Cache Compression" (knowledge note, section "CSA2: share cache, refresh
+ * selection only when needed"), where the Reuse layers that follow a Full or
+ * Reindex layer take its top-k unchanged.  Layer l gives exactly what
+ * csa2_attn_decode(cache, q[l], H, idx, cnt, kcap, swa[l], swa_cnt, W,
+ * softmax_scale, out[l], ws, stream) gives; one launch serves all L layers, so
+ * each (layer, sequence) row gets fewer split-K CTAs (none, when L * B rows
+ * fill the SMs) and the launch's fixed costs are paid once.
+ * L: 1..CSA2_MAX_ATTN_LAYERS.  q, swa, out: HOST arrays of L device pointers
+ * with the layouts of csa2_attn_decode; idx, cnt, swa_cnt shared.  L * B must
+ * not exceed 65,535.  Errors and ordering as csa2_attn_decode.
+ */
+csa2_status csa2_attn_decode_layers(const csa2_cache *cache, int32_t L, const uint16_t *const *q,
+                                    int32_t H, const int32_t *idx, const int32_t *cnt,
+                                    int32_t kcap, const uint8_t *const *swa,
+                                    const int32_t *swa_cnt, int32_t W, float softmax_scale,
+                                    float *const *out, void *ws, void *stream);
 
 /*
  * Steps 4-5, prefill chunk: as csa2_attn_decode for Tq query rows per

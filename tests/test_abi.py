@@ -57,6 +57,20 @@ def test_host_validation_without_gpu(lib):
     assert r == K.CSA2_ERR_INVALID
     r = K._attn_decode(ctypes.byref(c), 16, 65, 16, 16, 64, 16, None, 128, 0.0, 16, 16, None)
     assert r == K.CSA2_ERR_INVALID
+    # the layer-grouped attention: 1..MAX_ATTN_LAYERS layers, every pointer given
+    P = ctypes.c_void_p * 9
+    ptrs = P(*([16] * 9))
+    for n in (0, K.MAX_ATTN_LAYERS + 1):
+        r = K._attn_decode_layers(ctypes.byref(c), n, ptrs, 64, 16, 16, 64, ptrs, None, 128, 0.0,
+                                  ptrs, 16, None)
+        assert r == K.CSA2_ERR_INVALID
+    holes = P(16, None, *([16] * 7))
+    r = K._attn_decode_layers(ctypes.byref(c), 2, holes, 64, 16, 16, 64, ptrs, None, 128, 0.0,
+                              ptrs, 16, None)
+    assert r == K.CSA2_ERR_INVALID
+    r = K._attn_decode_layers(ctypes.byref(c), 2, ptrs, 64, 16, 16, 64, ptrs, None, 128, 0.0,
+                              holes, 16, None)
+    assert r == K.CSA2_ERR_INVALID
     assert K.entry_bytes(512) == 288 and K.entry_bytes(576) == 324
     assert K.status_string(K.CSA2_ERR_INVALID) == "invalid argument"
 

@@ -27,12 +27,13 @@ from synth.model import ModelInputs  # noqa: E402
 from synth.workloads import Workload, get_workload  # noqa: E402
 
 
-def run_two_tokens(base):
+def run_two_tokens(base, per_launch=None):
     """Two decode tokens (n even, then n + 1 completing a pair) through the 38
-    CSA2 layers; returns the model inputs and the schedule after the second."""
+    CSA2 layers; returns the model inputs and the schedule after the second.
+    per_launch: layers per attention launch (None: as many as fill the SMs)."""
     m = ModelInputs(base)
     sch = DecodeSchedule(m.caches, m.workspaces, base.heads, base.idx_heads, base.topk,
-                         base.window)
+                         base.window, per_launch)
     n = list(base.lengths)
     for step in range(2):
         pos = [x + step for x in n]
@@ -91,17 +92,22 @@ def check_layers(base, m, sch, seqs):
     return compared, total
 
 
-def test_two_decode_tokens_through_all_layers():
+@pytest.mark.parametrize("per_launch", [None, 1, 4])
+def test_two_decode_tokens_through_all_layers(per_launch):
+    """One layer per attention launch, four, and as many as the group holds
+    (None: six encoder layers, four decoder layers per launch at B = 2)."""
     base = Workload("model-mini", 2, [3000, 520], 128, 32, 8, 64, 16, 64, 16, seed=61,
                     outlier_frac=0.02, extra_capacity=8)
-    m, sch = run_two_tokens(base)
+    m, sch = run_two_tokens(base, per_launch)
     compared, total = check_layers(base, m, sch, range(base.batch))
     assert compared == total == 38 * base.batch
 
 
 def test_whole_model_at_full_size():
     """The bench's whole-model workload (B = 32 sequences of 131,072 tokens):
-    two decode tokens through all 38 layers, sequences 0 and 31 checked."""
+    two decode tokens through all 38 layers, sequences 0 and 31 checked, in
+    the bench's launch configuration (four layers per attention launch on 152
+    SMs)."""
     base = get_workload(9)
     base.extra_capacity = 8
     m, sch = run_two_tokens(base)

@@ -43,3 +43,24 @@ def test_groups(S):
         for l in range(head, head + 4):
             assert plan[l].cache == 3 and plan[l].selection == head
     assert all(plan[l].mode == S.REUSE for l in plan if l not in (2, 8, 14, 20, 24, 28, 32, 36))
+
+
+@pytest.mark.parametrize("per_launch", [1, 2, 3, 4, 8])
+def test_attention_chunks(S, per_launch):
+    """Attention launches cover the 38 layers in order; a launch never mixes
+    caches or selections and holds at most per_launch layers; the index call
+    of a group precedes all of its launches (the group's head leads its first
+    launch)."""
+    plan = S.layer_plan()
+    chunks = S.attention_chunks(plan, per_launch)
+    assert [p for c in chunks for p in c] == plan
+    for c in chunks:
+        assert 1 <= len(c) <= per_launch
+        assert len({(p.cache, p.selection) for p in c}) == 1
+        assert all(p.mode == S.REUSE for p in c[1:])
+    heads = [c[0].layer for c in chunks if c[0].mode != S.REUSE]
+    assert heads == [2, 8, 14, 20, 24, 28, 32, 36]
+    # fewest launches the groups allow: ceil(6 / n) per encoder group,
+    # ceil(4 / n) per decoder group
+    up = lambda a: -(-a // per_launch)
+    assert len(chunks) == 3 * up(6) + 5 * up(4)
