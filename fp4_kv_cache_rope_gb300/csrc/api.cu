@@ -103,6 +103,7 @@ csa2_status csa2_set_wait_limit(uint64_t ns) {
   const unsigned long long v = ns == 0 ? (unsigned long long)kWaitNs : (unsigned long long)ns;
   cudaError_t e = set_wait_limit_indexer(v);
   if (e == cudaSuccess) e = set_wait_limit_attention(v);
+  if (e == cudaSuccess) e = set_wait_limit_quant(v);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   return from_cuda(e);
 }
@@ -129,7 +130,7 @@ csa2_status csa2_quant_append(const csa2_cache* cache, const float* kv, const fl
   uint8_t* w = static_cast<uint8_t*>(ws);
   const WsLayout L = layout_for(cache, 1);
   return from_cuda(launch_quant_append(*cache, kv, nullptr, idx_k_in, T,
-                                       reinterpret_cast<uint32_t*>(w + L.status),
+                                       reinterpret_cast<uint32_t*>(w + L.status), num_sms(),
                                        (cudaStream_t)stream));
 }
 
@@ -144,7 +145,7 @@ csa2_status csa2_quant_append_pairs(const csa2_cache* cache, const float* kv, co
   uint8_t* w = static_cast<uint8_t*>(ws);
   const WsLayout L = layout_for(cache, 1);
   return from_cuda(launch_quant_append(*cache, kv, z, idx_k_in, T,
-                                       reinterpret_cast<uint32_t*>(w + L.status),
+                                       reinterpret_cast<uint32_t*>(w + L.status), num_sms(),
                                        (cudaStream_t)stream));
 }
 

@@ -40,19 +40,28 @@ __device__ __forceinline__ float e4m3_decode(uint32_t c) {
   return (c & 0x80u) ? -v : v;
 }
 
-// fp32 quotient -> 4-bit E2M1 code (bit 3 = sign).
-__device__ __forceinline__ uint32_t e2m1_encode(float q) {
-  const float a = fabsf(q);
-  uint32_t m;
-  if (a <= 0.25f) m = 0;
-  else if (a < 0.75f) m = 1;
-  else if (a <= 1.25f) m = 2;
-  else if (a < 1.75f) m = 3;
-  else if (a <= 2.5f) m = 4;
-  else if (a < 3.5f) m = 5;
-  else if (a <= 5.0f) m = 6;
-  else m = 7;
-  return m | ((__float_as_uint(q) >> 28) & 8u);
+// Two fp32 values -> one byte of E2M1 codes (lo in bits 0-3, hi in bits
+// 4-7): the hardware conversion, round to nearest with ties to the even code
+// (magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6; midpoints 0.25 and 1.25 and 2.5 and
+// 5 go down, 0.75 and 1.75 and 3.5 go up), saturating at +-6, sign kept (also
+// for values that round to zero).
+__device__ __forceinline__ uint32_t e2m1x2_from_f32(float lo, float hi) {
+  uint32_t out;
+  asm("{\n.reg .b8 t;\ncvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\ncvt.u32.u8 %0, t;\n}"
+      : "=r"(out)
+      : "f"(hi), "f"(lo));
+  return out;
+}
+
+// Two fp32 values -> two E4M3 bytes (lo in bits 0-7, hi in bits 8-15): the
+// hardware conversion, round to nearest even, saturating at +-448 -- the
+// same bytes as e4m3_encode.
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+  uint32_t out;
+  asm("{\n.reg .b16 t;\ncvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\ncvt.u32.u16 %0, t;\n}"
+      : "=r"(out)
+      : "f"(hi), "f"(lo));
+  return out;
 }
 
 // Two E2M1 codes packed in one byte (low nibble first) -> f16x2 (low half

@@ -55,6 +55,7 @@ inline int max_active_clusters(Kernel kern, int cluster, int threads, int smem) 
 // Limit of the bounded on-chip waits of each kernel file (0 = the default).
 cudaError_t set_wait_limit_indexer(unsigned long long ns);
 cudaError_t set_wait_limit_attention(unsigned long long ns);
+cudaError_t set_wait_limit_quant(unsigned long long ns);
 
 // Benchmark instrumentation (api.cu): records the family's begin/end events
 // on stream s when they are set.
@@ -64,7 +65,7 @@ void record_launch_end(int family, cudaStream_t s);
 // quant.cu
 cudaError_t launch_fp8_quant(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
 cudaError_t launch_quant_append(const csa2_cache& c, const float* kv, const float* z,
-                                const float* idx_in, int32_t T, uint32_t* status,
+                                const float* idx_in, int32_t T, uint32_t* status, int num_sms,
                                 cudaStream_t s);
 
 // Description of the query rows of one indexer call.

@@ -169,13 +169,15 @@ csa2_status csa2_fp8_quant(const float *x, int64_t n, uint8_t *out, void *stream
  * saturating, sign copied), all codes 0 when the scale decodes to 0.
  * Afterwards seq_len[b] += T.  A row with p >= max_len is skipped and sets
  * CSA2_DEV_OVERFLOW.
- * Ordering: small appends (decode sizes) are launched so that they may start
- * while the previous kernel on the stream finishes, when that kernel allows
- * its dependents to launch early (the library's own kernels do); they read
- * kv / idx_k_in and write the new rows before waiting for it, and update
- * seq_len only after it completes.  The kernel just before this call must
- * therefore not write kv or idx_k_in after allowing early launch (kernels
- * that do not use programmatic launch never overlap it).
+ * Ordering: appends are launched so that they may start while the previous
+ * kernel on the stream finishes, when that kernel allows its dependents to
+ * launch early (the library's own kernels do).  They read kv / idx_k_in
+ * before waiting for it; small appends (decode sizes) also write the new rows
+ * before the wait, large ones write them after reading seq_len behind the
+ * wait; seq_len is updated only after the previous kernel completes.  The
+ * kernel just before this call must therefore not write kv or idx_k_in after
+ * allowing early launch (kernels that do not use programmatic launch never
+ * overlap it).
  */
 csa2_status csa2_quant_append(const csa2_cache *cache, const float *kv, const float *idx_k_in,
                               int32_t T, void *ws, void *stream);

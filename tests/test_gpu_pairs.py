@@ -100,13 +100,16 @@ def test_pairs_decode_append_one_entry():
         assert np.array_equal(codes[:, : wl.dim // 2], rc) and np.array_equal(scales[:, :36], rs)
 
 
-def test_pairs_logit_edges_bit_exact():
+@pytest.mark.parametrize("T", [64, 320], ids=["cluster-kernel", "streaming-kernel"])
+def test_pairs_logit_edges_bit_exact(T):
     """Source rows with hand-built logits: equal, +-0 differences, tiny, around
-    the 80 cut, huge; compared with the oracle's compress + quantise."""
-    wl = enc_workload([64], 0, seed=53)
+    the 80 cut, huge; compared with the oracle's compress + quantise.  64
+    entries go through the small-append kernel, 320 through the streaming
+    kernel (rows staged in shared memory)."""
+    wl = enc_workload([T], 0, seed=53)
     dw = DeviceWorkload(wl, build_cache=False)
     rng = np.random.default_rng(53)
-    T, D = 64, wl.dim
+    D = wl.dim
     x = (rng.standard_normal((2 * T, D)) * 3).astype(np.float32)
     z0 = (rng.standard_normal((T, D)) * 4).astype(np.float32)
     diffs = np.array([0.0, -0.0, 1e-7, -1e-7, 1e-3, 79.9, 80.0, 80.1, -80.2, 200.0, -1e30, 0.5],

@@ -17,8 +17,10 @@ format, so these rows are built by hand:
 * rows appended at position 0 and at position max_len - 1, with edge values
   in the rotated channels too.
 
-Both append kernels are covered (one large append, then decode appends of
-one row per sequence), on a contiguous and on a paged cache.  Codes and scale
+The append kernels are covered: one large append (the streaming kernel),
+then decode appends of one row per sequence (the cluster kernel), on a
+contiguous and on a paged cache; and a large append whose cos / sin rows
+cannot be bulk-copied (the per-thread kernel).  Codes and scale
 bytes are compared with the oracle's quantiser bit for bit; the indexer-key
 bytes written by the same calls are compared with the oracle's E4M3 cast.
 """
@@ -147,3 +149,25 @@ def test_main_kv_quantiser_edges_bit_exact(page):
     # the edges were actually reached
     _, rs = O.quant_append_rows(kv[0], np.arange(L), dw.rope_cos, dw.rope_sin, R)
     assert (rs == 0x7E).any() and (rs == 0).any() and ((rs > 0) & (rs < 8)).any()
+
+
+def test_large_append_per_thread_kernel():
+    """A RoPE slice of 12 channels: cos / sin rows of 24 bytes are no multiple
+    of 16, so a large append takes the per-thread kernel instead of the
+    streaming one.  Codes, scales and indexer keys bit-exact."""
+    r12, n = 12, 300
+    wl = Workload("quant-rope12", 1, [n], D, r12, 64, DI, 64, 64, 128, seed=73)
+    dw = DeviceWorkload(wl, build_cache=False)
+    rng = np.random.default_rng(73)
+    kv = edge_rows(rng, n)
+    ik = idx_edge_rows(rng, n)
+    K.quant_append(dw.seq_view(0), torch.from_numpy(kv).cuda(), torch.from_numpy(ik).cuda(), n,
+                   dw.ws)
+    torch.cuda.synchronize()
+    assert K.get_status(dw.ws) == 0
+    assert int(dw.cache.seq_len[0]) == n
+    pos = np.arange(n)
+    codes, scales, idxk = read_rows(dw.cache, 0, pos)
+    rc, rs = O.quant_append_rows(kv, pos, dw.rope_cos, dw.rope_sin, r12)
+    assert np.array_equal(codes, rc) and np.array_equal(scales, rs)
+    assert np.array_equal(idxk, O.fp8_cast(ik))
