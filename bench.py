@@ -446,6 +446,9 @@ def roofline_bytes_per_step(wl, n_at):
 
 
 # ------------------------------------------------------------- CPU baseline
+ORACLE_FORM = ("the C++ oracle (oracle/cref.cpp: fp64 loops, one thread per core, pinned "
+               "against the numpy oracle); the m = 2 pair combination of encoder entries "
+               "stays numpy")
 def cpu_baseline(wl, per_piece_s=2.0):
     """The oracle on the host cores over one bounded sample of the workload's
     layer-step: the pieces of oracle_plan (the same plan the reference arm
@@ -457,23 +460,23 @@ def cpu_baseline(wl, per_piece_s=2.0):
         run()
         times.append(time.perf_counter() - t0)
     step_s = sum(w * t for (_, w), t in zip(pieces, times))
-    return {"value": layers / step_s, "unit": "layer-steps/s", "cores": os.cpu_count(),
+    from oracle import cref as CR
+    return {"value": layers / step_s, "unit": "layer-steps/s", "cores": CR.threads(),
             "kind": "oracle",
-            "sample": f"{text}; each of the {len(pieces)} pieces run once, numpy fp64 with the "
-                      f"host BLAS threads",
+            "sample": f"{text}; each of the {len(pieces)} pieces run once, {ORACLE_FORM}",
             "seconds_sampled": sum(times)}
 
 
 def _score_fn(wl, inp, ik, tq=0):
-    """Oracle indexer scores of query row tq against key positions [lo, hi)."""
-    from oracle import csa2 as O
+    """Oracle indexer scores (the C++ restatement, one thread per core) of
+    query row tq against key positions [lo, hi)."""
+    from oracle import cref as CR
 
     def score(lo, hi):
         if wl.idx_format == "mxfp4":
-            q = O.e4m3_decode(inp["q_idx"][tq]).reshape(wl.idx_heads, -1)
-            return O.indexer_scores_values(q, inp["w"][tq], O.dequantize_mxfp4(
-                ik[0][lo:hi], ik[1][lo:hi], wl.idx_dim))
-        return O.indexer_scores(inp["q_idx"][tq], inp["w"][tq], ik[lo:hi])
+            return CR.indexer_scores_mx(inp["q_idx"][tq], inp["w"][tq], ik[0][lo:hi],
+                                        ik[1][lo:hi], wl.idx_dim)
+        return CR.indexer_scores(inp["q_idx"][tq], inp["w"][tq], ik[lo:hi])
     return score
 
 
@@ -501,12 +504,16 @@ def oracle_plan(wl, per_step_s):
     length).  Inputs are prepared outside the pieces."""
     import numpy as np
     import synth
-    from oracle import csa2 as O
+    from oracle import cref as CR
     from oracle.formats import bf16_bits_to_f64
-    from oracle.workload import SeqRef
+    from oracle.workload import SeqRef as SeqRefNumpy
     from synth.host import host_rows_normal, supplied_pool, supplied_prior
     from synth.workloads import FULL, REINDEX, REUSE
     B, k = wl.batch, wl.topk
+    CR.build()
+
+    def SeqRef(*a, **kw):   # every arithmetic step through the C++ oracle
+        return SeqRefNumpy(*a, cpp=True, **kw)
 
     if wl.name.startswith("model-"):
         run = model_oracle_sample(wl, 0, wl.lengths[0])
@@ -521,12 +528,13 @@ def oracle_plan(wl, per_step_s):
         s_full = score(0, n)
         newrow = host_rows_normal(wl.seed, synth.T_KV, b, [n], wl.dim, ref.mult)
         q64 = bf16_bits_to_f64(inp["q_bf16"][0])
-        swa = O.swa_rows_decode(inp["swa"][: wl.window])
+        swa_codes = inp["swa"][: wl.window]
 
         def tail():
-            O.quant_append_rows(newrow, np.array([n]), ref.cos, ref.sin, wl.rope_dim)
-            idx, pool = O.full_select(s_full, k)
-            return O.sparse_attention(q64, np.concatenate([ref.dequant_rows(idx), swa]))
+            CR.quant_append_rows(newrow, np.array([n]), ref.cos, ref.sin, wl.rope_dim)
+            idx, pool = CR.full_select(s_full, k)
+            return CR.sparse_attention(q64, np.concatenate([ref.dequant_rows(idx),
+                                                            CR.e4m3_decode(swa_codes)]))
         return ref, score, s_full, tail
 
     def attend(ref, layer, idx, tq=0, tq_total=1):
@@ -551,11 +559,11 @@ def oracle_plan(wl, per_step_s):
         pieces = [(f, total_vis / vis) for f in _slices(score, vis, per_step_s)]
 
         def tail():
-            idx, pool = O.full_select(s_full, k)
+            idx, pool = CR.full_select(s_full, k)
             return ref.attention(0, idx, tq=tm, tq_total=T)
         pieces.append((tail, B * T))
-        pieces.append((lambda: O.quant_append_rows(rows, np.arange(n0, n0 + T), ref.cos, ref.sin,
-                                                   wl.rope_dim), B))
+        pieces.append((lambda: CR.quant_append_rows(rows, np.arange(n0, n0 + T), ref.cos, ref.sin,
+                                                    wl.rope_dim), B))
         return pieces, len(wl.layers), (
             f"query row {tm} of the {T}-token chunk: its scan of {vis} positions in "
             f"{len(pieces) - 2} slices weighted by the chunk's summed visible length, its "
@@ -569,7 +577,7 @@ def oracle_plan(wl, per_step_s):
         text = (f"sequence 0 of {B}: its Full scan of {n} positions in {len(pieces) - 1} slices, "
                 f"then append + select + dequantise + attend; each piece weighted by {B}")
         if len(wl.layers) > 1:   # the group: Reindex over the Full layer's pool, then Reuse
-            idx, pool = O.full_select(s_full, k)
+            idx, pool = CR.full_select(s_full, k)
             _, _, r_idx = ref.reindex(1, pool, k)
 
             def reindex():
@@ -644,9 +652,9 @@ def reference_arm(args, budget_s=90.0):
         times[j].append(time.perf_counter() - t0)
     step_s = sum(w * statistics.mean(t) for (_, w), t in zip(pieces, times))
     value = layers / step_s
-    sample = (f"step i = piece i mod {len(pieces)} of one layer-step: {text}; numpy fp64 with "
-              f"the host BLAS threads")
-    cpu = {"value": value, "unit": "layer-steps/s", "cores": os.cpu_count(), "kind": "oracle",
+    sample = f"step i = piece i mod {len(pieces)} of one layer-step: {text}; {ORACLE_FORM}"
+    from oracle import cref as CR
+    cpu = {"value": value, "unit": "layer-steps/s", "cores": CR.threads(), "kind": "oracle",
            "sample": sample}
     line = {"impl": "reference",
             "metric": ("CSA2 decode layer-steps/s (achieved HBM GB/s vs GB300 peak in roofline)"
@@ -675,15 +683,12 @@ def model_oracle_sample(base, b, positions_n):
     """One sequence of one model decode token on the oracle: the 38 CSA2
     layers (4 Full scans, 4 Reindex scans, 38 attentions) over caches holding
     positions_n tokens.  Inputs are prepared untimed; returns the timed work."""
-    import numpy as np
-    from oracle import csa2 as O
-    from oracle.formats import bf16_bits_to_f64
     from oracle.workload import SeqRef
     from fp4_kv_cache_rope_gb300.schedule import FULL, REINDEX, layer_plan
     from synth.model import model_workloads
     wls = model_workloads(base)
     entries = [positions_n // 2] * 3 + [positions_n]
-    refs = [SeqRef(wl, b, n=entries[c]) for c, wl in enumerate(wls)]
+    refs = [SeqRef(wl, b, n=entries[c], cpp=True) for c, wl in enumerate(wls)]
     plan = layer_plan()
     for p in plan:
         refs[p.cache].inputs(p.layer)

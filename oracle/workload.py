@@ -11,6 +11,7 @@ import synth
 from synth.host import host_layer_inputs, host_rows_normal
 from synth.workloads import Workload
 
+from . import cref as CR
 from . import csa2 as O
 from . import formats as F
 
@@ -18,7 +19,12 @@ from . import formats as F
 class SeqRef:
     """Reference quantities of sequence ``b`` of workload ``wl``."""
 
-    def __init__(self, wl: Workload, b: int, n: int | None = None, cos=None, sin=None):
+    def __init__(self, wl: Workload, b: int, n: int | None = None, cos=None, sin=None,
+                 cpp: bool = False):
+        # cpp: the arithmetic steps (FP4 append, scores, selection,
+        # dequantisation, attention) through the C++ restatement
+        # (oracle/cref.cpp) instead of numpy; the inputs are the same
+        self.cpp = cpp
         self.wl, self.b = wl, b
         self.n = wl.lengths[b] if n is None else n
         self.mult = (synth.outlier_multipliers(wl.seed, wl.dim, wl.outlier_frac)
@@ -42,7 +48,8 @@ class SeqRef:
             x = O.compress_pairs(x, z)
         else:
             x = host_rows_normal(self.wl.seed, synth.T_KV, self.b, positions, self.wl.dim, self.mult)
-        return O.quant_append_rows(x, positions, self.cos, self.sin, self.wl.rope_dim)
+        qa = CR.quant_append_rows if self.cpp else O.quant_append_rows
+        return qa(x, positions, self.cos, self.sin, self.wl.rope_dim)
 
     @property
     def mx_keys(self):
@@ -65,6 +72,11 @@ class SeqRef:
 
     def _scores_of(self, inp, tq, keys):
         """Scores of query ``tq`` against stored keys (either format)."""
+        if self.cpp:
+            if self.mx_keys:
+                return CR.indexer_scores_mx(inp["q_idx"][tq], inp["w"][tq], keys[0], keys[1],
+                                            self.wl.idx_dim)
+            return CR.indexer_scores(inp["q_idx"][tq], inp["w"][tq], keys)
         if self.mx_keys:
             q = F.e4m3_decode(inp["q_idx"][tq]).reshape(self.wl.idx_heads, -1)
             return O.indexer_scores_values(
@@ -73,7 +85,7 @@ class SeqRef:
 
     def dequant_rows(self, positions):
         codes, scales = self.cache_rows(positions)
-        return O.dequantize_fp4(codes, scales, self.wl.dim)
+        return (CR if self.cpp else O).dequantize_fp4(codes, scales, self.wl.dim)
 
     # ---- one layer ---------------------------------------------------------
     def inputs(self, layer, tq=1):
@@ -91,7 +103,7 @@ class SeqRef:
 
     def full(self, layer, k, n=None, tq=0, tq_total=1):
         s = self.scores(layer, n, tq, tq_total)
-        idx, pool = O.full_select(s, k)
+        idx, pool = (CR if self.cpp else O).full_select(s, k)
         return s, idx, pool
 
     def reindex(self, layer, pool, k, n=None, tq=0, tq_total=1):
@@ -106,7 +118,7 @@ class SeqRef:
         else:
             kp = self.idxk_rows(pos)
         s = self._scores_of(inp, tq, kp)
-        return s, pos, O.topk(s, k, ids=pos)
+        return s, pos, (CR if self.cpp else O).topk(s, k, ids=pos)
 
     def attention(self, layer, idx, swa_count=None, tq=0, tq_total=1, scale=None):
         """Decode attention (tq_total == 1) or prefill row tq."""
@@ -114,13 +126,14 @@ class SeqRef:
         wl = self.wl
         q = synth_bf16_to_f64(inp["q_bf16"][tq])
         rows = [self.dequant_rows(np.asarray(idx))] if len(idx) else [np.zeros((0, wl.dim))]
+        swa_decode = CR.e4m3_decode if self.cpp else O.swa_rows_decode
         if tq_total == 1:
             wc = wl.window if swa_count is None else swa_count
-            rows.append(O.swa_rows_decode(inp["swa"][:wc]))
+            rows.append(swa_decode(inp["swa"][:wc]))
         else:
             band = O.swa_band_rows(self.n_prior_positions, tq, wl.window)
-            rows.append(O.swa_rows_decode(inp["swa"][band]))
-        return O.sparse_attention(q, np.concatenate(rows), scale)
+            rows.append(swa_decode(inp["swa"][band]))
+        return (CR if self.cpp else O).sparse_attention(q, np.concatenate(rows), scale)
 
     n_prior_positions = 0
 

@@ -85,3 +85,15 @@ def test_cuda_sources_include_nothing_from_the_oracle():
             for line in open(os.path.join(csrc, f)):
                 if re.match(r"\s*#\s*include", line):
                     assert "oracle" not in line, (f, line)
+
+
+def test_oracle_cpp_includes_nothing_from_the_product():
+    """The C++ oracle includes only system headers: nothing from csrc/,
+    include/ or the product package."""
+    odir = os.path.join(ROOT, "oracle")
+    srcs = [f for f in os.listdir(odir) if f.endswith((".c", ".cc", ".cpp", ".h", ".hpp"))]
+    assert srcs, "no C++ oracle source"
+    for f in srcs:
+        for line in open(os.path.join(odir, f)):
+            if re.match(r"\s*#\s*include", line):
+                assert "<" in line and '"' not in line, (f, line)
