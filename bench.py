@@ -449,22 +449,28 @@ def roofline_bytes_per_step(wl, n_at):
 ORACLE_FORM = ("the C++ oracle (oracle/cref.cpp: fp64 loops, one thread per core, pinned "
                "against the numpy oracle); the m = 2 pair combination of encoder entries "
                "stays numpy")
-def cpu_baseline(wl, per_piece_s=2.0):
+def cpu_baseline(wl, per_piece_s=2.0, target_s=10.0, max_rounds=200):
     """The oracle on the host cores over one bounded sample of the workload's
     layer-step: the pieces of oracle_plan (the same plan the reference arm
-    times), each run once and weighted by the share of the step it stands for."""
+    times), run in rounds until about target_s of CPU work is sampled, each
+    piece's mean time weighted by the share of the step it stands for."""
     pieces, layers, text = oracle_plan(wl, per_piece_s)
-    times = []
-    for run, _w in pieces:
-        t0 = time.perf_counter()
-        run()
-        times.append(time.perf_counter() - t0)
-    step_s = sum(w * t for (_, w), t in zip(pieces, times))
+    times = [[] for _ in pieces]
+    total, rounds = 0.0, 0
+    while rounds < max_rounds and (rounds == 0 or total < target_s):
+        for j, (run, _w) in enumerate(pieces):
+            t0 = time.perf_counter()
+            run()
+            dt = time.perf_counter() - t0
+            times[j].append(dt)
+            total += dt
+        rounds += 1
+    step_s = sum(w * statistics.mean(t) for (_, w), t in zip(pieces, times))
     from oracle import cref as CR
     return {"value": layers / step_s, "unit": "layer-steps/s", "cores": CR.threads(),
             "kind": "oracle",
-            "sample": f"{text}; each of the {len(pieces)} pieces run once, {ORACLE_FORM}",
-            "seconds_sampled": sum(times)}
+            "sample": f"{text}; the {len(pieces)} pieces run in {rounds} rounds, {ORACLE_FORM}",
+            "seconds_sampled": total}
 
 
 def _score_fn(wl, inp, ik, tq=0):
@@ -624,10 +630,11 @@ def oracle_plan(wl, per_step_s):
 
 def reference_arm(args, budget_s=90.0):
     """The oracle on the host cores.  Step i runs piece i mod P of the
-    workload's layer-step (oracle_plan), with the pieces sized so that the
-    warm-up and timed steps together take about budget_s whatever --steps is.
-    `value` is layer-steps/s from each piece's mean time and weight;
-    `ms_per_step` is the measured wall time of one timed step (one piece)."""
+    workload's layer-step (oracle_plan), with the pieces sized (and a short
+    piece repeated within its step) so that the warm-up and timed steps
+    together take about budget_s whatever --steps is.  `value` is
+    layer-steps/s from each piece's mean time and weight; `ms_per_step` is
+    the measured wall time of one timed step."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
@@ -635,15 +642,22 @@ def reference_arm(args, budget_s=90.0):
     wl = get_workload(args.workload)
     per_step = budget_s / max(1, args.steps + args.warmup)
     pieces, layers, text = oracle_plan(wl, per_step)
+    # a piece shorter than the per-step share runs several times per step
+    reps = []
+    for j, (run, _w) in enumerate(pieces):
+        t0 = time.perf_counter()
+        run()
+        reps.append(max(1, min(1000, int(per_step / max(time.perf_counter() - t0, 1e-6)))))
     for i in range(args.warmup):
         pieces[i % len(pieces)][0]()
     times = [[] for _ in pieces]
     t_all = time.perf_counter()
     for i in range(args.steps):
         j = i % len(pieces)
-        t0 = time.perf_counter()
-        pieces[j][0]()
-        times[j].append(time.perf_counter() - t0)
+        for _ in range(reps[j]):
+            t0 = time.perf_counter()
+            pieces[j][0]()
+            times[j].append(time.perf_counter() - t0)
     dt = time.perf_counter() - t_all
     missing = [j for j, t in enumerate(times) if not t]
     for j in missing:  # fewer steps than pieces: time the rest once, outside the step count
@@ -652,7 +666,9 @@ def reference_arm(args, budget_s=90.0):
         times[j].append(time.perf_counter() - t0)
     step_s = sum(w * statistics.mean(t) for (_, w), t in zip(pieces, times))
     value = layers / step_s
-    sample = f"step i = piece i mod {len(pieces)} of one layer-step: {text}; {ORACLE_FORM}"
+    sample = (f"step i = piece i mod {len(pieces)} of one layer-step, run "
+              f"{'/'.join(str(r) for r in reps)} times per step (piece by piece): {text}; "
+              f"{ORACLE_FORM}")
     from oracle import cref as CR
     cpu = {"value": value, "unit": "layer-steps/s", "cores": CR.threads(), "kind": "oracle",
            "sample": sample}
@@ -1020,6 +1036,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-budget", type=float, default=90.0,
+                    help="--impl reference: seconds of oracle work over warm-up + timed steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="use only the first B sequences")
     ap.add_argument("--eager", action="store_true",
@@ -1028,7 +1046,7 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
-        return reference_arm(args)
+        return reference_arm(args, args.ref_budget)
     if args.workload == 9:
         return model_bench(args)
 
