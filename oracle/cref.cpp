@@ -143,6 +143,27 @@ void cref_quant_append_rows(const float* kv, const int64_t* pos, int64_t n, int3
   }
 }
 
+// The codecs over a range of fp32 bit patterns: for i in [first, first + n)
+// the value with bit pattern i, its E2M1 code and its E4M3 code (0xFF for
+// NaN patterns, which the encoders never receive).
+void cref_encode_range(uint64_t first, int64_t n, uint8_t* e2m1, uint8_t* e4m3,
+                       int32_t threads) {
+  parallel_for(n, threads, [&](int64_t lo, int64_t hi) {
+    for (int64_t i = lo; i < hi; ++i) {
+      const uint32_t bits = (uint32_t)(first + (uint64_t)i);
+      float x;
+      memcpy(&x, &bits, sizeof x);
+      if (isnan(x)) {
+        e2m1[i] = 0xFF;
+        e4m3[i] = 0xFF;
+        continue;
+      }
+      e2m1[i] = (uint8_t)e2m1_encode(x);
+      e4m3[i] = (uint8_t)e4m3_encode(x);
+    }
+  });
+}
+
 // ------------------------------------------------ step 2: indexer scores
 // s_t = sum_h w_h * max(0, sum_d q[h, d] k[t, d]) in fp64, q and k decoded
 // from E4M3 (k rows k_stride bytes apart).  Every product of two E4M3 values

@@ -43,6 +43,7 @@ def lib():
         P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_double
         L.cref_hardware_threads.restype = ctypes.c_int
         L.cref_quant_append_rows.argtypes = [P, P, I64, I32, P, P, I32, P, P]
+        L.cref_encode_range.argtypes = [ctypes.c_uint64, I64, P, P, I32]
         L.cref_index_scores.argtypes = [P, P, I32, I32, P, I64, I64, P, I32]
         L.cref_index_scores_mx.argtypes = [P, P, I32, I32, P, I64, P, I64, I64, P, I32]
         L.cref_block_maxima.argtypes = [P, I64, P]
@@ -51,7 +52,8 @@ def lib():
         L.cref_dequant_fp4.argtypes = [P, I64, P, I64, I64, I32, P]
         L.cref_decode_e4m3.argtypes = [P, I64, P]
         L.cref_attention.argtypes = [P, I32, I32, P, I64, D, P, I32]
-        for f in (L.cref_quant_append_rows, L.cref_index_scores, L.cref_index_scores_mx,
+        for f in (L.cref_quant_append_rows, L.cref_encode_range, L.cref_index_scores,
+                  L.cref_index_scores_mx,
                   L.cref_block_maxima, L.cref_dequant_fp4, L.cref_decode_e4m3,
                   L.cref_attention):
             f.restype = None
@@ -83,6 +85,15 @@ def quant_append_rows(kv, pos, cos_tab, sin_tab, rope_dim):
     lib().cref_quant_append_rows(_p(kv), _p(pos), n, d, _p(cos_tab), _p(sin_tab), rope_dim,
                                  _p(codes), _p(scales))
     return codes, scales
+
+
+def encode_range(first, n, nthreads=None):
+    """E2M1 and E4M3 codes of the fp32 values with bit patterns first ..
+    first + n - 1 (uint8 [n] each; 0xFF for NaN patterns)."""
+    e2 = np.empty(n, np.uint8)
+    e4 = np.empty(n, np.uint8)
+    lib().cref_encode_range(first, n, _p(e2), _p(e4), nthreads or threads())
+    return e2, e4
 
 
 def indexer_scores(q_codes, w, k_codes, nthreads=None):

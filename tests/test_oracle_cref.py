@@ -69,6 +69,29 @@ def test_quant_append_rows_bit_exact():
     assert np.array_equal(c1, c0) and np.array_equal(s1, s0)
 
 
+def test_encoders_on_bit_patterns():
+    """The C++ encoders equal the numpy ones on every fp32 bit pattern of a
+    few dense ranges (around 0, the E2M1 midpoints, the E4M3 subnormal and
+    saturation edges) and on random patterns; NaN patterns give 0xFF."""
+    rng = np.random.default_rng(11)
+    starts = [0, 0x80000000, 0x3E800000 - 4096, 0x3F400000 - 4096, 0x40A00000 - 4096,
+              0x3B000000 - 4096, 0x43E00000 - 4096, 0x7F800000 - 4096]
+    for first in starts:
+        e2, e4 = C.encode_range(first, 8192)
+        x = (np.arange(first, first + 8192, dtype=np.uint64) & 0xFFFFFFFF).astype(
+            np.uint32).view(np.float32)
+        ok = ~np.isnan(x)
+        assert np.array_equal(e2[ok], F.e2m1_encode(x[ok]))
+        assert np.array_equal(e4[ok], F.e4m3_encode(x[ok]))
+        assert np.all(e2[~ok] == 0xFF) and np.all(e4[~ok] == 0xFF)
+    bits = rng.integers(0, 2 ** 32, 20000, dtype=np.uint64)
+    for b in bits[:200]:
+        e2, e4 = C.encode_range(int(b), 1)
+        x = np.array([int(b)], np.uint32).view(np.float32)
+        if not np.isnan(x[0]):
+            assert e2[0] == F.e2m1_encode(x)[0] and e4[0] == F.e4m3_encode(x)[0]
+
+
 def test_e4m3_decode_all_codes():
     codes = np.arange(256, dtype=np.uint8)
     assert np.array_equal(C.e4m3_decode(codes), F.e4m3_decode(codes), equal_nan=True)
