@@ -14,6 +14,10 @@ It is written to be read against the pages it follows, in plain numpy:
 * ``csa2`` -- the five steps of the path: RoPE then FP4 quantisation of main-KV
   rows, lightning-indexer scores, top-k selection with the block pool,
   dequantisation, and one softmax over the selected rows and the SWA window.
+* ``workload`` -- the reference results of one sequence of a seeded workload.
+* ``cref`` -- the same definitions restated in plain C++ (``cref.cpp``, one
+  thread per host core), pinned against ``csa2`` and ``formats``; the timed
+  CPU baseline, and the oracle side of the exhaustive codec sweep.
 
 Floating point is fp64 except where the method's fp32 arithmetic decides an
 integer (the RoPE rotation, the FP4 scale and code choice): there the oracle

@@ -51,3 +51,17 @@ def test_reference_arm_ragged_mixed_modes():
     sample = d["cpu_baseline"]["sample"]
     assert "Full:" in sample and "Reindex:" in sample and "Reuse:" in sample
     assert wall < 400
+
+
+def test_cpu_baseline_times_the_cpp_oracle():
+    """The GPU arm's cpu_baseline: the C++ oracle's pieces in rounds until
+    the target time is sampled; cores = the oracle's thread count."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from oracle import cref
+    from synth.workloads import get_workload
+    r = bench.cpu_baseline(get_workload(1), target_s=0.3)
+    assert r["kind"] == "oracle" and r["unit"] == "layer-steps/s" and r["value"] > 0
+    assert r["cores"] == cref.threads()
+    assert r["seconds_sampled"] >= 0.3
+    assert "C++ oracle" in r["sample"] and "rounds" in r["sample"]
