@@ -1299,6 +1299,10 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
+        # the oracle's wall time per layer-step and the path bytes it covers per second
+        per_layer_step = statistics.mean(roof_bytes) / layers_per_step(wl)
+        cpu["ms_per_layer_step"] = 1e3 / cpu["value"]
+        cpu["path_gbs"] = cpu["value"] * per_layer_step / 1e9
     if rank == 0:
         line = {
             "metric": ("CSA2 decode layer-steps/s (achieved HBM GB/s vs GB300 peak in roofline)"
