@@ -447,8 +447,7 @@ def roofline_bytes_per_step(wl, n_at):
 
 # ------------------------------------------------------------- CPU baseline
 ORACLE_FORM = ("the C++ oracle (oracle/cref.cpp: fp64 loops, one thread per core, pinned "
-               "against the numpy oracle); the m = 2 pair combination of encoder entries "
-               "stays numpy")
+               "against the numpy oracle); the seeded inputs come from the numpy generators")
 def cpu_baseline(wl, per_piece_s=2.0, target_s=10.0, max_rounds=200):
     """The oracle on the host cores over one bounded sample of the workload's
     layer-step: the pieces of oracle_plan (the same plan the reference arm

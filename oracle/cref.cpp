@@ -143,6 +143,43 @@ void cref_quant_append_rows(const float* kv, const int64_t* pos, int64_t n, int3
   }
 }
 
+// ----------------------------------------- step 1b: m = 2 pair compression
+// e^x for fp32 x <= 0, one fp32 rounding per operation, 0 below -80:
+// k = rint(x / ln 2), r = (x - k ln2_hi) - k ln2_lo (ln2_hi = 2839/4096 has 12
+// significant bits, so k ln2_hi is exact), e^r by Horner on the degree-7
+// Taylor polynomial, times 2^k (k >= -116 keeps the result normal).
+float exp_neg_f32(float x) {
+  const float inv_ln2 = (float)(1.0 / 0.6931471805599453);
+  const float ln2_hi = (float)(2839.0 / 4096.0);
+  const float ln2_lo = (float)(0.6931471805599453 - 2839.0 / 4096.0);
+  if (x < -80.0f) return 0.0f;
+  const float k = rintf(x * inv_ln2);
+  const float r = (x - k * ln2_hi) - k * ln2_lo;
+  static const double fact[8] = {1.0, 1.0, 2.0, 6.0, 24.0, 120.0, 720.0, 5040.0};
+  float p = (float)(1.0 / fact[7]);
+  for (int i = 6; i >= 0; --i) p = p * r + (float)(1.0 / fact[i]);
+  return ldexpf(p, (int)k);
+}
+
+// Source rows kv [2T, D] and their logits z [2T, D] -> T compressed rows:
+// per channel, with d = z1 - z0 and t = e^-|d|, the larger logit's row gets
+// 1 / (1 + t) and the other t / (1 + t) (a softmax over the pair);
+// c = w0 x0 + w1 x1, each operation one fp32 rounding.
+void cref_compress_pairs(const float* kv, const float* z, int64_t T, int32_t D, float* out) {
+  for (int64_t j = 0; j < T; ++j)
+    for (int c = 0; c < D; ++c) {
+      const float z0 = z[(2 * j) * D + c], z1 = z[(2 * j + 1) * D + c];
+      const float d = z1 - z0;
+      const float t = exp_neg_f32(-fabsf(d));
+      const float s = 1.0f + t;
+      const float big = 1.0f / s, small = t / s;
+      const float w0 = d >= 0.0f ? small : big;
+      const float w1 = d >= 0.0f ? big : small;
+      const float a = w0 * kv[(2 * j) * D + c], b = w1 * kv[(2 * j + 1) * D + c];
+      out[j * D + c] = a + b;
+    }
+}
+
 // The codecs over a range of fp32 bit patterns: for i in [first, first + n)
 // the value with bit pattern i, its E2M1 code and its E4M3 code (0xFF for
 // NaN patterns, which the encoders never receive).

@@ -44,6 +44,7 @@ def lib():
         L.cref_hardware_threads.restype = ctypes.c_int
         L.cref_quant_append_rows.argtypes = [P, P, I64, I32, P, P, I32, P, P]
         L.cref_encode_range.argtypes = [ctypes.c_uint64, I64, P, P, I32]
+        L.cref_compress_pairs.argtypes = [P, P, I64, I32, P]
         L.cref_index_scores.argtypes = [P, P, I32, I32, P, I64, I64, P, I32]
         L.cref_index_scores_mx.argtypes = [P, P, I32, I32, P, I64, P, I64, I64, P, I32]
         L.cref_block_maxima.argtypes = [P, I64, P]
@@ -52,7 +53,8 @@ def lib():
         L.cref_dequant_fp4.argtypes = [P, I64, P, I64, I64, I32, P]
         L.cref_decode_e4m3.argtypes = [P, I64, P]
         L.cref_attention.argtypes = [P, I32, I32, P, I64, D, P, I32]
-        for f in (L.cref_quant_append_rows, L.cref_encode_range, L.cref_index_scores,
+        for f in (L.cref_quant_append_rows, L.cref_encode_range, L.cref_compress_pairs,
+                  L.cref_index_scores,
                   L.cref_index_scores_mx,
                   L.cref_block_maxima, L.cref_dequant_fp4, L.cref_decode_e4m3,
                   L.cref_attention):
@@ -85,6 +87,16 @@ def quant_append_rows(kv, pos, cos_tab, sin_tab, rope_dim):
     lib().cref_quant_append_rows(_p(kv), _p(pos), n, d, _p(cos_tab), _p(sin_tab), rope_dim,
                                  _p(codes), _p(scales))
     return codes, scales
+
+
+def compress_pairs(kv, z):
+    """As ``csa2.compress_pairs``: source rows [2T, D] and logits [2T, D] ->
+    T compressed rows (fp32)."""
+    kv, z = _c(kv, np.float32), _c(z, np.float32)
+    t2, d = kv.shape
+    out = np.zeros((t2 // 2, d), np.float32)
+    lib().cref_compress_pairs(_p(kv), _p(z), t2 // 2, d, _p(out))
+    return out
 
 
 def encode_range(first, n, nthreads=None):

@@ -45,7 +45,7 @@ class SeqRef:
             src = np.stack([2 * positions, 2 * positions + 1], axis=1).reshape(-1)
             x = host_rows_normal(self.wl.seed, synth.T_KV, self.b, src, self.wl.dim, self.mult)
             z = host_rows_normal(self.wl.seed, synth.T_Z, self.b, src, self.wl.dim) * np.float32(2.0)
-            x = O.compress_pairs(x, z)
+            x = (CR if self.cpp else O).compress_pairs(x, z)
         else:
             x = host_rows_normal(self.wl.seed, synth.T_KV, self.b, positions, self.wl.dim, self.mult)
         qa = CR.quant_append_rows if self.cpp else O.quant_append_rows

@@ -92,6 +92,22 @@ def test_encoders_on_bit_patterns():
             assert e2[0] == F.e2m1_encode(x)[0] and e4[0] == F.e4m3_encode(x)[0]
 
 
+def test_compress_pairs_bit_exact():
+    """The m = 2 pair combination, logits at the exponential's edges
+    (equal, +-0 apart, tiny, around the -80 cut, huge) and random."""
+    rng = np.random.default_rng(13)
+    t, d = 64, 576
+    x = (rng.standard_normal((2 * t, d)) * 3).astype(np.float32)
+    z0 = (rng.standard_normal((t, d)) * 4).astype(np.float32)
+    diffs = np.array([0.0, -0.0, 1e-7, -1e-7, 1e-3, 79.9, 80.0, 80.1, -80.2, 200.0, -1e30, 0.5],
+                     np.float32)
+    dd = diffs[rng.integers(0, len(diffs), (t, d))]
+    dd[:8] = (rng.standard_normal((8, d)) * 10).astype(np.float32)
+    z = np.empty((2 * t, d), np.float32)
+    z[0::2], z[1::2] = z0, (z0 + dd).astype(np.float32)
+    assert np.array_equal(C.compress_pairs(x, z), O.compress_pairs(x, z))
+
+
 def test_e4m3_decode_all_codes():
     codes = np.arange(256, dtype=np.uint8)
     assert np.array_equal(C.e4m3_decode(codes), F.e4m3_decode(codes), equal_nan=True)
