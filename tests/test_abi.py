@@ -71,6 +71,12 @@ def test_host_validation_without_gpu(lib):
     r = K._attn_decode_layers(ctypes.byref(c), 2, ptrs, 64, 16, 16, 64, ptrs, None, 128, 0.0,
                               holes, 16, None)
     assert r == K.CSA2_ERR_INVALID
+    # layers x rows beyond the grid's y extent (65,535) is refused on the host
+    big = K.Csa2Cache.from_buffer_copy(c)
+    big.batch = 16384
+    r = K._attn_decode_layers(ctypes.byref(big), 4, ptrs, 64, 16, 16, 64, ptrs, None, 128, 0.0,
+                              ptrs, 16, None)
+    assert r == K.CSA2_ERR_INVALID
     assert K.entry_bytes(512) == 288 and K.entry_bytes(576) == 324
     assert K.status_string(K.CSA2_ERR_INVALID) == "invalid argument"
 
